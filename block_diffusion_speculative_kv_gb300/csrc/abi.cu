@@ -1,0 +1,150 @@
+// C ABI of the drafting library: argument validation, workspace layout and
+// kernel launches.  Declarations and contracts are in include/dflash.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dfl {
+
+namespace {
+thread_local char g_err[1024] = "";
+}
+
+dflash_status set_error(dflash_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+dflash_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DFLASH_OK;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+size_t ws_header_bytes() { return 256; }
+
+}  // namespace dfl
+
+using namespace dfl;
+
+#define DFL_REQUIRE(cond, ...)                                   \
+  do {                                                           \
+    if (!(cond)) return set_error(DFLASH_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+extern "C" {
+
+const char* dflash_last_error(void) { return g_err; }
+int dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
+
+dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  DFL_REQUIRE(ws != nullptr && ws_bytes >= ws_header_bytes(), "workspace missing or too small");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error(DFLASH_ERR_CUDA, "workspace init: %s", cudaGetErrorString(e));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_read_status(void* ws, int* device_status, void* stream) {
+  DFL_REQUIRE(ws != nullptr && device_status != nullptr, "null argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  if (e != cudaSuccess) return set_error(DFLASH_ERR_CUDA, "read status: %s", cudaGetErrorString(e));
+  *device_status = host;
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Step a6 standalone: log-softmax + top-K over given logits.
+// ---------------------------------------------------------------------------
+size_t dflash_topk_workspace_bytes(int rows, int vocab, int K) {
+  if (rows < 0 || vocab <= 0 || K < 1 || K > 32) return 0;
+  return ws_header_bytes() + align_up(sizeof(int) * (size_t)rows, 256) +
+         topk_part_bytes(rows, 32);
+}
+
+dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
+                                 int K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  DFL_REQUIRE(rows >= 0, "rows must be >= 0");
+  DFL_REQUIRE(vocab >= 1 && ld >= vocab, "need 1 <= vocab <= ld");
+  DFL_REQUIRE(K >= 1 && K <= 32 && K <= vocab, "need 1 <= K <= min(32, vocab)");
+  DFL_REQUIRE(dtype == DFLASH_F32 || dtype == DFLASH_BF16, "dtype must be F32 or BF16");
+  if (rows == 0) return DFLASH_OK;
+  DFL_REQUIRE(logits && ids && logp, "null logits/ids/logp");
+  const size_t need = dflash_topk_workspace_bytes(rows, vocab, K);
+  if (ws == nullptr || ws_bytes < need)
+    return set_error(DFLASH_ERR_WORKSPACE, "top-K workspace needs %zu bytes, got %zu", need,
+                     ws_bytes);
+  char* w = static_cast<char*>(ws);
+  TopkLaunch a{};
+  a.logits = logits; a.rows = rows; a.vocab = vocab; a.ld = ld; a.dtype = dtype; a.K = K;
+  a.splits = topk_splits(rows, vocab);
+  a.counters = reinterpret_cast<int*>(w + ws_header_bytes());
+  a.part = reinterpret_cast<float*>(w + ws_header_bytes() +
+                                    align_up(sizeof(int) * (size_t)rows, 256));
+  a.ids = ids; a.logp = logp;
+  launch_topk(a, static_cast<cudaStream_t>(stream));
+  return check_launch("logits_topk");
+}
+
+// ---------------------------------------------------------------------------
+// Step a7: DDTree build.  Step a8: verifier walk.
+// ---------------------------------------------------------------------------
+dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_logp,
+                           const int32_t* topk_ids, const int32_t* root_tok, int32_t* n_nodes,
+                           int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
+                           uint32_t* mask, void* stream) {
+  DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
+  DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
+  DFL_REQUIRE(K >= 1 && K <= 32, "need 1 <= K <= 32");
+  DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
+  if (n_req == 0) return DFLASH_OK;
+  DFL_REQUIRE(topk_logp && topk_ids && root_tok && n_nodes && tok && parent && depth && rank &&
+                  mask,
+              "null pointer argument");
+  TreeBuildLaunch a{n_req, D, K, B, topk_logp, topk_ids, root_tok, n_nodes, tok, parent,
+                    depth, rank, mask};
+  launch_tree_build(a, static_cast<cudaStream_t>(stream));
+  return check_launch("ddtree_build");
+}
+
+dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes, const int32_t* tok,
+                            const int32_t* parent, const int32_t* target_tok,
+                            int32_t* accept_len, int32_t* accepted, int32_t* bonus,
+                            void* stream) {
+  DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
+  DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
+  DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
+  if (n_req == 0) return DFLASH_OK;
+  DFL_REQUIRE(n_nodes && tok && parent && target_tok && accept_len && accepted && bonus,
+              "null pointer argument");
+  TreeAcceptLaunch a{n_req, D, B, n_nodes, tok, parent, target_tok, accept_len, accepted, bonus};
+  launch_tree_accept(a, static_cast<cudaStream_t>(stream));
+  return check_launch("ddtree_accept");
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Internal launch interface between the C ABI layer (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace dfl {
+
+// ---- log-softmax + top-K (topk.cu) ----
+struct TopkLaunch {
+  const void* logits;
+  int rows, vocab;
+  long long ld;
+  int dtype;      // DFLASH_F32 / DFLASH_BF16
+  int K;          // <= 32
+  int splits;     // <= 32; 1 = one CTA per row, no partial records
+  float* part;    // [rows][splits][2 + 2*32] when splits > 1
+  int* counters;  // [rows], zero on entry, left zero on exit
+  int32_t* ids;
+  float* logp;
+};
+int topk_splits(int rows, int vocab);
+size_t topk_part_bytes(int rows, int splits);
+void launch_topk(const TopkLaunch& a, cudaStream_t st);
+
+// ---- DDTree (ddtree.cu) ----
+struct TreeBuildLaunch {
+  int n_req, D, K, B;
+  const float* topk_logp;
+  const int32_t* topk_ids;
+  const int32_t* root_tok;
+  int32_t* n_nodes;
+  int32_t* tok;
+  int32_t* parent;
+  int32_t* depth;
+  int32_t* rank;
+  uint32_t* mask;
+};
+size_t tree_build_smem_bytes(int D, int K, int B);
+void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st);
+
+struct TreeAcceptLaunch {
+  int n_req, D, B;
+  const int32_t* n_nodes;
+  const int32_t* tok;
+  const int32_t* parent;
+  const int32_t* target;
+  int32_t* accept_len;
+  int32_t* accepted;
+  int32_t* bonus;
+};
+void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st);
+
+}  // namespace dfl

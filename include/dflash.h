@@ -1,0 +1,261 @@
+/*
+ * dflash.h - C ABI of the block-diffusion speculative drafting library
+ * (DFlash drafter + DDTree draft trees) for one NVIDIA GB300 (sm_103a).
+ *
+ * One drafter cycle is four calls, in the order the pages describe a round:
+ *
+ *   dflash_inject_kv    project the target's fused hidden features into every
+ *                       drafter layer's KV cache
+ *                       ("DFlash: Block Diffusion for Flash Speculative Decoding",
+ *                       section 3.4.3, feature fusion and KV injection);
+ *   dflash_draft_block  one parallel pass of the drafter over
+ *                       [anchor, mask x (L-1)], LM head, log-softmax and top-K
+ *                       (same page, section 3.4.4; "Accelerating Speculative
+ *                       Decoding with Block Diffusion Draft Trees", section 3.4.2);
+ *   ddtree_build        Algorithm 1: the best-first heap over rank tuples, with
+ *                       the flattened tree, depth position ids and the ancestor
+ *                       attention mask (DDTree page, sections 3.4.4-3.4.5);
+ *   ddtree_accept       the verifier walk against the target's token choices
+ *                       (DDTree page, section 3.4.5).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Memory: every tensor argument is a DEVICE pointer unless marked "host".
+ *   The caller owns all memory.  The library never allocates device memory;
+ *   scratch space comes from a caller-provided workspace (see
+ *   dflash_workspace_bytes).  The only host allocation is the model handle.
+ * - Layout: row-major, innermost index last, densely packed unless a leading
+ *   dimension is given.  "T" below is the model dtype: fp32 (DFLASH_F32) or
+ *   bf16 (DFLASH_BF16, IEEE-754 binary32 truncated to its top 16 bits, round to
+ *   nearest even when produced here).
+ * - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *   call only enqueues work on it and returns; nothing synchronises.  Calls are
+ *   capturable into a CUDA graph (no allocation, no host synchronisation).
+ * - Errors: arguments are validated on the host before anything is enqueued; a
+ *   rejected call returns non-zero, enqueues nothing and leaves outputs
+ *   untouched.  DFLASH_ERR_CUDA means a launch failed (the CUDA error string is
+ *   in dflash_last_error()).  Problems found on the device (a bounded wait that
+ *   ran out) are recorded in the workspace status word, read with
+ *   dflash_read_status.  dflash_last_error() returns a thread-local message for
+ *   the last non-OK status of the calling thread.
+ * - Concurrency: calls that share a workspace must be ordered on one stream.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_ABI_VERSION 1
+#define DFLASH_MAX_LAYERS 16
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,   /* null pointer, bad size, unsupported shape    */
+  DFLASH_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement  */
+  DFLASH_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required   */
+  DFLASH_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed            */
+  DFLASH_ERR_TIMEOUT = 5        /* device-side bounded wait expired (status word)*/
+} dflash_status;
+
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+
+/* Drafter shape and the readings the pages leave open.
+ * - Pre-norm RMSNorm: x / sqrt(mean(x^2) + rms_eps) * gain, before attention,
+ *   before the MLP and before the LM head; SwiGLU MLP; no biases.
+ * - Rotary embedding (rotate-half, base rope_theta) on queries and keys at
+ *   absolute positions: cache slot t has position t, block row j of a request
+ *   whose context holds ctx_len entries has position ctx_len + j.
+ * - anchor_sees_block = 1: every block row attends to the whole context and the
+ *   whole block (bidirectional block).  0: the anchor row attends only to the
+ *   context and itself, as the DFlash page's attention bullet list states.
+ * Supported: 1 <= n_layers <= 16; head_dim in {64, 128}; n_q % n_kv == 0;
+ * bf16 models need d, d_feat*n_feat, n_q*head_dim and d_ff multiples of 128
+ * (every GEMM reduction dimension a multiple of 64). */
+typedef struct {
+  int n_layers;
+  int d;            /* hidden size; also the fused feature size            */
+  int n_q;          /* query heads                                         */
+  int n_kv;         /* key/value heads                                     */
+  int head_dim;
+  int d_ff;         /* SwiGLU inner size                                   */
+  int vocab;
+  int n_feat;       /* target layers whose hidden states are concatenated  */
+  int d_feat;       /* target hidden size                                  */
+  int dtype;        /* dflash_dtype                                        */
+  float rope_theta;
+  float rms_eps;
+  int mask_id;      /* token id of the mask token, 0 <= mask_id < vocab    */
+  int anchor_sees_block;
+} dflash_dims;
+
+/* Device pointers to the drafter weights (type T unless noted), in the packed
+ * layouts the kernels stream.  [out][in] matrices are the usual y = W x form.
+ *   w_proj      [d][n_feat*d_feat]        fusion projection W_proj
+ *   embed       [vocab][d]                token embedding (shared with target)
+ *   lm_head     [vocab][d]                LM head (shared with target)
+ *   final_norm  [d]                       gain of the norm before the LM head
+ *   u_kv        [n_layers][2][n_kv*head_dim][d]
+ *                                         injection projections: per layer
+ *                                         U_K rows, then U_V rows
+ *   per layer l < n_layers:
+ *   attn_norm   [d]
+ *   w_qkv       [(n_q + 2*n_kv)*head_dim][d]   rows of W_q, then W_k, then W_v
+ *   wo          [d][n_q*head_dim]
+ *   mlp_norm    [d]
+ *   w_gate_up   [2*d_ff][d]               interleaved: row 2j = gate row j,
+ *                                         row 2j+1 = up row j
+ *   w_down      [d][d_ff]
+ * All pointers 16-byte aligned.  The weights must stay valid and unchanged for
+ * the lifetime of a dflash_model built from them. */
+typedef struct {
+  const void* w_proj;
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* u_kv;
+  const void* attn_norm[DFLASH_MAX_LAYERS];
+  const void* w_qkv[DFLASH_MAX_LAYERS];
+  const void* wo[DFLASH_MAX_LAYERS];
+  const void* mlp_norm[DFLASH_MAX_LAYERS];
+  const void* w_gate_up[DFLASH_MAX_LAYERS];
+  const void* w_down[DFLASH_MAX_LAYERS];
+} dflash_weights;
+
+/* The drafter's injected-context KV cache (DFlash page, 3.4.3: the projected
+ * features are stored in the drafter's KV cache and reused across cycles).
+ * Per layer l: k[l], v[l] are T [n_req][n_kv][cap][head_dim]; slot t of a
+ * request holds the entry injected for position t (keys already rotated at t).
+ * Written by dflash_inject_kv, read by dflash_draft_block. */
+typedef struct {
+  void* k[DFLASH_MAX_LAYERS];
+  void* v[DFLASH_MAX_LAYERS];
+  int n_req;
+  int cap;
+} dflash_cache;
+
+/* Opaque model handle: the dims, the weight pointers and the TMA descriptors
+ * built for them once.  Host memory only. */
+typedef struct dflash_model dflash_model;
+
+/* Build a model handle.  Validates dims and weight pointers (non-null, 16-byte
+ * aligned).  Returns DFLASH_ERR_INVALID_ARG / DFLASH_ERR_UNSUPPORTED on a bad
+ * or unsupported shape, DFLASH_ERR_CUDA if the TMA descriptors cannot be
+ * encoded.  *out is set only on success; free it with dflash_model_destroy. */
+dflash_status dflash_model_create(const dflash_dims* dims, const dflash_weights* weights,
+                                  dflash_model** out);
+void dflash_model_destroy(dflash_model* model);
+
+/* Workspace bytes for calls on this model with at most n_req requests,
+ * max_inject_rows feature rows per dflash_inject_kv call, block length L <= 16
+ * and top-K K <= 32.  The same workspace also serves dflash_logits_topk for up
+ * to n_req*(L-1) rows of this model's vocabulary.  0 on invalid arguments. */
+size_t dflash_workspace_bytes(const dflash_model* model, int n_req, int max_inject_rows,
+                              int L, int K);
+
+/* Zero a workspace (its status word and arrival counters).  Required once before
+ * first use, and again after a call reported a device-side error. */
+dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Read (synchronously) and clear the device status word of a workspace:
+ * *device_status receives DFLASH_OK or the first device-side error recorded. */
+dflash_status dflash_read_status(void* ws, int* device_status, void* stream);
+
+/* Step a1 + a2: KV injection (DFlash page, 3.4.3).
+ * For each request r and each of its feature rows i (global row
+ * row_off[r] + i, i < row_off[r+1] - row_off[r]):
+ *   f       = W_proj * feats[row]                       (fusion, no norm)
+ *   K_l,pos = RoPE(U_K,l f, pos),  V_l,pos = U_V,l f    for every layer l
+ * stored at cache slot pos = pos0[r] + i of request r.
+ *   row_off  int32 [n_req+1] (device) prefix offsets, row_off[0] = 0,
+ *            row_off[n_req] = n_rows
+ *   pos0     int32 [n_req]   (device) first cache slot written per request;
+ *            pos0[r] + rows of r must not exceed cache->cap (not checked on
+ *            the device: the caller guarantees it)
+ *   feats    T [n_rows][n_feat*d_feat] (device)
+ * n_rows may be 0 (nothing is enqueued).  Overwrites only the addressed slots. */
+dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* cache,
+                               int n_req, int n_rows, const int32_t* row_off,
+                               const int32_t* pos0, const void* feats,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Steps a3 - a6: one drafter pass over the block [anchor, mask x (L-1)] of each
+ * request, then per-position log-softmax and top-K (DFlash page, 3.4.4; DDTree
+ * page, 3.4.2: q_i = softmax(l_i)).
+ *   anchor    int32 [n_req] (device) the bonus token of each request
+ *   ctx_len   int32 [n_req] (device) context entries of each request in the
+ *             cache, 0 <= ctx_len[r] <= max_ctx <= cache->cap
+ *   max_ctx   host bound on ctx_len used to size the attention grid
+ *   L         block length, 2 <= L <= 16; D = L-1 draft positions
+ *   K         1 <= K <= 32 (and K <= vocab)
+ *   topk_ids  int32 [n_req][L-1][K] (device) out: token ids by (logit desc,
+ *             id asc)
+ *   topk_logp fp32  [n_req][L-1][K] (device) out: logit - logsumexp(row)
+ *   logits    fp32  [n_req][L-1][vocab] (device) out, optional (NULL skips)
+ */
+dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache,
+                                 int n_req, const int32_t* anchor, const int32_t* ctx_len,
+                                 int max_ctx, int L, int K, int32_t* topk_ids,
+                                 float* topk_logp, float* logits,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Step a6 on its own: log-softmax + top-K over given logits rows (DDTree page,
+ * 3.4.2 and Lemma 1 in 3.4.4: only the top-K tokens per depth are needed).
+ *   logits  [rows][ld] of dtype (DFLASH_F32 or DFLASH_BF16), vocab <= ld
+ *   ids     int32 [rows][K], logp fp32 [rows][K] (device) out; order is
+ *           (logit desc, token id asc); logp = logit - logsumexp over the row
+ * Requires 1 <= K <= 32, K <= vocab, rows >= 0; ws of at least
+ * dflash_topk_workspace_bytes(rows, vocab, K) bytes (zero-initialised once). */
+size_t dflash_topk_workspace_bytes(int rows, int vocab, int K);
+dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
+                                 int K, int32_t* ids, float* logp,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Step a7: DDTree tree construction, Algorithm 1 (DDTree page, 3.4.4), plus the
+ * flattened tree and its ancestor-only mask (3.4.5).  Per request r:
+ *   topk_logp fp32 [n_req][D][K] log q of the rank-k token at depth d+1,
+ *             descending along k; topk_ids int32 [n_req][D][K] its token id
+ *   root_tok  int32 [n_req] the bonus token (tree root)
+ * Outputs (device), width W1 = B+1 nodes per request, node 0 = root, nodes
+ * 1..n in pop order:
+ *   n_nodes   int32 [n_req]        n = min(B, number of prefixes available)
+ *   tok       int32 [n_req][B+1]   token of the node (root: root_tok)
+ *   parent    int32 [n_req][B+1]   parent node index (root: -1)
+ *   depth     int32 [n_req][B+1]   depth = position id (root: 0)
+ *   rank      int32 [n_req][B+1]   1-based rank of the node's token (root: 0)
+ *   mask      uint32 [n_req][B+1][ceil((B+1)/32)] bit j of row i set iff node
+ *             j is node i or an ancestor of it
+ * Entries past node n are -1 (mask rows 0).  Scores: the candidate score is the
+ * parent's score plus logp, one fp32 add; the heap pops the highest score and,
+ * on equal scores, the candidate created first (each pop creates its next
+ * sibling before its first child).  Requires 0 <= B <= 1024, 1 <= K <= 32,
+ * 1 <= D <= 16.  Needs no workspace. */
+dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_logp,
+                           const int32_t* topk_ids, const int32_t* root_tok,
+                           int32_t* n_nodes, int32_t* tok, int32_t* parent,
+                           int32_t* depth, int32_t* rank, uint32_t* mask, void* stream);
+
+/* Step a8: greedy verifier walk (DDTree page, 3.4.5).  From the root, while the
+ * current node has a child whose token equals target_tok[current], move to it.
+ *   target_tok int32 [n_req][B+1]  the target's choice at every node
+ *   accept_len int32 [n_req]       accepted draft tokens (tau = accept_len + 1)
+ *   accepted   int32 [n_req][D]    accepted node indices, -1 padded
+ *   bonus      int32 [n_req]       target_tok at the node where the walk stops
+ * Tree arrays as produced by ddtree_build with the same B. */
+dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes,
+                            const int32_t* tok, const int32_t* parent,
+                            const int32_t* target_tok, int32_t* accept_len,
+                            int32_t* accepted, int32_t* bonus, void* stream);
+
+/* Thread-local message for the calling thread's last non-OK status. */
+const char* dflash_last_error(void);
+int dflash_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

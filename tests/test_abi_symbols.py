@@ -1,0 +1,56 @@
+"""The C-ABI library builds, loads without a GPU, and exports every function
+include/dflash.h declares; the binding wraps each of them.  No compute calls."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_diffusion_speculative_kv_gb300 import binding, build
+
+HEADER = os.path.join(build.ROOT, "include", "dflash.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keep = [n for n in names if n.startswith(("dflash_", "ddtree_"))]
+    return sorted(set(keep))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    return build.build()
+
+
+def test_header_declares_the_path_calls():
+    d = _declared()
+    for name in ("dflash_inject_kv", "dflash_draft_block", "ddtree_build", "ddtree_accept",
+                 "dflash_logits_topk", "dflash_model_create", "dflash_workspace_bytes"):
+        assert name in d
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol(libpath):
+    assert sorted(binding.exported_symbols()) == _declared()
+    lib = binding.lib()
+    assert lib.dflash_abi_version() == 1
+
+
+def test_host_validation_needs_no_gpu(libpath):
+    lib = binding.lib()
+    # invalid budget and depth are rejected before anything touches the device
+    assert lib.ddtree_build(1, 0, 8, 64, *([None] * 9), None) == 1
+    assert lib.ddtree_build(1, 8, 8, 2000, *([None] * 9), None) == 1
+    assert lib.ddtree_build(1, 8, 40, 64, *([None] * 9), None) == 1
+    assert b"K" in lib.dflash_last_error()
+    assert lib.dflash_logits_topk(4, 100, 50, 1, None, 8, None, None, None, 0, None) == 1
+    assert lib.dflash_topk_workspace_bytes(4, 100, 0) == 0
+    # zero-sized requests are valid no-ops
+    assert lib.ddtree_build(0, 8, 8, 64, *([None] * 9), None) == 0
