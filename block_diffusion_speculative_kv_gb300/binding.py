@@ -72,6 +72,8 @@ _SIGS = {
     "dflash_logits_topk": (_i, [_i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "ddtree_build": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ddtree_accept": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_linear_workspace_bytes": (_sz, [_i, _i, _i]),
+    "dflash_linear_bf16": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -152,6 +154,22 @@ def logits_topk(logits: torch.Tensor, K: int, ids: torch.Tensor, logp: torch.Ten
     vocab = ld if vocab is None else vocab
     _check(lib().dflash_logits_topk(rows, vocab, ld, _dtype_code(logits), _ptr(logits), K,
                                     _ptr(ids), _ptr(logp), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# The dense contraction on its own
+# ---------------------------------------------------------------------------
+
+def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().dflash_linear_workspace_bytes(M, N, K))
+
+
+def linear_bf16(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor, ws: torch.Tensor, stream=None):
+    """Y = X . W^T (bf16 in, fp32 out) on the tensor cores."""
+    M, K = X.shape
+    N = W.shape[0]
+    _check(lib().dflash_linear_bf16(M, N, K, _ptr(X), _ptr(W), _ptr(Y), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -1,0 +1,444 @@
+// Block attention of the drafter (step a4, attention part).
+//
+// "DFlash: Block Diffusion for Flash Speculative Decoding", section 3.4.4: the
+// block's queries attend bidirectionally within the block and to the target
+// context injected into the layer's KV cache (section 3.4.3).  With grouped
+// query attention, the G = n_q / n_kv query heads of a KV head share its keys,
+// so a KV head's work is G * L query rows (64 for 32/8 heads and L = 16).
+//
+// bf16 path (split-KV, HBM-bound): grid (chunk, kv head, request).  Chunk c <
+// n_chunks covers context positions [c*chunk, (c+1)*chunk) of the request
+// (empty chunks past ctx_len exit at once); the last chunk holds the block's
+// own L keys.  A CTA keeps its query rows in shared memory, streams 64-key
+// tiles of K and V through a double-buffered cp.async ring (XOR-swizzled 16 B
+// chunks, conflict-free for ldmatrix), computes S = Q K^T and O += P V with
+// bf16 mma.sync (fp32 accumulators) and an online softmax in base 2, and
+// writes an unnormalised partial (O, running max, running sum).  A second
+// kernel merges the partials of each (request, KV head) with the usual
+// log-sum-exp rescaling and writes bf16 outputs.
+//
+// fp32 path: one warp per query row, lanes over the head dimension, every key
+// in turn with an online softmax (used for fp32 models).
+#include "attention.h"
+#include "common.cuh"
+
+#include <math_constants.h>
+
+namespace dfl {
+
+namespace {
+
+constexpr int kKeyTile = 64;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of 16-byte chunk `ch` of row `row` in a [rows][HD] bf16 tile.
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int ch) {
+  return static_cast<uint32_t>(row * (HD * 2) + ((ch ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_split_kernel(const AttnParams p) {
+  constexpr int NCH = HD / 8;  // 16-byte chunks per row
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int QR = p.G * p.L;
+  const int QRp = (QR + 15) / 16 * 16;
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + QRp * HD * 2;
+  uint8_t* sV = sK + 2 * kKeyTile * HD * 2;
+
+  const int chunk_id = blockIdx.x;
+  const int g = blockIdx.y;
+  const int req = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const bool is_block = chunk_id == p.n_chunks;
+  const int ctx = min(max(p.ctx_len[req], 0), p.cap);  // never read past the cache slab
+  int k_begin, k_end;
+  if (is_block) { k_begin = 0; k_end = p.L; }
+  else { k_begin = chunk_id * p.chunk; k_end = min(ctx, k_begin + p.chunk); }
+
+  const size_t part_row0 = (((size_t)req * p.n_kv + g) * (p.n_chunks + 1) + chunk_id) * QR;
+  if (k_end <= k_begin) {
+    for (int r = tid; r < QR; r += blockDim.x) {
+      p.part_ml[(part_row0 + r) * 2 + 0] = -CUDART_INF_F;
+      p.part_ml[(part_row0 + r) * 2 + 1] = 0.f;
+    }
+    return;
+  }
+
+  const __nv_bfloat16* kbase;
+  const __nv_bfloat16* vbase;
+  long long kv_ld;
+  if (is_block) {
+    kbase = p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + g) * HD;
+    vbase = p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + p.n_kv + g) * HD;
+    kv_ld = p.qkv_ld;
+  } else {
+    const size_t off = ((size_t)req * p.n_kv + g) * p.cap * HD;
+    kbase = p.cache_k + off;
+    vbase = p.cache_v + off;
+    kv_ld = HD;
+  }
+
+  // ---- stage Q (rows: head g*G + r/L, token r%L) ----
+  for (int i = tid; i < QRp * NCH; i += blockDim.x) {
+    const int r = i / NCH, ch = i % NCH;
+    const bool valid = r < QR;
+    const int h = g * p.G + (valid ? r / p.L : 0);
+    const int j = valid ? r % p.L : 0;
+    const __nv_bfloat16* src = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD + ch * 8;
+    cp_async16(smem_u32(sQ) + swz<HD>(r, ch), src, valid);
+  }
+  auto load_tile = [&](int buf, int key0) {
+    uint8_t* dK = sK + buf * kKeyTile * HD * 2;
+    uint8_t* dV = sV + buf * kKeyTile * HD * 2;
+    for (int i = tid; i < kKeyTile * NCH; i += blockDim.x) {
+      const int r = i / NCH, ch = i % NCH;
+      const int key = key0 + r;
+      const bool valid = key < k_end;
+      const size_t off = (size_t)(valid ? key : k_begin) * kv_ld + ch * 8;
+      cp_async16(smem_u32(dK) + swz<HD>(r, ch), kbase + off, valid);
+      cp_async16(smem_u32(dV) + swz<HD>(r, ch), vbase + off, valid);
+    }
+  };
+  load_tile(0, k_begin);
+  cp_async_commit();
+
+  const int qrow0 = warp * 16;
+  const bool warp_active = qrow0 < QR;
+  const int gq = lane >> 2, tq = lane & 3;
+  float o[HD / 8][4];
+#pragma unroll
+  for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  uint32_t qa[HD / 16][4];
+
+  const int ntiles = (k_end - k_begin + kKeyTile - 1) / kKeyTile;
+  for (int t = 0; t < ntiles; ++t) {
+    const int key0 = k_begin + t * kKeyTile;
+    if (t + 1 < ntiles) load_tile((t + 1) & 1, key0 + kKeyTile);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (t == 0 && warp_active) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const int r = qrow0 + (lane & 15);
+        const int ch = kk * 2 + (lane >> 4);
+        ldsm_x4(smem_u32(sQ) + swz<HD>(r, ch), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    if (warp_active) {
+      const uint32_t kb = smem_u32(sK + (t & 1) * kKeyTile * HD * 2);
+      const uint32_t vb = smem_u32(sV + (t & 1) * kKeyTile * HD * 2);
+      float s[kKeyTile / 8][4];
+#pragma unroll
+      for (int n = 0; n < kKeyTile / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      // S = Q K^T
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+        for (int np = 0; np < kKeyTile / 16; ++np) {
+          const int r = np * 16 + ((lane >> 4) << 3) + (lane & 7);
+          const int ch = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + swz<HD>(r, ch), b0, b1, b2, b3);
+          mma16816(s[2 * np], qa[kk], b0, b1);
+          mma16816(s[2 * np + 1], qa[kk], b2, b3);
+        }
+      }
+      // scale, mask, online softmax (base 2)
+      const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
+      const bool iso0 = is_block && !p.anchor_sees_block && (rq0 % p.L) == 0;
+      const bool iso1 = is_block && !p.anchor_sees_block && (rq1 % p.L) == 0;
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+      for (int n = 0; n < kKeyTile / 8; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key0 + n * 8 + 2 * tq + e;
+          const bool ok = key < k_end;
+          float v0 = s[n][e] * p.scale_log2;
+          float v1 = s[n][2 + e] * p.scale_log2;
+          if (!ok || (iso0 && key > 0)) v0 = -CUDART_INF_F;
+          if (!ok || (iso1 && key > 0)) v1 = -CUDART_INF_F;
+          s[n][e] = v0;
+          s[n][2 + e] = v1;
+          mx0 = fmaxf(mx0, v0);
+          mx1 = fmaxf(mx1, v1);
+        }
+      }
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+      const float base1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+      const float c0 = exp2f(m0 - base0), c1 = exp2f(m1 - base1);
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < kKeyTile / 8; ++n) {
+        s[n][0] = exp2f(s[n][0] - base0);
+        s[n][1] = exp2f(s[n][1] - base0);
+        s[n][2] = exp2f(s[n][2] - base1);
+        s[n][3] = exp2f(s[n][3] - base1);
+        rs0 += s[n][0] + s[n][1];
+        rs1 += s[n][2] + s[n][3];
+      }
+      l0 = l0 * c0 + rs0;
+      l1 = l1 * c1 + rs1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n) {
+        o[n][0] *= c0; o[n][1] *= c0;
+        o[n][2] *= c1; o[n][3] *= c1;
+      }
+      // O += P V
+#pragma unroll
+      for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < HD / 16; ++dp) {
+          const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int ch = dp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + swz<HD>(r, ch), b0, b1, b2, b3);
+          mma16816(o[2 * dp], pa, b0, b1);
+          mma16816(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // row sums: reduce over the quad
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  if (warp_active) {
+    const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      const int d = n * 8 + 2 * tq;
+      if (rq0 < QR) {
+        float2* dst = reinterpret_cast<float2*>(p.part_o + (part_row0 + rq0) * HD + d);
+        *dst = make_float2(o[n][0], o[n][1]);
+      }
+      if (rq1 < QR) {
+        float2* dst = reinterpret_cast<float2*>(p.part_o + (part_row0 + rq1) * HD + d);
+        *dst = make_float2(o[n][2], o[n][3]);
+      }
+    }
+    if (tq == 0) {
+      if (rq0 < QR) {
+        p.part_ml[(part_row0 + rq0) * 2 + 0] = m0;
+        p.part_ml[(part_row0 + rq0) * 2 + 1] = l0;
+      }
+      if (rq1 < QR) {
+        p.part_ml[(part_row0 + rq1) * 2 + 0] = m1;
+        p.part_ml[(part_row0 + rq1) * 2 + 1] = l1;
+      }
+    }
+  }
+  (void)nwarps;
+}
+
+// Merge the partials of one (request, KV head): 4 query rows per CTA, a warp
+// per row, 4 dims per lane (HD = 128) or 2 (HD = 64).
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_combine_kernel(const AttnParams p) {
+  const int QR = p.G * p.L;
+  const int req = blockIdx.z, g = blockIdx.y;
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= QR) return;
+  const int nparts = p.n_chunks + 1;
+  const size_t base = ((size_t)req * p.n_kv + g) * nparts * QR;
+  float M = -CUDART_INF_F;
+  for (int c = 0; c < nparts; ++c) M = fmaxf(M, p.part_ml[(base + (size_t)c * QR + r) * 2]);
+  constexpr int DPL = HD / 32;
+  float acc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+  float Lsum = 0.f;
+  for (int c = 0; c < nparts; ++c) {
+    const size_t row = base + (size_t)c * QR + r;
+    const float l = p.part_ml[row * 2 + 1];
+    if (l == 0.f) continue;
+    const float w = exp2f(p.part_ml[row * 2] - M);
+    Lsum += w * l;
+    const float* src = p.part_o + row * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] += w * src[i];
+  }
+  const float inv = 1.f / Lsum;
+  const int h = g * p.G + r / p.L, j = r % p.L;
+  __nv_bfloat16* dst = p.out + ((size_t)req * p.L + j) * p.out_ld + (size_t)h * HD + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) dst[i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+// fp32 reference-precision path: one warp per (request, query head, token).
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_f32_kernel(const AttnParamsF32 p) {
+  constexpr int DPL = HD / 32;
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int total = p.n_req * p.n_q * p.L;
+  if (wid >= total) return;
+  const int j = wid % p.L;
+  const int h = (wid / p.L) % p.n_q;
+  const int req = wid / (p.L * p.n_q);
+  const int g = h / (p.n_q / p.n_kv);
+  const int ctx = min(max(p.ctx_len[req], 0), p.cap);
+  const float* q = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD;
+  float qv[DPL], o[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) { qv[i] = q[lane + 32 * i]; o[i] = 0.f; }
+  float m = -CUDART_INF_F, l = 0.f;
+  const float scale = rsqrtf(static_cast<float>(HD));
+  const bool iso = !p.anchor_sees_block && j == 0;
+  const int nkeys = ctx + (iso ? 1 : p.L);
+  for (int s = 0; s < nkeys; ++s) {
+    const float* kr;
+    const float* vr;
+    if (s < ctx) {
+      const size_t off = (((size_t)req * p.n_kv + g) * p.cap + s) * HD;
+      kr = p.cache_k + off;
+      vr = p.cache_v + off;
+    } else {
+      const int jj = s - ctx;
+      kr = p.qkv + ((size_t)req * p.L + jj) * p.qkv_ld + (size_t)(p.n_q + g) * HD;
+      vr = p.qkv + ((size_t)req * p.L + jj) * p.qkv_ld + (size_t)(p.n_q + p.n_kv + g) * HD;
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) part = fmaf(qv[i], kr[lane + 32 * i], part);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    const float sc = part * scale;
+    const float mn = fmaxf(m, sc);
+    const float corr = expf(m - mn);
+    const float pw = expf(sc - mn);
+    l = l * corr + pw;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = o[i] * corr + pw * vr[lane + 32 * i];
+    m = mn;
+  }
+  float* dst = p.out + ((size_t)req * p.L + j) * p.out_ld + (size_t)h * HD;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) dst[lane + 32 * i] = o[i] / l;
+}
+
+}  // namespace
+
+int attn_chunk(int max_ctx, int n_kv, int n_req) {
+  const long long target = 2LL * num_sms();
+  long long work = (long long)max_ctx * n_kv * n_req;
+  long long c = (work + target - 1) / target;
+  c = (c + kKeyTile - 1) / kKeyTile * kKeyTile;
+  if (c < kKeyTile) c = kKeyTile;
+  if (c > 8192) c = 8192;
+  return static_cast<int>(c);
+}
+
+size_t attn_smem_bytes(int G, int L, int HD) {
+  const int QRp = (G * L + 15) / 16 * 16;
+  return (size_t)QRp * HD * 2 + 4 * kKeyTile * HD * 2;
+}
+
+dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStream_t st) {
+  const int QR = p.G * p.L;
+  const int warps = (QR + 15) / 16;
+  if (warps > 4) return set_error(DFLASH_ERR_UNSUPPORTED, "attention: G*L > 64 query rows");
+  const size_t smem = attn_smem_bytes(p.G, p.L, head_dim);
+  dim3 grid(p.n_chunks + 1, p.n_kv, p.n_req);
+  dim3 cgrid((QR + 3) / 4, p.n_kv, p.n_req);
+  if (head_dim == 128) {
+    static bool set = false;
+    if (!set) {
+      cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           160 * 1024);
+      set = true;
+    }
+    attn_split_kernel<128><<<grid, 128, smem, st>>>(p);
+    attn_combine_kernel<128><<<cgrid, 128, 0, st>>>(p);
+  } else if (head_dim == 64) {
+    static bool set = false;
+    if (!set) {
+      cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           160 * 1024);
+      set = true;
+    }
+    attn_split_kernel<64><<<grid, 128, smem, st>>>(p);
+    attn_combine_kernel<64><<<cgrid, 128, 0, st>>>(p);
+  } else {
+    return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
+  }
+  return check_launch("attention_bf16");
+}
+
+dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStream_t st) {
+  const int total = p.n_req * p.n_q * p.L;
+  const int blocks = (total + 3) / 4;
+  if (head_dim == 128) attn_f32_kernel<128><<<blocks, 128, 0, st>>>(p);
+  else if (head_dim == 64) attn_f32_kernel<64><<<blocks, 128, 0, st>>>(p);
+  else return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
+  return check_launch("attention_f32");
+}
+
+}  // namespace dfl

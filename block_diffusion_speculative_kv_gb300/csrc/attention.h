@@ -1,0 +1,50 @@
+// Attention launch interface (attention.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace dfl {
+
+// bf16 split-KV attention of one layer.  qkv: [n_req*L][qkv_ld] with Q at
+// column 0, the block's K at n_q*hd and V at (n_q+n_kv)*hd; cache_k/v:
+// [n_req][n_kv][cap][hd]; out: [n_req*L][out_ld], head h at column h*hd.
+struct AttnParams {
+  const __nv_bfloat16* qkv;
+  long long qkv_ld;
+  const __nv_bfloat16* cache_k;
+  const __nv_bfloat16* cache_v;
+  const int* ctx_len;
+  int cap;
+  int n_req, n_q, n_kv, G, L;
+  int chunk;      // context keys per CTA (multiple of 64)
+  int n_chunks;   // context chunks per (request, KV head); one more holds the block
+  float scale_log2;
+  int anchor_sees_block;
+  float* part_o;   // [n_req][n_kv][n_chunks+1][G*L][hd]
+  float* part_ml;  // [n_req][n_kv][n_chunks+1][G*L][2]
+  __nv_bfloat16* out;
+  long long out_ld;
+};
+
+struct AttnParamsF32 {
+  const float* qkv;
+  long long qkv_ld;
+  const float* cache_k;
+  const float* cache_v;
+  const int* ctx_len;
+  int cap;
+  int n_req, n_q, n_kv, L;
+  int anchor_sees_block;
+  float* out;
+  long long out_ld;
+};
+
+int attn_chunk(int max_ctx, int n_kv, int n_req);
+size_t attn_smem_bytes(int G, int L, int HD);
+dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStream_t st);
+dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStream_t st);
+
+}  // namespace dfl

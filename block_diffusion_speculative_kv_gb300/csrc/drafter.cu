@@ -1,8 +1,25 @@
-// Drafter model handle, KV injection and the block pass (steps a1-a6).
+// Drafter model handle, workspace layout, KV injection (steps a1-a2) and the
+// block pass with LM head and top-K (steps a3-a6).  Contracts: include/dflash.h.
+//
+// Call sequence of dflash_draft_block for a model of n_layers layers
+// ("DFlash: Block Diffusion for Flash Speculative Decoding", section 3.4.4):
+//   block_prologue                          x, xn = x*g, RMS partials, RoPE table
+//   per layer: GEMM  xn . [W_q|W_k|W_v]^T    -> QKV epilogue (RMS scale, RoPE)
+//              attention over [context ; block]  (split-KV + combine)
+//              GEMM  o . W_o^T               -> residual epilogue (x, xn, RMS partials)
+//              GEMM  xn . [W_gate|W_up]^T    -> SwiGLU epilogue
+//              GEMM  h . W_down^T            -> residual epilogue
+//   GEMM  xn . W_lm^T                       -> logits of the L-1 mask rows (fp32)
+//   log-softmax + top-K per row             (DDTree page, section 3.4.2)
+// dflash_inject_kv (section 3.4.3): GEMM feats . W_proj^T -> f; GEMM
+// f . [U_K|U_V]^T (all layers stacked) -> KV epilogue (RoPE on K, cache scatter).
 #include <cstdlib>
 #include <cstring>
+#include <new>
 
+#include "attention.h"
 #include "common.cuh"
+#include "gemm.h"
 #include "kernels.h"
 
 using namespace dfl;
@@ -10,40 +27,458 @@ using namespace dfl;
 struct dflash_model {
   dflash_dims dims;
   dflash_weights w;
+  bool bf16;
+  CUtensorMap tm_proj, tm_ukv, tm_lm;
+  CUtensorMap tm_qkv[DFLASH_MAX_LAYERS], tm_o[DFLASH_MAX_LAYERS], tm_gu[DFLASH_MAX_LAYERS],
+      tm_down[DFLASH_MAX_LAYERS];
 };
+
+namespace {
+
+size_t esize(const dflash_dims& d) { return d.dtype == DFLASH_BF16 ? 2 : 4; }
+
+// Workspace regions of a model-sized workspace (byte offsets).
+struct WsLayout {
+  size_t counters, x, xn, ssq, qkv, attn_o, h, logits, gpart, apart_o, apart_ml, tpart, rope_blk,
+      f, rope_inj, total;
+  int attn_chunks_cap;
+};
+
+int ssq_parts(const dflash_dims& d) { return (d.d + 127) / 128; }
+
+WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L, int K) {
+  const dflash_dims& d = m.dims;
+  const size_t es = esize(d);
+  const int R = n_req * L;
+  const int D = L - 1;
+  const int G = d.n_q / d.n_kv;
+  const int qkv_dim = (d.n_q + 2 * d.n_kv) * d.head_dim;
+  const int sms = num_sms();
+  WsLayout w{};
+  size_t off = 256;  // status word and reserved header
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const int n_counters = 4096 > R ? 4096 : R;
+  w.counters = take(sizeof(int) * n_counters);
+  w.x = take(sizeof(float) * (size_t)R * d.d);
+  w.xn = take(es * (size_t)R * d.d);
+  w.ssq = take(sizeof(float) * (size_t)ssq_parts(d) * R);
+  w.qkv = take(es * (size_t)R * qkv_dim);
+  w.attn_o = take(es * (size_t)R * d.n_q * d.head_dim);
+  w.h = take(es * (size_t)R * d.d_ff);
+  w.logits = take(sizeof(float) * (size_t)n_req * D * d.vocab);
+  // GEMM partial sums: the largest plan among the GEMMs of a call
+  size_t gp = 0;
+  if (m.bf16) {
+    // the largest need among all activation-row counts up to this call's maximum:
+    // for a fixed row tile the partial count peaks at the tile's smallest row
+    // count, so the row-tile sizes themselves cover every row count in between
+    const int Mmax = R > max_inject_rows ? R : max_inject_rows;
+    int Ms[8];
+    int nm = 0;
+    for (int t = 16; t <= tc_row_tile(Mmax); t <<= 1) Ms[nm++] = t;
+    Ms[nm++] = R;
+    if (max_inject_rows > 0) Ms[nm++] = max_inject_rows;
+    for (int mi = 0; mi < nm; ++mi) {
+      const int M = Ms[mi];
+      const int NK[7][2] = {{qkv_dim, d.d}, {d.d, d.n_q * d.head_dim}, {2 * d.d_ff, d.d},
+                            {d.d, d.d_ff}, {d.vocab, d.d}, {d.d, d.n_feat * d.d_feat},
+                            {d.n_layers * 2 * d.n_kv * d.head_dim, d.d}};
+      for (auto& nk : NK) {
+        const TcPlan pl = tc_plan(M, nk[0], nk[1], sms);
+        if (pl.part_bytes > gp) gp = pl.part_bytes;
+      }
+    }
+  }
+  w.gpart = take(gp);
+  // attention partials: enough chunks for ~2 CTAs per SM plus the block chunk
+  int cap_chunks = (2 * sms + d.n_kv * n_req - 1) / (d.n_kv * n_req) + 2;
+  w.attn_chunks_cap = cap_chunks;
+  const size_t arows = (size_t)n_req * d.n_kv * (cap_chunks + 1) * G * L;
+  w.apart_o = take(m.bf16 ? sizeof(float) * arows * d.head_dim : 0);
+  w.apart_ml = take(m.bf16 ? sizeof(float) * arows * 2 : 0);
+  w.tpart = take(topk_part_bytes(n_req * D, 32));
+  w.rope_blk = take(sizeof(float2) * (size_t)R * (d.head_dim / 2));
+  w.f = take(es * (size_t)max_inject_rows * d.d);
+  w.rope_inj = take(sizeof(float2) * (size_t)max_inject_rows * (d.head_dim / 2));
+  w.total = off;
+  (void)K;
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+dflash_status validate_dims(const dflash_dims& d) {
+  if (d.n_layers < 1 || d.n_layers > DFLASH_MAX_LAYERS)
+    return set_error(DFLASH_ERR_INVALID_ARG, "n_layers must be in [1, %d]", DFLASH_MAX_LAYERS);
+  if (d.d <= 0 || d.n_q <= 0 || d.n_kv <= 0 || d.d_ff <= 0 || d.vocab <= 0 || d.n_feat <= 0 ||
+      d.d_feat <= 0)
+    return set_error(DFLASH_ERR_INVALID_ARG, "all sizes must be positive");
+  if (d.n_q % d.n_kv != 0) return set_error(DFLASH_ERR_INVALID_ARG, "n_q %% n_kv != 0");
+  if (d.head_dim != 64 && d.head_dim != 128)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (d.mask_id < 0 || d.mask_id >= d.vocab)
+    return set_error(DFLASH_ERR_INVALID_ARG, "mask_id out of range");
+  if (d.dtype != DFLASH_F32 && d.dtype != DFLASH_BF16)
+    return set_error(DFLASH_ERR_INVALID_ARG, "dtype must be F32 or BF16");
+  if (!(d.rope_theta > 0.f) || !(d.rms_eps >= 0.f))
+    return set_error(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+  if (d.dtype == DFLASH_BF16) {
+    const int q = d.n_q * d.head_dim;
+    if (d.d % 128 || (d.n_feat * d.d_feat) % 128 || q % 128 || d.d_ff % 128)
+      return set_error(DFLASH_ERR_UNSUPPORTED,
+                       "bf16 models need d, n_feat*d_feat, n_q*head_dim, d_ff multiples of 128");
+    if ((d.n_q / d.n_kv) > 4)
+      return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention supports n_q/n_kv <= 4");
+  }
+  return DFLASH_OK;
+}
+
+EpiParams epi_base(const dflash_model& m, int M_rows, int N_feat) {
+  EpiParams e{};
+  e.M_rows = M_rows;
+  e.N_feat = N_feat;
+  e.inv_d = 1.f / static_cast<float>(m.dims.d);
+  e.eps = m.dims.rms_eps;
+  e.ssq_parts = ssq_parts(m.dims);
+  e.head_dim = m.dims.head_dim;
+  return e;
+}
+
+struct CallCtx {
+  const dflash_model* m;
+  char* ws;
+  WsLayout L;
+  cudaStream_t st;
+  int* status;
+  int* counters;
+};
+
+// One GEMM: acc = X . W^T with epilogue e.  X [M][K] (row stride ldx, elements).
+dflash_status gemm(const CallCtx& c, const CUtensorMap* tmW, const void* W, const void* X,
+                   long long ldx, int M, int N, int K, const EpiParams& e) {
+  if (M <= 0) return DFLASH_OK;
+  if (c.m->bf16) {
+    const TcPlan pl = tc_plan(M, N, K, num_sms());
+    CUtensorMap tmX;
+    if (!encode_kmajor_map(&tmX, X, M, K, ldx, pl.n_tile))
+      return set_error(DFLASH_ERR_CUDA, "cannot encode the activation TMA descriptor");
+    return launch_gemm_tc(*tmW, tmX, pl, M, N, K, reinterpret_cast<float*>(c.ws + c.L.gpart),
+                          c.counters, c.status, e, c.st);
+  }
+  return launch_gemm_f32(static_cast<const float*>(X), ldx, static_cast<const float*>(W), M, N,
+                         K, e, c.st);
+}
+
+}  // namespace
 
 extern "C" {
 
 dflash_status dflash_model_create(const dflash_dims* dims, const dflash_weights* weights,
                                   dflash_model** out) {
   if (!dims || !weights || !out) return set_error(DFLASH_ERR_INVALID_ARG, "null argument");
-  return set_error(DFLASH_ERR_UNSUPPORTED, "drafter kernels not built yet");
+  dflash_status st = validate_dims(*dims);
+  if (st != DFLASH_OK) return st;
+  const dflash_weights& w = *weights;
+  const void* req_ptrs[] = {w.w_proj, w.embed, w.lm_head, w.final_norm, w.u_kv};
+  for (const void* p : req_ptrs)
+    if (!p || !aligned16(p)) return set_error(DFLASH_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
+  for (int l = 0; l < dims->n_layers; ++l) {
+    const void* lp[] = {w.attn_norm[l], w.w_qkv[l], w.wo[l], w.mlp_norm[l], w.w_gate_up[l],
+                        w.w_down[l]};
+    for (const void* p : lp)
+      if (!p || !aligned16(p))
+        return set_error(DFLASH_ERR_INVALID_ARG, "layer %d weight pointer null or misaligned", l);
+  }
+  dflash_model* m = new (std::nothrow) dflash_model();
+  if (!m) return set_error(DFLASH_ERR_INVALID_ARG, "out of host memory");
+  m->dims = *dims;
+  m->w = w;
+  m->bf16 = dims->dtype == DFLASH_BF16;
+  if (m->bf16) {
+    const dflash_dims& d = *dims;
+    const int qkv_dim = (d.n_q + 2 * d.n_kv) * d.head_dim;
+    const int qd = d.n_q * d.head_dim;
+    bool ok = encode_kmajor_map(&m->tm_proj, w.w_proj, d.d, d.n_feat * d.d_feat,
+                                (long long)d.n_feat * d.d_feat, 128) &&
+              encode_kmajor_map(&m->tm_ukv, w.u_kv, d.n_layers * 2 * d.n_kv * d.head_dim, d.d,
+                                d.d, 128) &&
+              encode_kmajor_map(&m->tm_lm, w.lm_head, d.vocab, d.d, d.d, 128);
+    for (int l = 0; ok && l < d.n_layers; ++l) {
+      ok = encode_kmajor_map(&m->tm_qkv[l], w.w_qkv[l], qkv_dim, d.d, d.d, 128) &&
+           encode_kmajor_map(&m->tm_o[l], w.wo[l], d.d, qd, qd, 128) &&
+           encode_kmajor_map(&m->tm_gu[l], w.w_gate_up[l], 2 * d.d_ff, d.d, d.d, 128) &&
+           encode_kmajor_map(&m->tm_down[l], w.w_down[l], d.d, d.d_ff, d.d_ff, 128);
+    }
+    if (!ok) {
+      delete m;
+      return set_error(DFLASH_ERR_CUDA, "cannot encode weight TMA descriptors");
+    }
+  }
+  *out = m;
+  return DFLASH_OK;
 }
 
-void dflash_model_destroy(dflash_model* model) { std::free(model); }
+void dflash_model_destroy(dflash_model* model) { delete model; }
 
 size_t dflash_workspace_bytes(const dflash_model* model, int n_req, int max_inject_rows, int L,
                               int K) {
-  (void)model; (void)n_req; (void)max_inject_rows; (void)L; (void)K;
-  return 0;
+  if (!model || n_req < 1 || max_inject_rows < 0 || L < 2 || L > 16 || K < 1 || K > 32)
+    return 0;
+  return ws_layout(*model, n_req, max_inject_rows, L, K).total;
 }
 
 dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* cache, int n_req,
                                int n_rows, const int32_t* row_off, const int32_t* pos0,
                                const void* feats, void* ws, size_t ws_bytes, void* stream) {
-  (void)model; (void)cache; (void)n_req; (void)n_rows; (void)row_off; (void)pos0;
-  (void)feats; (void)ws; (void)ws_bytes; (void)stream;
-  return set_error(DFLASH_ERR_UNSUPPORTED, "drafter kernels not built yet");
+  if (!model || !cache) return set_error(DFLASH_ERR_INVALID_ARG, "null model or cache");
+  if (n_req < 1 || n_req > cache->n_req)
+    return set_error(DFLASH_ERR_INVALID_ARG, "n_req must be in [1, cache->n_req]");
+  if (n_rows < 0) return set_error(DFLASH_ERR_INVALID_ARG, "n_rows must be >= 0");
+  if (n_rows == 0) return DFLASH_OK;
+  if (!row_off || !pos0 || !feats)
+    return set_error(DFLASH_ERR_INVALID_ARG, "null row_off/pos0/feats");
+  const dflash_dims& d = model->dims;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!cache->k[l] || !cache->v[l]) return set_error(DFLASH_ERR_INVALID_ARG, "null cache layer %d", l);
+  if (cache->cap < 1) return set_error(DFLASH_ERR_INVALID_ARG, "cache cap must be >= 1");
+  if (model->bf16 && !aligned16(feats))
+    return set_error(DFLASH_ERR_INVALID_ARG, "feats must be 16-byte aligned");
+  // the workspace must have been sized for at least n_rows injected rows
+  const WsLayout L = ws_layout(*model, n_req, n_rows, 2, 1);
+  const size_t need = L.rope_inj + sizeof(float2) * (size_t)n_rows * (d.head_dim / 2);
+  if (!ws || ws_bytes < need)
+    return set_error(DFLASH_ERR_WORKSPACE, "inject workspace needs %zu bytes, got %zu", need,
+                     ws_bytes);
+  CallCtx c{model, static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream),
+            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + L.counters)};
+  float2* rope = reinterpret_cast<float2*>(c.ws + L.rope_inj);
+  launch_inject_rope(row_off, pos0, n_req, n_rows, d.head_dim, d.rope_theta, rope, c.st);
+  dflash_status st = check_launch("inject rope");
+  if (st) return st;
+
+  // a1: f = feats . W_proj^T
+  void* f = c.ws + L.f;
+  EpiParams e1 = epi_base(*model, n_rows, d.d);
+  e1.kind = EPI_STORE;
+  e1.ssq_in = nullptr;
+  e1.out = f;
+  e1.ldo = d.d;
+  st = gemm(c, &model->tm_proj, model->w.w_proj, feats, (long long)d.n_feat * d.d_feat, n_rows,
+            d.d, d.n_feat * d.d_feat, e1);
+  if (st) return st;
+  // a2: [K|V] of every layer = f . U^T, K rotated, scattered into the cache
+  EpiParams e2 = epi_base(*model, n_rows, d.n_layers * 2 * d.n_kv * d.head_dim);
+  e2.kind = EPI_KV;
+  e2.ssq_in = nullptr;
+  e2.rope = rope;
+  for (int l = 0; l < d.n_layers; ++l) {
+    e2.cache_k[l] = cache->k[l];
+    e2.cache_v[l] = cache->v[l];
+  }
+  e2.n_kv = d.n_kv;
+  e2.cap = cache->cap;
+  e2.n_req = n_req;
+  e2.row_off = row_off;
+  e2.pos0 = pos0;
+  return gemm(c, &model->tm_ukv, model->w.u_kv, f, d.d, n_rows,
+              d.n_layers * 2 * d.n_kv * d.head_dim, d.d, e2);
 }
 
 dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache, int n_req,
                                  const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
                                  int L, int K, int32_t* topk_ids, float* topk_logp,
                                  float* logits, void* ws, size_t ws_bytes, void* stream) {
-  (void)model; (void)cache; (void)n_req; (void)anchor; (void)ctx_len; (void)max_ctx; (void)L;
-  (void)K; (void)topk_ids; (void)topk_logp; (void)logits; (void)ws; (void)ws_bytes;
-  (void)stream;
-  return set_error(DFLASH_ERR_UNSUPPORTED, "drafter kernels not built yet");
+  if (!model || !cache) return set_error(DFLASH_ERR_INVALID_ARG, "null model or cache");
+  const dflash_dims& d = model->dims;
+  if (n_req < 1 || n_req > cache->n_req)
+    return set_error(DFLASH_ERR_INVALID_ARG, "n_req must be in [1, cache->n_req]");
+  if (L < 2 || L > 16) return set_error(DFLASH_ERR_INVALID_ARG, "L must be in [2, 16]");
+  if (K < 1 || K > 32 || K > d.vocab)
+    return set_error(DFLASH_ERR_INVALID_ARG, "K must be in [1, min(32, vocab)]");
+  if (max_ctx < 0 || max_ctx > cache->cap)
+    return set_error(DFLASH_ERR_INVALID_ARG, "max_ctx must be in [0, cache->cap]");
+  if (!anchor || !ctx_len || !topk_ids || !topk_logp)
+    return set_error(DFLASH_ERR_INVALID_ARG, "null anchor/ctx_len/topk output");
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!cache->k[l] || !cache->v[l]) return set_error(DFLASH_ERR_INVALID_ARG, "null cache layer %d", l);
+  const WsLayout W = ws_layout(*model, n_req, 0, L, K);
+  if (!ws || ws_bytes < W.f)
+    return set_error(DFLASH_ERR_WORKSPACE, "draft workspace needs %zu bytes, got %zu", W.f,
+                     ws_bytes);
+  CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
+            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
+  const int R = n_req * L;
+  const int D = L - 1;
+  const int hd = d.head_dim;
+  const int qd = d.n_q * hd;
+  const int qkv_dim = (d.n_q + 2 * d.n_kv) * hd;
+  float* x = reinterpret_cast<float*>(c.ws + W.x);
+  void* xn = c.ws + W.xn;
+  float* ssq = reinterpret_cast<float*>(c.ws + W.ssq);
+  void* qkv = c.ws + W.qkv;
+  void* ao = c.ws + W.attn_o;
+  void* hbuf = c.ws + W.h;
+  float* lg = logits ? logits : reinterpret_cast<float*>(c.ws + W.logits);
+  float2* rope = reinterpret_cast<float2*>(c.ws + W.rope_blk);
+
+  BlockPrologueLaunch pa{model->bf16, model->w.embed, model->w.attn_norm[0], anchor, ctx_len,
+                         n_req, L, d.d, d.vocab, d.mask_id, hd, d.rope_theta, x, xn, ssq, rope,
+                         c.status};
+  launch_block_prologue(pa, c.st);
+  dflash_status st = check_launch("block prologue");
+  if (st) return st;
+
+  // attention decomposition
+  int chunk = attn_chunk(max_ctx > 0 ? max_ctx : 1, d.n_kv, n_req);
+  int n_chunks = (max_ctx + chunk - 1) / chunk;
+  if (n_chunks > W.attn_chunks_cap) {
+    chunk = ((max_ctx + W.attn_chunks_cap - 1) / W.attn_chunks_cap + 63) / 64 * 64;
+    n_chunks = (max_ctx + chunk - 1) / chunk;
+  }
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    // Q, K, V of the block rows
+    EpiParams eq = epi_base(*model, R, qkv_dim);
+    eq.kind = EPI_QKV;
+    eq.ssq_in = ssq;
+    eq.out = qkv;
+    eq.ldo = qkv_dim;
+    eq.rope = rope;
+    eq.rope_cols = (d.n_q + d.n_kv) * hd;
+    st = gemm(c, &model->tm_qkv[l], model->w.w_qkv[l], xn, d.d, R, qkv_dim, d.d, eq);
+    if (st) return st;
+    // attention over [context ; block]
+    if (model->bf16) {
+      AttnParams ap{};
+      ap.qkv = static_cast<const __nv_bfloat16*>(qkv);
+      ap.qkv_ld = qkv_dim;
+      ap.cache_k = static_cast<const __nv_bfloat16*>(cache->k[l]);
+      ap.cache_v = static_cast<const __nv_bfloat16*>(cache->v[l]);
+      ap.ctx_len = ctx_len;
+      ap.cap = cache->cap;
+      ap.n_req = n_req;
+      ap.n_q = d.n_q;
+      ap.n_kv = d.n_kv;
+      ap.G = d.n_q / d.n_kv;
+      ap.L = L;
+      ap.chunk = chunk;
+      ap.n_chunks = n_chunks;
+      ap.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
+      ap.anchor_sees_block = d.anchor_sees_block;
+      ap.part_o = reinterpret_cast<float*>(c.ws + W.apart_o);
+      ap.part_ml = reinterpret_cast<float*>(c.ws + W.apart_ml);
+      ap.out = static_cast<__nv_bfloat16*>(ao);
+      ap.out_ld = qd;
+      st = launch_attention_bf16(ap, hd, c.st);
+    } else {
+      AttnParamsF32 ap{};
+      ap.qkv = static_cast<const float*>(qkv);
+      ap.qkv_ld = qkv_dim;
+      ap.cache_k = static_cast<const float*>(cache->k[l]);
+      ap.cache_v = static_cast<const float*>(cache->v[l]);
+      ap.ctx_len = ctx_len;
+      ap.cap = cache->cap;
+      ap.n_req = n_req;
+      ap.n_q = d.n_q;
+      ap.n_kv = d.n_kv;
+      ap.L = L;
+      ap.anchor_sees_block = d.anchor_sees_block;
+      ap.out = static_cast<float*>(ao);
+      ap.out_ld = qd;
+      st = launch_attention_f32(ap, hd, c.st);
+    }
+    if (st) return st;
+    // x += o . W_o^T ; xn = x * g_mlp
+    EpiParams eo = epi_base(*model, R, d.d);
+    eo.kind = EPI_RESID;
+    eo.ssq_in = nullptr;
+    eo.x = x;
+    eo.xn = xn;
+    eo.gain = model->w.mlp_norm[l];
+    eo.ssq_out = ssq;
+    st = gemm(c, &model->tm_o[l], model->w.wo[l], ao, qd, R, d.d, qd, eo);
+    if (st) return st;
+    // h = silu(g) * u
+    EpiParams eg = epi_base(*model, R, 2 * d.d_ff);
+    eg.kind = EPI_SWIGLU;
+    eg.ssq_in = ssq;
+    eg.out = hbuf;
+    eg.ldo = d.d_ff;
+    st = gemm(c, &model->tm_gu[l], model->w.w_gate_up[l], xn, d.d, R, 2 * d.d_ff, d.d, eg);
+    if (st) return st;
+    // x += h . W_down^T ; xn = x * g_next
+    EpiParams ed = epi_base(*model, R, d.d);
+    ed.kind = EPI_RESID;
+    ed.ssq_in = nullptr;
+    ed.x = x;
+    ed.xn = xn;
+    ed.gain = (l + 1 < d.n_layers) ? model->w.attn_norm[l + 1] : model->w.final_norm;
+    ed.ssq_out = ssq;
+    st = gemm(c, &model->tm_down[l], model->w.w_down[l], hbuf, d.d_ff, R, d.d, d.d_ff, ed);
+    if (st) return st;
+  }
+  // LM head on the mask rows, then log-softmax + top-K
+  EpiParams el = epi_base(*model, R, d.vocab);
+  el.kind = EPI_LOGITS;
+  el.ssq_in = ssq;
+  el.logits = lg;
+  el.L = L;
+  st = gemm(c, &model->tm_lm, model->w.lm_head, xn, d.d, R, d.vocab, d.d, el);
+  if (st) return st;
+  TopkLaunch tk{};
+  tk.logits = lg;
+  tk.rows = n_req * D;
+  tk.vocab = d.vocab;
+  tk.ld = d.vocab;
+  tk.dtype = DFLASH_F32;
+  tk.K = K;
+  tk.splits = topk_splits(tk.rows, d.vocab);
+  tk.part = reinterpret_cast<float*>(c.ws + W.tpart);
+  tk.counters = c.counters;
+  tk.ids = topk_ids;
+  tk.logp = topk_logp;
+  launch_topk(tk, c.st);
+  return check_launch("top-K");
+}
+
+size_t dflash_linear_workspace_bytes(int M, int N, int K) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 64 || N % 128) return 0;
+  const TcPlan pl = tc_plan(M > 0 ? M : 1, N, K, num_sms());
+  const int n_counters = pl.grid > 4096 ? pl.grid : 4096;
+  return 256 + align_up(sizeof(int) * n_counters, 256) + align_up(pl.part_bytes, 256);
+}
+
+dflash_status dflash_linear_bf16(int M, int N, int K, const void* X, const void* W, float* Y,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 64 || N % 128)
+    return set_error(DFLASH_ERR_INVALID_ARG, "need M >= 0, K %% 64 == 0, N %% 128 == 0");
+  if (M == 0) return DFLASH_OK;
+  if (!X || !W || !Y || !aligned16(X) || !aligned16(W))
+    return set_error(DFLASH_ERR_INVALID_ARG, "X, W, Y must be non-null, X and W 16-byte aligned");
+  const size_t need = dflash_linear_workspace_bytes(M, N, K);
+  if (!ws || ws_bytes < need)
+    return set_error(DFLASH_ERR_WORKSPACE, "linear workspace needs %zu bytes, got %zu", need,
+                     ws_bytes);
+  const TcPlan pl = tc_plan(M, N, K, num_sms());
+  CUtensorMap tmW, tmX;
+  if (!encode_kmajor_map(&tmW, W, N, K, K, 128) || !encode_kmajor_map(&tmX, X, M, K, K, pl.n_tile))
+    return set_error(DFLASH_ERR_CUDA, "cannot encode TMA descriptors");
+  EpiParams e{};
+  e.kind = EPI_STORE_F32;
+  e.M_rows = M;
+  e.N_feat = N;
+  e.logits = Y;
+  e.ldo = N;
+  char* w = static_cast<char*>(ws);
+  const int n_counters = pl.grid > 4096 ? pl.grid : 4096;
+  int* counters = reinterpret_cast<int*>(w + 256);
+  float* part = reinterpret_cast<float*>(w + 256 + align_up(sizeof(int) * n_counters, 256));
+  return launch_gemm_tc(tmW, tmX, pl, M, N, K, part, counters, static_cast<int*>(ws), e,
+                        static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,0 +1,216 @@
+// Fused GEMM epilogues of the drafter pass.
+//
+// Every GEMM of the path computes acc[row][col] = sum_k X[row][k] W[col][k]
+// (X: activations, W: a weight matrix in [out][in] layout) and then one of the
+// operations below, applied to 16-row chunks of a 128-column tile that sit in
+// shared memory (buf[r][c], r < 16, c < 128).  The thread with tile column f
+// (0..127) handles column f of every row of the chunk.
+//
+//   STORE   out[row][col] = T(acc * s(row))                     (fusion, W_proj)
+//   QKV     Q/K columns rotated (RoPE at the row's block position), V plain,
+//           all scaled by the row's RMS factor s(row)             (W_q|W_k|W_v)
+//   RESID   x[row][col] += acc;  xn[row][col] = T(x * gain[col]); per-tile
+//           sum of x^2 of the row for the next RMSNorm            (W_o, W_down)
+//   SWIGLU  h[row][col/2] = T(silu(g) * u), g = even col, u = odd col, both
+//           scaled by s(row)                                       (W_gate|W_up)
+//   KV      columns [layer][K|V][n_kv*hd]: K rotated at the row's cache
+//           position, written to that layer's cache slot           (U_K|U_V)
+//   LOGITS  logits[req][j-1][col] = acc * s(row) for block rows j >= 1 (LM head)
+//   STORE_F32  logits[row][col] = acc (fp32, plain dense product)
+//
+// s(row) = rsqrt(sum of the row's per-tile x^2 partials / d + eps) is the
+// RMSNorm factor; the norm's gain is folded into xn when the residual is
+// written, so (xn . W) * s = RMSNorm(x) . W.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+enum EpiKind : int {
+  EPI_STORE = 0,
+  EPI_QKV = 1,
+  EPI_RESID = 2,
+  EPI_SWIGLU = 3,
+  EPI_KV = 4,
+  EPI_LOGITS = 5,
+  EPI_STORE_F32 = 6
+};
+
+constexpr int kTileN = 128;   // weight rows (output columns) per tile
+constexpr int kChunk = 16;    // activation rows per epilogue chunk
+constexpr int kBufLd = 132;   // padded row stride of the chunk buffer (floats)
+
+struct EpiParams {
+  int kind;
+  int M_rows;   // activation rows
+  int N_feat;   // GEMM output columns
+  // RMS row scale; ssq_in == nullptr means s = 1
+  const float* ssq_in;
+  int ssq_parts;
+  float inv_d;
+  float eps;
+  // STORE / QKV / SWIGLU destination (type T)
+  void* out;
+  long long ldo;
+  // RoPE table [M_rows][head_dim/2] of (cos, sin); columns < rope_cols rotate
+  const float2* rope;
+  int head_dim;
+  int rope_cols;
+  // RESID
+  float* x;           // [M_rows][N_feat] fp32, updated in place
+  void* xn;           // [M_rows][N_feat] T
+  const void* gain;   // [N_feat] T
+  float* ssq_out;     // [N_feat/128][M_rows]
+  // KV
+  void* cache_k[DFLASH_MAX_LAYERS];
+  void* cache_v[DFLASH_MAX_LAYERS];
+  int n_kv;
+  int cap;
+  int n_req;
+  const int* row_off;  // [n_req+1]
+  const int* pos0;     // [n_req]
+  // LOGITS
+  float* logits;
+  int L;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
+
+// Row scales of the rows [row0, row0 + n) into s_scale (s = 1 without ssq).
+__device__ __forceinline__ void epi_row_scales(const EpiParams& e, int row0, int n,
+                                               float* s_scale, int tid, int nthreads) {
+  for (int r = tid; r < n; r += nthreads) {
+    float s = 1.f;
+    const int row = row0 + r;
+    if (e.ssq_in != nullptr && row < e.M_rows) {
+      float acc = 0.f;
+      for (int p = 0; p < e.ssq_parts; ++p) acc += e.ssq_in[(size_t)p * e.M_rows + row];
+      s = rsqrtf(acc * e.inv_d + e.eps);
+    }
+    s_scale[r] = s;
+  }
+}
+
+// Request of a global activation row (row_off is a prefix-offset array).
+__device__ __forceinline__ int row_request(const int* row_off, int n_req, int row) {
+  int lo = 0, hi = n_req - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (row_off[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Apply the epilogue to one chunk: rows [crow0, crow0 + nrows) of the tile whose
+// first column is col0.  buf[r * kBufLd + c] holds acc.  `f` is this thread's
+// tile column; all 128 threads of the group call this together (warp-uniform
+// control flow, shuffles inside).  s_scale is indexed by row - srow0.
+// s_red[warp][row - srow0] accumulates RESID sums of squares.
+template <typename T>
+__device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float* buf, int col0,
+                                                int crow0, int nrows, int f,
+                                                const float* s_scale, int srow0,
+                                                float* s_red, int s_red_ld, int ewarp) {
+  const int col = col0 + f;
+  const bool cvalid = col < e.N_feat;
+  const int lane = f & 31;
+  for (int r = 0; r < nrows; ++r) {
+    const int row = crow0 + r;
+    const float s = s_scale[row - srow0];
+    const float a = buf[r * kBufLd + f];
+    switch (e.kind) {
+      case EPI_STORE: {
+        if (cvalid) static_cast<T*>(e.out)[(size_t)row * e.ldo + col] = from_f32<T>(a * s);
+        break;
+      }
+      case EPI_QKV: {
+        float v = a * s;
+        if (col < e.rope_cols) {
+          const int half = e.head_dim >> 1;
+          const int i = col % e.head_dim;
+          const int pf = (i < half) ? f + half : f - half;
+          const float pv = buf[r * kBufLd + pf] * s;
+          const float2 cs = e.rope[(size_t)row * half + (i % half)];
+          v = (i < half) ? (v * cs.x - pv * cs.y) : (v * cs.x + pv * cs.y);
+        }
+        if (cvalid) static_cast<T*>(e.out)[(size_t)row * e.ldo + col] = from_f32<T>(v);
+        break;
+      }
+      case EPI_RESID: {
+        float xv = 0.f;
+        if (cvalid) {
+          const size_t idx = (size_t)row * e.N_feat + col;
+          xv = e.x[idx] + a;
+          e.x[idx] = xv;
+          const float g = to_f32<T>(static_cast<const T*>(e.gain)[col]);
+          static_cast<T*>(e.xn)[idx] = from_f32<T>(xv * g);
+        }
+        float sq = xv * xv;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (lane == 0) s_red[ewarp * s_red_ld + (row - srow0)] += sq;
+        break;
+      }
+      case EPI_SWIGLU: {
+        const float v = a * s;
+        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+        if ((f & 1) == 0 && cvalid) {
+          const float h = silu_f(v) * other;
+          static_cast<T*>(e.out)[(size_t)row * e.ldo + (col >> 1)] = from_f32<T>(h);
+        }
+        break;
+      }
+      case EPI_KV: {
+        if (!cvalid) break;
+        const int kvd = e.n_kv * e.head_dim;
+        const int layer = col / (2 * kvd);
+        const int kind = (col / kvd) & 1;
+        const int c = col % kvd;
+        const int head = c / e.head_dim;
+        const int i = c % e.head_dim;
+        float v = a;
+        if (kind == 0) {
+          const int half = e.head_dim >> 1;
+          const int pf = (i < half) ? f + half : f - half;
+          const float pv = buf[r * kBufLd + pf];
+          const float2 cs = e.rope[(size_t)row * half + (i % half)];
+          v = (i < half) ? (v * cs.x - pv * cs.y) : (v * cs.x + pv * cs.y);
+        }
+        const int req = row_request(e.row_off, e.n_req, row);
+        const int pos = e.pos0[req] + (row - e.row_off[req]);
+        if (pos < 0 || pos >= e.cap) break;  // outside the request's cache slab
+        T* dst = static_cast<T*>(kind == 0 ? e.cache_k[layer] : e.cache_v[layer]);
+        dst[(((size_t)req * e.n_kv + head) * e.cap + pos) * e.head_dim + i] = from_f32<T>(v);
+        break;
+      }
+      case EPI_LOGITS: {
+        const int req = row / e.L;
+        const int j = row - req * e.L;
+        if (j >= 1 && cvalid)
+          e.logits[((size_t)req * (e.L - 1) + (j - 1)) * e.N_feat + col] = a * s;
+        break;
+      }
+      case EPI_STORE_F32: {
+        if (cvalid) e.logits[(size_t)row * e.ldo + col] = a;
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+// After all chunks of a RESID tile: fold the per-warp sums of squares.
+__device__ __forceinline__ void epi_resid_flush(const EpiParams& e, int ftile, int row0, int n,
+                                                const float* s_red, int s_red_ld, int nwarps,
+                                                int tid, int nthreads) {
+  for (int r = tid; r < n; r += nthreads) {
+    float acc = 0.f;
+    for (int w = 0; w < nwarps; ++w) acc += s_red[w * s_red_ld + r];
+    e.ssq_out[(size_t)ftile * e.M_rows + row0 + r] = acc;
+  }
+}
+
+}  // namespace dfl

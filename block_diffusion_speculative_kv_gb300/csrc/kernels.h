@@ -52,4 +52,23 @@ struct TreeAcceptLaunch {
 };
 void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st);
 
+// ---- block prologue and rotary tables (prologue.cu) ----
+struct BlockPrologueLaunch {
+  bool bf16;
+  const void* embed;   // [vocab][d]
+  const void* gain;    // [d] first attention-norm gain
+  const int* anchor;   // [n_req]
+  const int* ctx_len;  // [n_req]
+  int n_req, L, d, vocab, mask_id, head_dim;
+  float theta;
+  float* x;            // [n_req*L][d] fp32
+  void* xn;            // [n_req*L][d] T
+  float* ssq;          // [ceil(d/128)][n_req*L]
+  float2* rope;        // [n_req*L][head_dim/2]
+  int* status;
+};
+void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st);
+void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_rows, int head_dim,
+                        float theta, float2* rope, cudaStream_t st);
+
 }  // namespace dfl

@@ -1,0 +1,108 @@
+// Small per-call kernels that start the block pass and the injection.
+//
+// block_prologue (step a3): x_j = E[anchor] for j = 0 and E[mask] otherwise
+// ("DFlash: Block Diffusion for Flash Speculative Decoding", section 3.4.4,
+// block [anchor, mask x (L-1)]), written as the fp32 residual x, the
+// gain-scaled GEMM operand xn = x * g (first attention norm) and per-128-column
+// sums of squares for the RMS factor; plus the rotary (cos, sin) table of the
+// block positions ctx_len + j.
+// inject_rope: the rotary table of the injected cache positions.
+// Angles are formed and reduced in double precision (pos * theta^(-2i/hd)),
+// then rounded to fp32.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dfl {
+
+namespace {
+
+__device__ __forceinline__ float2 rope_cs(int pos, int i, int head_dim, float theta) {
+  const double inv = pow(static_cast<double>(theta), -2.0 * i / head_dim);
+  double s, c;
+  sincos(static_cast<double>(pos) * inv, &s, &c);
+  return make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
+                      const int* __restrict__ anchor, const int* __restrict__ ctx_len, int n_req,
+                      int L, int d, int vocab, int mask_id, int head_dim, float theta,
+                      float* __restrict__ x, T* __restrict__ xn, float* __restrict__ ssq,
+                      float2* __restrict__ rope, int* status) {
+  __shared__ float red[4];
+  const int R = n_req * L;
+  const int row = blockIdx.x;
+  const int req = row / L, j = row % L;
+  int tok = (j == 0) ? anchor[req] : mask_id;
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) record_status(status, DFLASH_ERR_INVALID_ARG);
+    tok = 0;
+  }
+  const int parts = (d + 127) / 128;
+  for (int p = 0; p < parts; ++p) {
+    const int c = p * 128 + threadIdx.x;
+    float v = 0.f;
+    if (c < d) {
+      v = to_f32<T>(embed[(size_t)tok * d + c]);
+      x[(size_t)row * d + c] = v;
+      xn[(size_t)row * d + c] = from_f32<T>(v * to_f32<T>(gain[c]));
+    }
+    float sq = v * v;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) ssq[(size_t)p * R + row] = red[0] + red[1] + red[2] + red[3];
+    __syncthreads();
+  }
+  const int half = head_dim / 2;
+  const int pos = ctx_len[req] + j;
+  for (int i = threadIdx.x; i < half; i += blockDim.x)
+    rope[(size_t)row * half + i] = rope_cs(pos, i, head_dim, theta);
+}
+
+__global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* __restrict__ pos0,
+                                   int n_req, int n_rows, int head_dim, float theta,
+                                   float2* __restrict__ rope) {
+  const int half = head_dim / 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)n_rows * half) return;
+  const int row = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+  int lo = 0, hi = n_req - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (row_off[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  const int pos = pos0[lo] + (row - row_off[lo]);
+  rope[idx] = rope_cs(pos, i, head_dim, theta);
+}
+
+}  // namespace
+
+void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st) {
+  const int R = a.n_req * a.L;
+  if (R <= 0) return;
+  if (a.bf16) {
+    block_prologue_kernel<__nv_bfloat16><<<R, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(a.embed), static_cast<const __nv_bfloat16*>(a.gain),
+        a.anchor, a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.theta, a.x,
+        static_cast<__nv_bfloat16*>(a.xn), a.ssq, a.rope, a.status);
+  } else {
+    block_prologue_kernel<float><<<R, 128, 0, st>>>(
+        static_cast<const float*>(a.embed), static_cast<const float*>(a.gain), a.anchor,
+        a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.theta, a.x,
+        static_cast<float*>(a.xn), a.ssq, a.rope, a.status);
+  }
+}
+
+void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_rows, int head_dim,
+                        float theta, float2* rope, cudaStream_t st) {
+  const long long n = (long long)n_rows * (head_dim / 2);
+  if (n <= 0) return;
+  inject_rope_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(
+      row_off, pos0, n_req, n_rows, head_dim, theta, rope);
+}
+
+}  // namespace dfl

@@ -251,6 +251,16 @@ dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes,
                             const int32_t* target_tok, int32_t* accept_len,
                             int32_t* accepted, int32_t* bonus, void* stream);
 
+/* The dense contraction every step above is built on, exposed on its own:
+ * Y[M][N] = X[M][K] . W[N][K]^T with bf16 X and W and fp32 Y, on the tcgen05
+ * tensor cores (the same kernel, work split and reduction the drafter's GEMMs
+ * use, with a plain fp32 store as epilogue).  Requires K % 64 == 0, N % 128 ==
+ * 0, X, W 16-byte aligned; M >= 0.  ws of dflash_linear_workspace_bytes(M, N,
+ * K) bytes, zero-initialised once. */
+size_t dflash_linear_workspace_bytes(int M, int N, int K);
+dflash_status dflash_linear_bf16(int M, int N, int K, const void* X, const void* W, float* Y,
+                                 void* ws, size_t ws_bytes, void* stream);
+
 /* Thread-local message for the calling thread's last non-OK status. */
 const char* dflash_last_error(void);
 int dflash_abi_version(void);

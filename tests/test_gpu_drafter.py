@@ -1,0 +1,185 @@
+"""GPU parity of KV injection (steps a1-a2) and the drafter block pass with LM
+head and top-K (steps a3-a6), through the C ABI, against the oracle on the
+same seeded inputs.
+
+Tolerances (from the pages' bar and the arithmetic): logits per row
+max|l_gpu - l_ora| / max|l_ora| <= 2e-2 for bf16 models, 1e-4 for fp32;
+injected cache entries the same per (layer, position).  The top-K sets may
+differ only by tokens whose oracle logit lies within delta of the oracle's
+K-th logit, delta = 2 * (that row's max logit error) + 1e-3 nats: both sides
+take the top-K decision on their own logits, so the decision can only flip
+where the logit error can reach (the 1e-3 nat tie window applies to identical
+logits, checked in test_gpu_topk_tree)."""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_kv_gb300 import synth
+from block_diffusion_speculative_kv_gb300.configs import WORKLOADS, DrafterShape
+from block_diffusion_speculative_kv_gb300.drafter import Drafter
+from oracle import drafter as od
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+class F64:
+    """Lazy float64 view of a torch tensor (bf16 has no NumPy dtype)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, idx):
+        return self.t[idx].float().cpu().numpy().astype(np.float64)
+
+    def __array__(self, dtype=None, copy=None):
+        return self.t.float().cpu().numpy().astype(np.float64)
+
+
+def oracle_weights(w):
+    out = {}
+    for k, v in w.items():
+        out[k] = [F64(t) for t in v] if isinstance(v, list) else F64(v)
+    return out
+
+
+def oracle_dims(s: DrafterShape):
+    return dict(n_layers=s.n_layers, d=s.d, n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim,
+                vocab=s.vocab, mask_id=s.mask_id, rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+
+
+def tol(s: DrafterShape):
+    return 1e-4 if s.dtype == "fp32" else 2e-2
+
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32), device=DEV)
+
+
+# ---------------------------------------------------------------------------
+# injection
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wid,rows_per_req,pos0", [
+    (0, [64], [0]),                   # fp32: the whole context in one call
+    (0, [5, 3], [10, 60]),            # fp32: two requests, ragged
+    (1, [16], [2032]),                # 4B shape: one cycle's worth at the tail
+    (1, [7, 16, 1], [0, 100, 2047]),  # ragged rows, last slot of the cache
+])
+def test_inject_matches_oracle(wid, rows_per_req, pos0):
+    wl = WORKLOADS[wid]
+    s = wl.shape
+    n_req = len(rows_per_req)
+    w = synth.drafter_weights(s, wl.seed, device=DEV)
+    if wid == 0:
+        w.update(synth.random_gains(s, wl.seed, device=DEV))
+    n_rows = sum(rows_per_req)
+    dr = Drafter(s, w, n_req=n_req, cap=wl.cap, max_inject_rows=n_rows, L=wl.L, K=wl.K)
+    feats = synth.features(n_rows, s, wl.seed, device=DEV)
+    row_off = np.concatenate([[0], np.cumsum(rows_per_req)])
+    dr.inject_kv(feats, _i32(row_off), _i32(pos0))
+    torch.cuda.synchronize()
+    assert dr.read_status() == 0
+    ow = oracle_weights(w)
+    f = od.fuse_features(F64(feats), ow["w_proj"])
+    for r in range(n_req):
+        rows = slice(row_off[r], row_off[r + 1])
+        pos = pos0[r] + np.arange(rows_per_req[r])
+        for l in range(s.n_layers):
+            K, V = od.inject_kv(f[rows], ow["uk"][l], ow["uv"][l], pos, s.n_kv, s.head_dim,
+                                s.rope_theta)
+            gk = dr.cache_k[l][r][:, pos].float().cpu().numpy()
+            gv = dr.cache_v[l][r][:, pos].float().cpu().numpy()
+            for ref, got in ((K, gk), (V, gv)):
+                err = np.max(np.abs(got - ref), axis=(0, 2)) / np.max(np.abs(ref), axis=(0, 2))
+                assert np.all(err <= tol(s)), (l, float(err.max()))
+        # slots outside the injected range stay untouched (zero)
+        mask = np.ones(wl.cap, dtype=bool)
+        mask[pos] = False
+        assert torch.count_nonzero(dr.cache_k[0][r][:, torch.from_numpy(mask).to(DEV)]) == 0
+
+
+# ---------------------------------------------------------------------------
+# the block pass
+# ---------------------------------------------------------------------------
+
+def _check_logits_topk(ref_logits, gpu_logits, gpu_ids, gpu_lp, K, tolerance):
+    rows = ref_logits.shape[0]
+    err = np.max(np.abs(gpu_logits - ref_logits), axis=1)
+    scale = np.max(np.abs(ref_logits), axis=1)
+    assert np.all(err / scale <= tolerance), float(np.max(err / scale))
+    ref_ids, ref_vals = od.topk(ref_logits, K)
+    lp_ref, lse_ref = od.log_softmax(ref_logits)
+    for r in range(rows):
+        delta = 2.0 * err[r] + 1e-3
+        kth = ref_vals[r, K - 1]
+        for tok in set(ref_ids[r].tolist()) ^ set(gpu_ids[r].tolist()):
+            assert abs(ref_logits[r, tok] - kth) <= delta, (r, tok)
+        # the GPU's logp of its own tokens agree with the oracle's logp of them
+        assert np.all(np.abs(gpu_lp[r] - lp_ref[r, gpu_ids[r]]) <= delta)
+        # and are sorted
+        assert np.all(np.diff(gpu_lp[r]) <= 0)
+
+
+def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None):
+    wl = WORKLOADS[wid]
+    s = wl.shape
+    w = synth.drafter_weights(s, wl.seed, device=DEV)
+    if gains:
+        w.update(synth.random_gains(s, wl.seed, device=DEV))
+    ctx = synth.context_lengths(wl)
+    max_ctx = int(ctx.max())
+    dr = Drafter(s, w, n_req=wl.n_req, cap=wl.cap, max_inject_rows=0, L=wl.L, K=wl.K,
+                 anchor_sees_block=anchor_sees_block)
+    ks, vs = synth.cache_prefix(s, wl.n_req, wl.cap, wl.seed, device=DEV)
+    for l in range(s.n_layers):
+        dr.cache_k[l].copy_(ks[l])
+        dr.cache_v[l].copy_(vs[l])
+    del ks, vs
+    anchors = synth.anchors(wl.n_req, s.vocab, s.mask_id, wl.seed)
+    D = wl.L - 1
+    ids = torch.empty(wl.n_req, D, wl.K, dtype=torch.int32, device=DEV)
+    lp = torch.empty(wl.n_req, D, wl.K, dtype=torch.float32, device=DEV)
+    logits = torch.empty(wl.n_req, D, s.vocab, dtype=torch.float32, device=DEV)
+    dr.draft_block(_i32(anchors), _i32(ctx), max_ctx, ids, lp, logits)
+    ids2, lp2 = torch.empty_like(ids), torch.empty_like(lp)
+    dr.draft_block(_i32(anchors), _i32(ctx), max_ctx, ids2, lp2)
+    torch.cuda.synchronize()
+    assert dr.read_status() == 0
+    assert torch.equal(ids, ids2) and torch.equal(lp, lp2), "two runs differ"
+    ow = oracle_weights(w)
+    dims = oracle_dims(s)
+    reqs = range(wl.n_req) if sample_reqs is None else sample_reqs
+    for r in reqs:
+        ck = [F64(dr.cache_k[l][r]) for l in range(s.n_layers)]
+        cv = [F64(dr.cache_v[l][r]) for l in range(s.n_layers)]
+        ref = od.drafter_block(ow, dims, ck, cv, int(ctx[r]), int(anchors[r]), wl.L,
+                               anchor_sees_block=anchor_sees_block)
+        _check_logits_topk(ref, logits[r].cpu().numpy().astype(np.float64),
+                           ids[r].cpu().numpy(), lp[r].cpu().numpy(), wl.K, tol(s))
+
+
+def test_draft_tiny_fp32():
+    _draft_case(0)
+
+
+def test_draft_tiny_fp32_gains_and_anchor_isolation():
+    _draft_case(0, gains=True)
+    _draft_case(0, anchor_sees_block=False, gains=True)
+
+
+def test_draft_qwen3_4b_shape():
+    _draft_case(1)
+
+
+def test_draft_qwen3_8b_shape_long_context():
+    _draft_case(2)
+
+
+def test_draft_batched_ragged_sampled():
+    # 32 requests with contexts U[512, 8192]: the shortest, the longest and one more
+    wl = WORKLOADS[3]
+    ctx = synth.context_lengths(wl)
+    pick = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 7})
+    _draft_case(3, sample_reqs=pick)

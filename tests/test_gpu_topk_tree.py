@@ -71,7 +71,11 @@ def test_topk_stress_workload_full_size():
     o_ids, o_lp = _oracle_topk(logits, wl.K)
     assert np.array_equal(ids, o_ids)
     assert np.allclose(lp, o_lp, atol=1e-5, rtol=0)
-    assert np.mean(ids[:, 0] == planted.numpy()) > 0.99
+    # sanity of the workload itself: the planted token (+8 on an N(0, 2) draw) is
+    # usually the argmax and almost always inside the top-K
+    pl = planted.numpy()
+    assert np.mean(ids[:, 0] == pl) > 0.8
+    assert np.mean((ids == pl[:, None]).any(axis=1)) > 0.9
     # the rows are normalised: the top-K mass is below one
     assert np.all(np.exp(lp.astype(np.float64)).sum(1) <= 1.0 + 1e-5)
 
