@@ -1,0 +1,531 @@
+#!/usr/bin/env python
+"""Drafter-cycle benchmark: inject + draft block + top-K + DDTree build.
+
+One step is one drafter cycle of the Qwen3-8B-shaped batch-1 workload
+(5 layers, hidden 4096, 32/8 heads of 128, FFN 12288, vocabulary 151936,
+8192 injected context positions, block L = 16, top-K 8, DDTree budget 256):
+  dflash_inject_kv    the 16 newest context positions (W_proj and U_K/U_V)
+  dflash_draft_block  5 layers + LM head + log-softmax + top-K
+  ddtree_build        Algorithm 1 + ancestor mask
+The acceptance walk is timed separately (accept_us).  Inputs are seeded
+synthetic data of those shapes (no trained weights or datasets exist here).
+
+Timed region: K replays of a CUDA graph of the cycle, CUDA events on the
+launching stream, barrier + synchronize on both sides, max over ranks.  Each
+cycle streams ~3.6 GB of weights and cache, far above the 129 MB L2, so no
+flush is needed between steps.  Per-kernel times (roofline, shares) come from
+traced eager cycles: CUDA events recorded around every kernel launch through
+the library's trace hook.  e2e repeats the cycle through the C-ABI calls with
+pinned host inputs and outputs, copies included.
+
+--impl reference times the CPU oracle on the same workload (bounded sample).
+Multi-GPU (torchrun): every rank runs an independent replica (batch-1 drafting
+does not shard); value is the sum of cycles/s over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "draft cycles/sec & µs/cycle (inject+draft+top-K+DDTree) at Qwen3-8B shape"
+UNIT = "cycles/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=60.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and max-over-ranks timing)
+# ---------------------------------------------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        bus = None
+        try:
+            p = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            pass
+        rows = [l.split(", ") for l in self.lines if l]
+        rows = [r for r in rows if len(r) >= 10]
+        if bus is not None:
+            mine = [r for r in rows if r[1].upper().endswith(bus[-12:])]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workload set-up (untimed)
+# ---------------------------------------------------------------------------
+
+def gemm_shapes(s, M_inject, R):
+    """(name, M, N, K) of every tensor-core GEMM of one cycle."""
+    out = [("w_proj", M_inject, s.d, s.n_feat * s.d_feat),
+           ("u_kv", M_inject, s.n_layers * 2 * s.kv_dim, s.d)]
+    for _ in range(s.n_layers):
+        out += [("qkv", R, s.qkv_dim, s.d), ("o", R, s.d, s.n_q * s.head_dim),
+                ("gate_up", R, 2 * s.d_ff, s.d), ("down", R, s.d, s.d_ff)]
+    out.append(("lm_head", R, s.vocab, s.d))
+    return out
+
+
+def algorithmic_bytes(s, wl, ctx):
+    """Bytes one cycle must move at least: every weight once, the context KV once,
+    the logits written and read once, the new features read once."""
+    es = 2 if s.dtype == "bf16" else 4
+    R = wl.n_req * wl.L
+    w = sum(N * K for _, _, N, K in gemm_shapes(s, wl.n_req * wl.L, R)) * es
+    kv = int(np.sum(ctx)) * s.n_layers * 2 * s.kv_dim * es
+    logits = 2 * wl.n_req * (wl.L - 1) * s.vocab * 4
+    feats = wl.n_req * wl.L * s.n_feat * s.d_feat * es
+    return w + kv + logits + feats, w
+
+
+class Cycle:
+    def __init__(self, wid):
+        from block_diffusion_speculative_kv_gb300 import binding as bd
+        from block_diffusion_speculative_kv_gb300 import synth
+        from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
+        from block_diffusion_speculative_kv_gb300.drafter import Drafter
+        self.bd = bd
+        self.wl = wl = WORKLOADS[wid]
+        self.s = s = wl.shape
+        dev = "cuda"
+        self.ctx = synth.context_lengths(wl)
+        T = int(self.ctx.max())
+        L, n_req = wl.L, wl.n_req
+        self.w = synth.drafter_weights(s, wl.seed, device=dev)
+        prefill_rows = int(np.sum(self.ctx - L))
+        self.dr = Drafter(s, self.w, n_req=n_req, cap=wl.cap,
+                          max_inject_rows=max(prefill_rows, n_req * L), L=L, K=wl.K)
+        i32 = dict(dtype=torch.int32, device=dev)
+        # untimed prefill: context [0, T-L) of every request from N(0,1) features
+        rows = (self.ctx - L).astype(np.int64)
+        off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+        feats = synth.features(int(off[-1]), s, wl.seed, stream=101, device=dev)
+        self.dr.inject_kv(feats, torch.as_tensor(off, **i32),
+                          torch.zeros(n_req, **i32))
+        del feats
+        # per-cycle inputs: the L newest positions [ctx-L, ctx) of each request
+        self.feats = synth.features(n_req * L, s, wl.seed, stream=102, device=dev)
+        self.row_off = torch.as_tensor(np.arange(n_req + 1, dtype=np.int32) * L, **i32)
+        self.pos0 = torch.as_tensor(self.ctx - L, **i32)
+        self.ctx_len = torch.as_tensor(self.ctx, **i32)
+        self.anchor = torch.as_tensor(synth.anchors(n_req, s.vocab, s.mask_id, wl.seed), **i32)
+        self.max_ctx = T
+        D = L - 1
+        self.ids = torch.empty(n_req, D, wl.K, **i32)
+        self.lp = torch.empty(n_req, D, wl.K, dtype=torch.float32, device=dev)
+        self.tree = bd.tree_buffers(n_req, wl.B, dev)
+        self.accept_len = torch.empty(n_req, **i32)
+        self.accepted = torch.empty(n_req, D, **i32)
+        self.bonus = torch.empty(n_req, **i32)
+        torch.cuda.synchronize()
+        self.target = None
+
+    def run(self):
+        self.dr.inject_kv(self.feats, self.row_off, self.pos0)
+        self.dr.draft_block(self.anchor, self.ctx_len, self.max_ctx, self.ids, self.lp)
+        self.bd.ddtree_build(self.lp, self.ids, self.anchor, self.wl.B, *self.tree)
+
+    def make_targets(self):
+        from block_diffusion_speculative_kv_gb300 import synth
+        torch.cuda.synchronize()
+        n_nodes = self.tree[0].cpu().numpy()
+        depth = self.tree[3].cpu().numpy()
+        tgt = synth.target_tokens(n_nodes, depth, self.lp.cpu().numpy(), self.ids.cpu().numpy(),
+                                  self.s.vocab, self.wl.target_agree, seed=self.wl.seed)
+        self.target = torch.as_tensor(tgt, device="cuda")
+
+    def accept(self):
+        self.bd.ddtree_accept(self.wl.L - 1, self.wl.B, self.tree[0], self.tree[1], self.tree[2],
+                              self.target, self.accept_len, self.accepted, self.bonus)
+
+
+class Tracer:
+    """Records CUDA events around every library kernel launch."""
+
+    def __init__(self):
+        self.open = []
+        self.done = []
+
+    def __call__(self, name, phase, stream):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(torch.cuda.current_stream())
+        if phase == 0:
+            self.open.append((name, ev))
+        else:
+            n, e0 = self.open.pop()
+            self.done.append((n, e0, ev))
+
+    def durations(self):
+        torch.cuda.synchronize()
+        out = {}
+        for n, e0, e1 in self.done:
+            out.setdefault(n, []).append(e0.elapsed_time(e1) * 1e3)   # us
+        return out
+
+
+def timed_region(fn, steps, warmup, world):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = ClockSampler()
+    clk.start()
+    time.sleep(0.3)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk.stop()
+    return e0.elapsed_time(e1), clk.summary()
+
+
+def traffic_from_profile(kernel_src):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    only if the kernel source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_qwen3_8b_b1.md")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    meta = {}
+    for line in open(path):
+        if line.startswith("<!-- ") and ":" in line:
+            k, v = line[5:].split("-->")[0].split(":", 1)
+            meta[k.strip()] = v.strip()
+    if meta.get("kernel_sha") != sha:
+        return None
+    try:
+        return float(meta["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_baseline(cyc, budget_s):
+    """Time the CPU oracle on one request's cycle (inject of the L newest rows,
+    the block pass, log-softmax/top-K, Algorithm 1) on this host's cores."""
+    from oracle import ddtree as odt
+    from oracle import drafter as od
+
+    class F64:
+        def __init__(self, t):
+            self.t = t
+
+        def __getitem__(self, i):
+            return self.t[i].float().numpy().astype(np.float64)
+
+        def __array__(self, dtype=None, copy=None):
+            return self.t.float().numpy().astype(np.float64)
+
+    s, wl = cyc.s, cyc.wl
+    host = {k: ([F64(t.cpu()) for t in v] if isinstance(v, list) else F64(v.cpu()))
+            for k, v in cyc.w.items()}
+    ck = [F64(cyc.dr.cache_k[l][0].cpu()) for l in range(s.n_layers)]
+    cv = [F64(cyc.dr.cache_v[l][0].cpu()) for l in range(s.n_layers)]
+    feats = F64(cyc.feats[:wl.L].cpu())
+    dims = dict(n_layers=s.n_layers, d=s.d, n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim,
+                vocab=s.vocab, mask_id=s.mask_id, rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+    T = int(cyc.ctx[0])
+    anchor = int(cyc.anchor[0].item())
+    t0 = time.perf_counter()
+    f = od.fuse_features(feats, host["w_proj"])
+    pos = T - wl.L + np.arange(wl.L)
+    for l in range(s.n_layers):
+        od.inject_kv(f, host["uk"][l], host["uv"][l], pos, s.n_kv, s.head_dim, s.rope_theta)
+    logits = od.drafter_block(host, dims, ck, cv, T, anchor, wl.L)
+    ids, lp, _ = od.logits_topk(logits, wl.K)
+    odt.build_tree(lp.astype(np.float32), ids, anchor, wl.B)
+    dt = time.perf_counter() - t0
+    return {"value": 1.0 / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "one full cycle of request 0 (inject of 16 rows, 5 layers over 8192 "
+                      "context entries, LM head over 151936 tokens, top-8, B=256 tree), "
+                      "NumPy float64 with its threaded BLAS; %.1f s" % dt}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    torch.cuda.set_device(0)
+    cyc = Cycle(args.workload)
+    times = []
+    t_start = time.perf_counter()
+    steps_done = 0
+    warm = min(args.warmup, 1)
+    for i in range(warm + args.steps):
+        b = cpu_baseline(cyc, args.cpu_budget_s)
+        if i >= warm:
+            times.append(1.0 / b["value"])
+            steps_done += 1
+        if time.perf_counter() - t_start > 240 and steps_done >= 1:
+            break
+    ms = 1e3 * statistics.mean(times)
+    val = 1e3 / ms
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+            "steps": steps_done, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cyc.wl.name},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "full oracle cycles of request 0; steps capped to end "
+                                       "within a few minutes"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    from block_diffusion_speculative_kv_gb300 import binding as bd
+    cyc = Cycle(args.workload)
+    s, wl = cyc.s, cyc.wl
+
+    # ---- launches per cycle (trace hook, eager) ----
+    count = [0]
+
+    def counter(name, phase, stream):
+        if phase == 0:
+            count[0] += 1
+
+    bd.set_trace_hook(counter)
+    cyc.run()
+    bd.set_trace_hook(None)
+    launches_per_cycle = count[0]
+    torch.cuda.synchronize()
+    cyc.make_targets()
+
+    # ---- graph of one cycle ----
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            cyc.run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cyc.run()
+    torch.cuda.synchronize()
+
+    ms_total, clocks = timed_region(graph.replay, args.steps, max(args.warmup, 3), world)
+    ms_step = max_over_ranks(ms_total / args.steps, world)
+    status = cyc.dr.read_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+
+    # ---- per-kernel times from traced eager cycles ----
+    tr = Tracer()
+    bd.set_trace_hook(tr)
+    for _ in range(3):
+        cyc.run()
+    bd.set_trace_hook(None)
+    dur = tr.durations()
+    per_cycle = {k: sum(v) / 3.0 for k, v in dur.items()}
+    launches = {k: len(v) // 3 for k, v in dur.items()}
+    total_k = sum(per_cycle.values())
+    shares = {k: round(v / total_k, 4) for k, v in sorted(per_cycle.items(), key=lambda x: -x[1])}
+
+    # ---- acceptance walk on its own ----
+    for _ in range(3):
+        cyc.accept()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(20):
+        cyc.accept()
+    a1.record()
+    torch.cuda.synchronize()
+    accept_us = a0.elapsed_time(a1) * 1e3 / 20
+
+    # ---- roofline of the dominant kernel (the tensor-core GEMM) ----
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peaks = json.load(open(peaks_path))
+        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        hbm_peak, peak_src = 6800.0, "fallback"
+    total_bytes, w_bytes = algorithmic_bytes(s, wl, cyc.ctx)
+    R = wl.n_req * wl.L
+    gemm_bytes = 0
+    for _, M, N, K in gemm_shapes(s, wl.n_req * wl.L, R):
+        gemm_bytes += 2 * (N * K + M * K) + 4 * M * N
+    n_gemm = launches.get("gemm_tc", 1)
+    gemm_us = per_cycle.get("gemm_tc", float("nan"))
+    achieved = (gemm_bytes / n_gemm) / (gemm_us / n_gemm * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gemm_tc", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4),
+                "bytes_per_launch": int(gemm_bytes / n_gemm),
+                "us_per_launch": round(gemm_us / n_gemm, 2),
+                "traffic": traffic_from_profile(os.path.join(
+                    ROOT, "block_diffusion_speculative_kv_gb300", "csrc", "gemm_tc.cu"))}
+    cycle_gbs = total_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- e2e: C-ABI calls with pinned host buffers, copies in the timed region ----
+    h_feats = cyc.feats.cpu().pin_memory()
+    h_anchor = cyc.anchor.cpu().pin_memory()
+    h_ctx = cyc.ctx_len.cpu().pin_memory()
+    outs = [cyc.ids, cyc.lp] + list(cyc.tree)
+    h_outs = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = h_feats.numel() * h_feats.element_size() + h_anchor.numel() * 4 + h_ctx.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def e2e_step():
+        cyc.feats.copy_(h_feats, non_blocking=True)
+        cyc.anchor.copy_(h_anchor, non_blocking=True)
+        cyc.ctx_len.copy_(h_ctx, non_blocking=True)
+        cyc.run()
+        for h, o in zip(h_outs, outs):
+            h.copy_(o, non_blocking=True)
+
+    ms_e2e_total, _ = timed_region(e2e_step, args.steps, 3, world)
+    ms_e2e = max_over_ranks(ms_e2e_total / args.steps, world)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline(cyc, args.cpu_budget_s)
+        except Exception as ex:  # report, do not hide
+            cpu = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"failed: {type(ex).__name__}: {ex}"}
+
+    value = world * 1e3 / ms_step
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4),
+        "us_per_cycle": round(ms_step * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "n_layers": s.n_layers, "d": s.d, "heads": [s.n_q, s.n_kv],
+                   "head_dim": s.head_dim, "d_ff": s.d_ff, "vocab": s.vocab,
+                   "ctx": int(cyc.ctx.max()), "L": wl.L, "K": wl.K, "B": wl.B,
+                   "n_req": wl.n_req, "parallelism": "replicas" if world > 1 else "single",
+                   "timed": "CUDA graph of the cycle",
+                   "l2": "inputs larger than L2 (%.2f GB per cycle vs 129 MB)" % (total_bytes / 1e9)},
+        "roofline": roofline,
+        "cycle_hbm": {"algorithmic_bytes": int(total_bytes), "achieved_gbs": round(cycle_gbs, 1),
+                      "frac": round(cycle_gbs / hbm_peak, 4)},
+        "kernel_us_per_cycle": {k: round(v, 1) for k, v in per_cycle.items()},
+        "kernel_share": shares,
+        "accept_us": round(accept_us, 2),
+        "e2e": {"value": round(world * 1e3 / ms_e2e, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(ms_e2e, 4), "path": "C-ABI calls, eager"},
+        "gpu_launches": launches_per_cycle * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

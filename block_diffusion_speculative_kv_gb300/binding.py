@@ -74,7 +74,10 @@ _SIGS = {
     "ddtree_accept": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dflash_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_linear_bf16": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dflash_set_trace_hook": (None, [_vp, _vp]),
 }
+
+TRACE_FN = C.CFUNCTYPE(None, C.c_void_p, C.c_char_p, C.c_int, C.c_void_p)
 
 
 def lib():
@@ -92,6 +95,25 @@ def lib():
             f.argtypes = args
         _lib = l
     return _lib
+
+
+def set_trace_hook(fn) -> None:
+    """Install fn(name: str, phase: int, stream_ptr: int) around every kernel
+    launch (None removes it).  Keeps a reference to the ctypes thunk."""
+    global _trace_thunk
+    if fn is None:
+        lib().dflash_set_trace_hook(None, None)
+        _trace_thunk = None
+        return
+
+    def _cb(user, name, phase, stream):
+        fn(name.decode(), phase, stream or 0)
+
+    _trace_thunk = TRACE_FN(_cb)
+    lib().dflash_set_trace_hook(C.cast(_trace_thunk, C.c_void_p), None)
+
+
+_trace_thunk = None
 
 
 def exported_symbols() -> List[str]:

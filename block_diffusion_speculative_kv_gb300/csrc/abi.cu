@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -44,6 +45,16 @@ int num_sms() {
 
 size_t ws_header_bytes() { return 256; }
 
+namespace {
+std::atomic<dflash_trace_fn> g_trace_fn{nullptr};
+std::atomic<void*> g_trace_user{nullptr};
+}  // namespace
+
+void trace(const char* kernel, int phase, cudaStream_t st) {
+  dflash_trace_fn fn = g_trace_fn.load(std::memory_order_acquire);
+  if (fn) fn(g_trace_user.load(std::memory_order_relaxed), kernel, phase, st);
+}
+
 }  // namespace dfl
 
 using namespace dfl;
@@ -56,6 +67,11 @@ using namespace dfl;
 extern "C" {
 
 const char* dflash_last_error(void) { return g_err; }
+
+void dflash_set_trace_hook(dflash_trace_fn fn, void* user) {
+  g_trace_user.store(user, std::memory_order_relaxed);
+  g_trace_fn.store(fn, std::memory_order_release);
+}
 int dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
 
 dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, void* stream) {

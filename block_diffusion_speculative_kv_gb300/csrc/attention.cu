@@ -415,7 +415,11 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
                            160 * 1024);
       set = true;
     }
-    attn_split_kernel<128><<<grid, 128, smem, st>>>(p);
+    {
+      TraceScope ts("attn_split", st);
+      attn_split_kernel<128><<<grid, 128, smem, st>>>(p);
+    }
+    TraceScope ts("attn_combine", st);
     attn_combine_kernel<128><<<cgrid, 128, 0, st>>>(p);
   } else if (head_dim == 64) {
     static bool set = false;
@@ -424,7 +428,11 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
                            160 * 1024);
       set = true;
     }
-    attn_split_kernel<64><<<grid, 128, smem, st>>>(p);
+    {
+      TraceScope ts("attn_split", st);
+      attn_split_kernel<64><<<grid, 128, smem, st>>>(p);
+    }
+    TraceScope ts("attn_combine", st);
     attn_combine_kernel<64><<<cgrid, 128, 0, st>>>(p);
   } else {
     return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
@@ -435,6 +443,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
 dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStream_t st) {
   const int total = p.n_req * p.n_q * p.L;
   const int blocks = (total + 3) / 4;
+  TraceScope ts("attn_f32", st);
   if (head_dim == 128) attn_f32_kernel<128><<<blocks, 128, 0, st>>>(p);
   else if (head_dim == 64) attn_f32_kernel<64><<<blocks, 128, 0, st>>>(p);
   else return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");

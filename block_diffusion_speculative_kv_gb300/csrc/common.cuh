@@ -64,4 +64,13 @@ __host__ __device__ __forceinline__ size_t align_up(size_t a, size_t b) {
 // Number of SMs of the current device (cached per device on the host).
 int num_sms();
 
+// Launch tracing (dflash_set_trace_hook): host callbacks around each launch.
+void trace(const char* kernel, int phase, cudaStream_t st);
+struct TraceScope {
+  const char* name;
+  cudaStream_t st;
+  TraceScope(const char* n, cudaStream_t s) : name(n), st(s) { trace(name, 0, st); }
+  ~TraceScope() { trace(name, 1, st); }
+};
+
 }  // namespace dfl

@@ -223,6 +223,7 @@ void launch_build_t(const TreeBuildLaunch& a, cudaStream_t st) {
     attr_set = true;
   }
   dim3 grid(ceil_div(a.n_req, kBuildWarps));
+  TraceScope ts("ddtree_build", st);
   ddtree_build_kernel<SMAX><<<grid, kBuildWarps * 32, smem, st>>>(
       a.n_req, a.D, a.K, a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
       a.depth, a.rank, a.mask);
@@ -285,6 +286,7 @@ void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st) {
 void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st) {
   if (a.n_req <= 0) return;
   const int warps = 4;
+  TraceScope ts("ddtree_accept", st);
   ddtree_accept_kernel<<<ceil_div(a.n_req, warps), warps * 32, 0, st>>>(
       a.n_req, a.D, a.B, a.n_nodes, a.tok, a.parent, a.target, a.accept_len, a.accepted,
       a.bonus);

@@ -76,6 +76,7 @@ dflash_status launch_gemm_f32(const float* X, long long ldx, const float* W, int
                               int N_feat, int K, const EpiParams& epi, cudaStream_t st) {
   if (M_rows <= 0) return DFLASH_OK;
   dim3 grid(ceil_div(N_feat, kTileN), ceil_div(M_rows, kChunk));
+  TraceScope ts("gemm_f32", st);
   gemm_f32_kernel<<<grid, 128, 0, st>>>(X, ldx, W, M_rows, N_feat, K, epi);
   return check_launch("gemm_f32");
 }

@@ -418,6 +418,7 @@ dflash_status launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, con
   p.status = status;
   p.epi = epi;
   set_smem_attr_once<__nv_bfloat16>(pl.smem_bytes);
+  TraceScope ts("gemm_tc", st);
   gemm_tc_kernel<__nv_bfloat16><<<pl.grid, kThreads, pl.smem_bytes, st>>>(tmW, tmX, p);
   return check_launch("gemm_tc");
 }

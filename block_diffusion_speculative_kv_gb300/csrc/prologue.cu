@@ -84,6 +84,7 @@ __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* _
 void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st) {
   const int R = a.n_req * a.L;
   if (R <= 0) return;
+  TraceScope ts("block_prologue", st);
   if (a.bf16) {
     block_prologue_kernel<__nv_bfloat16><<<R, 128, 0, st>>>(
         static_cast<const __nv_bfloat16*>(a.embed), static_cast<const __nv_bfloat16*>(a.gain),
@@ -101,6 +102,7 @@ void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_ro
                         float theta, float2* rope, cudaStream_t st) {
   const long long n = (long long)n_rows * (head_dim / 2);
   if (n <= 0) return;
+  TraceScope ts("inject_rope", st);
   inject_rope_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(
       row_off, pos0, n_req, n_rows, head_dim, theta, rope);
 }

@@ -267,6 +267,7 @@ void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
   chunk = ceil_div(chunk, 8) * 8;
   TopkPart part{a.part, 2 + 2 * KMAX};
   dim3 grid(a.rows * a.splits);
+  TraceScope ts("lse_topk", st);
   if (vec_ok) {
     topk_kernel<T, KMAX, true><<<grid, kTopkThreads, 0, st>>>(
         static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,

@@ -261,6 +261,14 @@ size_t dflash_linear_workspace_bytes(int M, int N, int K);
 dflash_status dflash_linear_bf16(int M, int N, int K, const void* X, const void* W, float* Y,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* Launch tracing.  When a hook is set, the library calls it on the host right
+ * before (phase 0) and right after (phase 1) it enqueues each kernel, with the
+ * kernel's name and the stream, so a caller can record CUDA events around
+ * every kernel (also while a stream is being captured into a graph).  One hook
+ * per process; NULL removes it.  The hook must not call back into the library. */
+typedef void (*dflash_trace_fn)(void* user, const char* kernel, int phase, void* stream);
+void dflash_set_trace_hook(dflash_trace_fn fn, void* user);
+
 /* Thread-local message for the calling thread's last non-OK status. */
 const char* dflash_last_error(void);
 int dflash_abi_version(void);
