@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
+    ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "topk_stress", "tree_stress"],
+                    default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
 
@@ -377,8 +379,63 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def run_case(args):
+    """One kernel on its own, launched back to back (inputs larger than L2)."""
+    from block_diffusion_speculative_kv_gb300 import binding as bd
+    from block_diffusion_speculative_kv_gb300 import synth
+    from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda").manual_seed(1)
+    if args.case in ("lm_head_gemm", "down_gemm"):
+        M, N, K = (16, 151936, 4096) if args.case == "lm_head_gemm" else (16, 4096, 12288)
+        copies = max(1, int(math.ceil(400e6 / (2 * N * K))))   # rotate > L2 of weights
+        X = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+        Ws = [torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+              for _ in range(copies)]
+        Y = torch.empty(M, N, device="cuda")
+        ws = torch.zeros(bd.linear_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        fn_i = [0]
+
+        def fn():
+            bd.linear_bf16(X, Ws[fn_i[0] % copies], Y, ws)
+            fn_i[0] += 1
+        nbytes = 2 * N * K + 2 * M * K + 4 * M * N
+    elif args.case == "topk_stress":
+        wl = WORKLOADS[4]
+        logits, _ = synth.stress_logits(wl.n_req, wl.D, wl.vocab, wl.seed, device="cuda")
+        rows = logits.shape[0]
+        ids = torch.empty(rows, wl.K, dtype=torch.int32, device="cuda")
+        lp = torch.empty(rows, wl.K, device="cuda")
+        ws = torch.zeros(bd.topk_workspace_bytes(rows, wl.vocab, wl.K), dtype=torch.uint8,
+                         device="cuda")
+
+        def fn():
+            bd.logits_topk(logits, wl.K, ids, lp, ws)
+        nbytes = logits.numel() * 2
+    else:
+        wl = WORKLOADS[4]
+        lp, idt = synth.random_topk_table(wl.n_req, wl.D, wl.K, wl.vocab, wl.seed)
+        lp_d, id_d = torch.from_numpy(lp).cuda(), torch.from_numpy(idt).cuda()
+        roots = torch.zeros(wl.n_req, dtype=torch.int32, device="cuda")
+        bufs = bd.tree_buffers(wl.n_req, wl.B, "cuda")
+
+        def fn():
+            bd.ddtree_build(lp_d, id_d, roots, wl.B, *bufs)
+        nbytes = 0
+    ms, clocks = timed_region(fn, args.steps, max(args.warmup, 3), 1)
+    us = ms * 1e3 / args.steps
+    out = {"case": args.case, "us_per_launch": round(us, 2), "steps": args.steps,
+           "clocks": clocks}
+    if nbytes:
+        out["gbs"] = round(nbytes / (us * 1e-6) / 1e9, 1)
+    print(json.dumps(out))
+
+
 def main():
     args = parse()
+    if args.case:
+        run_case(args)
+        return
     rank, world, local = dist_init()
     if args.impl == "reference":
         run_reference(args, rank, world)
