@@ -75,6 +75,7 @@ _SIGS = {
     "dflash_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_linear_bf16": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_set_trace_hook": (None, [_vp, _vp]),
+    "dflash_logits_topk_noalloc": (_i, [_i, _i, _i, _i, _vp, _i, _vp, _vp, _vp]),
 }
 
 TRACE_FN = C.CFUNCTYPE(None, C.c_void_p, C.c_char_p, C.c_int, C.c_void_p)
@@ -177,6 +178,16 @@ def logits_topk(logits: torch.Tensor, K: int, ids: torch.Tensor, logp: torch.Ten
     _check(lib().dflash_logits_topk(rows, vocab, ld, _dtype_code(logits), _ptr(logits), K,
                                     _ptr(ids), _ptr(logp), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def logits_topk_noalloc(logits: torch.Tensor, K: int, ids: torch.Tensor, logp: torch.Tensor,
+                        vocab: Optional[int] = None, stream=None):
+    """Step a6 without a workspace, for callers that cannot allocate device
+    memory at this point (the library keeps a fixed scratch array per device)."""
+    rows, ld = logits.shape
+    vocab = ld if vocab is None else vocab
+    _check(lib().dflash_logits_topk_noalloc(rows, vocab, ld, _dtype_code(logits), _ptr(logits),
+                                            K, _ptr(ids), _ptr(logp), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -215,6 +215,24 @@ dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const v
                                  int K, int32_t* ids, float* logp,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* Step a6 for callers that cannot provide a workspace.  The pages have no
+ * counterpart: this variant exists for callers that cannot allocate device
+ * memory when they run this step (a serving loop whose device memory is carved
+ * up once at start-up and that must not call cudaMalloc afterwards, since that
+ * can synchronise the device; a plugin host that passes inputs and outputs but
+ * offers no scratch).  Same arguments, kernel and results as
+ * dflash_logits_topk, without ws: the scratch lives in a fixed array inside the
+ * library image (about 286 KB on every device that loads the library, held
+ * until the process exits).  Limits: rows <= 4096, larger requests return
+ * DFLASH_ERR_UNSUPPORTED.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  Every call on a device shares the array and
+ * clears its counters first, so calls that overlap on the GPU race: order them
+ * on one stream.  Allocates nothing. */
+dflash_status dflash_logits_topk_noalloc(int rows, int vocab, int ld, int dtype,
+                                         const void* logits, int K, int32_t* ids, float* logp,
+                                         void* stream);
+
 /* Step a7: DDTree tree construction, Algorithm 1 (DDTree page, 3.4.4), plus the
  * flattened tree and its ancestor-only mask (3.4.5).  Per request r:
  *   topk_logp fp32 [n_req][D][K] log q of the rank-k token at depth d+1,
