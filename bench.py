@@ -54,7 +54,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
-    ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "topk_stress", "tree_stress"],
+    ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
+                                       "tree_stress", "tree_b1"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -386,8 +387,9 @@ def run_case(args):
     from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda").manual_seed(1)
-    if args.case in ("lm_head_gemm", "down_gemm"):
-        M, N, K = (16, 151936, 4096) if args.case == "lm_head_gemm" else (16, 4096, 12288)
+    if args.case in ("lm_head_gemm", "down_gemm", "o_gemm"):
+        M, N, K = {"lm_head_gemm": (16, 151936, 4096), "down_gemm": (16, 4096, 12288),
+                   "o_gemm": (16, 4096, 4096)}[args.case]
         copies = max(1, int(math.ceil(400e6 / (2 * N * K))))   # rotate > L2 of weights
         X = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
         Ws = [torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
@@ -413,8 +415,8 @@ def run_case(args):
             bd.logits_topk(logits, wl.K, ids, lp, ws)
         nbytes = logits.numel() * 2
     else:
-        wl = WORKLOADS[4]
-        lp, idt = synth.random_topk_table(wl.n_req, wl.D, wl.K, wl.vocab, wl.seed)
+        wl = WORKLOADS[4] if args.case == "tree_stress" else WORKLOADS[2]
+        lp, idt = synth.random_topk_table(wl.n_req, wl.D, wl.K, 151936, wl.seed)
         lp_d, id_d = torch.from_numpy(lp).cuda(), torch.from_numpy(idt).cuda()
         roots = torch.zeros(wl.n_req, dtype=torch.int32, device="cuda")
         bufs = bd.tree_buffers(wl.n_req, wl.B, "cuda")

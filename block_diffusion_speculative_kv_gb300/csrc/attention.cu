@@ -295,8 +295,10 @@ attn_split_kernel(const AttnParams p) {
   (void)nwarps;
 }
 
-// Merge the partials of one (request, KV head): 4 query rows per CTA, a warp
-// per row, 4 dims per lane (HD = 128) or 2 (HD = 64).
+// Merge the partials of one (request, KV head) with log-sum-exp rescaling: a
+// warp per query row (4 rows per CTA), lanes over the head dimension.  The
+// chunk maxima are gathered 32 at a time, then the rescaled partial outputs
+// are accumulated with several chunks' loads in flight.
 template <int HD>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const AttnParams p) {
@@ -308,21 +310,46 @@ attn_combine_kernel(const AttnParams p) {
   const int nparts = p.n_chunks + 1;
   const size_t base = ((size_t)req * p.n_kv + g) * nparts * QR;
   float M = -CUDART_INF_F;
-  for (int c = 0; c < nparts; ++c) M = fmaxf(M, p.part_ml[(base + (size_t)c * QR + r) * 2]);
+  for (int c0 = 0; c0 < nparts; c0 += 32) {
+    const int c = c0 + lane;
+    if (c < nparts) {
+      const size_t row = base + (size_t)c * QR + r;
+      if (p.part_ml[row * 2 + 1] > 0.f) M = fmaxf(M, p.part_ml[row * 2]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   constexpr int DPL = HD / 32;
   float acc[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
   float Lsum = 0.f;
-  for (int c = 0; c < nparts; ++c) {
-    const size_t row = base + (size_t)c * QR + r;
-    const float l = p.part_ml[row * 2 + 1];
-    if (l == 0.f) continue;
-    const float w = exp2f(p.part_ml[row * 2] - M);
-    Lsum += w * l;
-    const float* src = p.part_o + row * HD + lane * DPL;
+  constexpr int U = 4;
+  for (int c0 = 0; c0 < nparts; c0 += U) {
+    float w[U], l[U], v[U][DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] += w * src[i];
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u;
+      w[u] = 0.f;
+      l[u] = 0.f;
+      if (c < nparts) {
+        const size_t row = base + (size_t)c * QR + r;
+        l[u] = p.part_ml[row * 2 + 1];
+        w[u] = (l[u] > 0.f) ? exp2f(p.part_ml[row * 2] - M) : 0.f;
+        const float* src = p.part_o + row * HD + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) v[u][i] = (l[u] > 0.f) ? src[i] : 0.f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) v[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      Lsum += w[u] * l[u];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] += w[u] * v[u][i];
+    }
   }
   const float inv = 1.f / Lsum;
   const int h = g * p.G + r / p.L, j = r % p.L;

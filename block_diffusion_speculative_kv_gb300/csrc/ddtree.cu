@@ -9,16 +9,19 @@
 // GPU formulation of the heap.  The candidates alive at any time are exactly
 // one per "open" parent: the parent's next unpopped child rank (children of a
 // node are popped in rank order, since a sibling is offered only after its
-// predecessor pops).  So the heap is kept as a set of slots, one per open
-// parent, spread over the 32 lanes of a warp (slot s lives in lane s % 32,
-// register s / 32).  A pop is a warp-wide maximum over 64-bit keys
-// (order-preserving score bits, then the complemented creation counter, so
-// equal scores pop in creation order) done with two redux.sync reductions;
-// the popped slot advances to its next rank in place (or closes), a new slot
-// opens for the popped node's first child, and only the lanes that own those
-// two slots refresh their local best.  Candidate scores are the parent score
-// plus one log-probability, a single fp32 add, so the result is bit-identical
-// to a plain binary-heap implementation of the same rule.
+// predecessor pops).  So the heap is kept as a set of slots in shared memory,
+// one per open parent; slot s belongs to lane s % 32, and every lane keeps the
+// best key among its own slots in a register.  Keys are 64-bit:
+// order-preserving score bits, then the complemented creation counter, so
+// equal scores pop in creation order.  A pop is a warp-wide maximum of the
+// lanes' bests (redux.sync on the high word, and on the low word only when the
+// high word ties); the popped slot advances to its next rank in place (or
+// closes), a new slot opens for the popped node's first child, and the winning
+// lane's best is recomputed by the whole warp (each lane reads one of that
+// lane's slots, then one more warp maximum), so a pop costs O(1) warp
+// instructions whatever the budget.  Candidate scores are the parent score plus
+// one log-probability, a single fp32 add, so the result is bit-identical to a
+// plain binary-heap implementation of the same rule.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,20 +47,44 @@ struct WarpSmem {
   int* par;         // [B+1]
   int* dep;         // [B+1]
   int* rnk;         // [B+1]
+  uint64_t* key;    // [B+1] slot keys (0 = closed)
+  uint32_t* info;   // [B+1] slot (parent, depth, rank)
+  float* psc;       // [B+1] slot parent score
   uint32_t* stage;  // [32][W]
 };
 
 __host__ __device__ inline size_t build_warp_bytes(int D, int K, int B) {
   const int W = (B + 1 + 31) / 32;
   size_t b = 0;
+  b += align_up(sizeof(uint64_t) * (B + 1), 16);
   b += align_up(sizeof(float) * D * K, 16);
   b += align_up(sizeof(int) * D * K, 16);
   b += 4 * align_up(sizeof(int) * (B + 1), 16);
+  b += align_up(sizeof(uint32_t) * (B + 1), 16);
+  b += align_up(sizeof(float) * (B + 1), 16);
   b += align_up(sizeof(uint32_t) * 32 * W, 16);
   return b;
 }
 
-template <int SMAX>
+// Warp-wide maximum of 64-bit keys; returns the lane holding it (keys unique
+// unless all are 0) and the key.
+__device__ __forceinline__ int warp_argmax_key(uint64_t k, uint64_t& kmax) {
+  const unsigned FULL = 0xffffffffu;
+  const uint32_t hi = static_cast<uint32_t>(k >> 32);
+  const uint32_t lo = static_cast<uint32_t>(k);
+  const uint32_t mhi = __reduce_max_sync(FULL, hi);
+  unsigned b = __ballot_sync(FULL, hi == mhi);
+  uint32_t mlo;
+  if (__popc(b) == 1) {
+    mlo = __shfl_sync(FULL, lo, __ffs(b) - 1);
+  } else {
+    mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
+    b = __ballot_sync(FULL, hi == mhi && lo == mlo);
+  }
+  kmax = (static_cast<uint64_t>(mhi) << 32) | mlo;
+  return __ffs(b) - 1;
+}
+
 __global__ void __launch_bounds__(kBuildWarps * 32)
 ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
                     const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
@@ -69,19 +96,21 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   const int wib = threadIdx.x >> 5;
   const int req = blockIdx.x * kBuildWarps + wib;
   if (req >= n_req) return;
-  const unsigned FULL = 0xffffffffu;
   const int W = (B + 1 + 31) / 32;
 
   unsigned char* base = smem_raw + build_warp_bytes(D, K, B) * wib;
   WarpSmem sm;
   {
     size_t off = 0;
+    sm.key = reinterpret_cast<uint64_t*>(base + off); off += align_up(sizeof(uint64_t) * (B + 1), 16);
     sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
     sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
     sm.tok = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
     sm.par = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
     sm.dep = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
     sm.rnk = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
+    sm.info = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * (B + 1), 16);
+    sm.psc = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * (B + 1), 16);
     sm.stage = reinterpret_cast<uint32_t*>(base + off);
   }
   const float* lp_r = lp_g + (size_t)req * D * K;
@@ -93,44 +122,31 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   __syncwarp();
 
   // ---- Algorithm 1 ----
-  uint64_t key[SMAX];
-  uint32_t info[SMAX];
-  float psc[SMAX];
-#pragma unroll
-  for (int j = 0; j < SMAX; ++j) { key[j] = 0; info[j] = 0; psc[j] = 0.f; }
-  uint64_t lbest = 0;
-  int lbj = 0;
+  uint64_t lbest = 0;  // best key among this lane's slots
+  int lbs = 0;         // its slot index
   int n = 0, n_slots = 0;
   uint32_t seq = 0;
   if (B > 0) {
     if (lane == 0) {
-      key[0] = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
-      info[0] = pack_info(0, 1, 1);
-      psc[0] = 0.f;
-      lbest = key[0];
-      lbj = 0;
+      const uint64_t k0 = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
+      sm.key[0] = k0;
+      sm.info[0] = pack_info(0, 1, 1);
+      sm.psc[0] = 0.f;
+      lbest = k0;
+      lbs = 0;
     }
     n_slots = 1;
     seq = 1;
   }
+  __syncwarp();
   while (n < B) {
-    const uint32_t hi = static_cast<uint32_t>(lbest >> 32);
-    const uint32_t lo = static_cast<uint32_t>(lbest);
-    const uint32_t mhi = __reduce_max_sync(FULL, hi);
-    if (mhi == 0u) break;  // no candidate left
-    const uint32_t mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
-    const int w = __ffs(__ballot_sync(FULL, hi == mhi && lo == mlo)) - 1;
-    uint32_t winfo = 0;
-    float wpsc = 0.f;
-    if (lane == w) {
-#pragma unroll
-      for (int j = 0; j < SMAX; ++j)
-        if (j == lbj) { winfo = info[j]; wpsc = psc[j]; }
-    }
-    winfo = __shfl_sync(FULL, winfo, w);
-    wpsc = __shfl_sync(FULL, wpsc, w);
-    const int wj = __shfl_sync(FULL, lbj, w);
-    const float wscore = from_ordered_bits(mhi);
+    uint64_t kmax;
+    const int w = warp_argmax_key(lbest, kmax);
+    if (kmax == 0) break;  // no candidate left
+    const int slot = __shfl_sync(0xffffffffu, lbs, w);
+    const uint32_t winfo = sm.info[slot];
+    const float wpsc = sm.psc[slot];
+    const float wscore = from_ordered_bits(static_cast<uint32_t>(kmax >> 32));
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
     const int r = (winfo >> 16) & 0x3F;
@@ -140,41 +156,47 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
       sm.par[n] = p; sm.dep[n] = d; sm.rnk[n] = r;
     }
     // next sibling: the popped slot advances in place (or closes)
-    if (r < K) {
-      if (lane == w) {
-        const uint64_t k2 = make_key(__fadd_rn(wpsc, sm.lp[(d - 1) * K + r]), seq);
-#pragma unroll
-        for (int j = 0; j < SMAX; ++j)
-          if (j == wj) { key[j] = k2; info[j] = pack_info(p, d, r + 1); }
-      }
-      ++seq;
-    } else if (lane == w) {
-#pragma unroll
-      for (int j = 0; j < SMAX; ++j)
-        if (j == wj) key[j] = 0;
-    }
-    // first child: a new slot for the popped node
-    int child_lane = -1, cj = 0;
-    uint64_t ck = 0;
-    if (d < D) {
-      const int idx = n_slots++;
-      child_lane = idx & 31;
-      cj = idx >> 5;
-      if (lane == child_lane) {
-        ck = make_key(__fadd_rn(wscore, sm.lp[d * K]), seq);
-#pragma unroll
-        for (int j = 0; j < SMAX; ++j)
-          if (j == cj) { key[j] = ck; info[j] = pack_info(n, d + 1, 1); psc[j] = wscore; }
-      }
-      ++seq;
-    }
     if (lane == w) {
-      lbest = 0; lbj = 0;
-#pragma unroll
-      for (int j = 0; j < SMAX; ++j)
-        if (key[j] > lbest) { lbest = key[j]; lbj = j; }
-    } else if (lane == child_lane) {
-      if (ck > lbest) { lbest = ck; lbj = cj; }
+      if (r < K) {
+        sm.key[slot] = make_key(__fadd_rn(wpsc, sm.lp[(d - 1) * K + r]), seq);
+        sm.info[slot] = pack_info(p, d, r + 1);
+      } else {
+        sm.key[slot] = 0;
+      }
+    }
+    if (r < K) ++seq;
+    // first child: a new slot for the popped node
+    int child_lane = -1;
+    uint64_t ck = 0;
+    int cslot = 0;
+    if (d < D) {
+      cslot = n_slots++;
+      child_lane = cslot & 31;
+      ck = make_key(__fadd_rn(wscore, sm.lp[d * K]), seq);
+      if (lane == child_lane) {
+        sm.key[cslot] = ck;
+        sm.info[cslot] = pack_info(n, d + 1, 1);
+        sm.psc[cslot] = wscore;
+      }
+      ++seq;
+    }
+    __syncwarp();
+    // the winning lane's best, recomputed by the whole warp over its slots
+    uint64_t mine = 0;
+    int mslot = w;
+    for (int s_read = w + 32 * lane; s_read < n_slots; s_read += 32 * 32) {
+      const uint64_t k = sm.key[s_read];
+      if (k > mine) { mine = k; mslot = s_read; }
+    }
+    uint64_t nb;
+    const int t = warp_argmax_key(mine, nb);
+    const int nslot = __shfl_sync(0xffffffffu, mslot, t);
+    if (lane == w) {
+      lbest = nb;
+      lbs = nslot;
+    } else if (lane == child_lane && ck > lbest) {
+      lbest = ck;
+      lbs = cslot;
     }
   }
   __syncwarp();
@@ -212,19 +234,18 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   }
 }
 
-template <int SMAX>
-void launch_build_t(const TreeBuildLaunch& a, cudaStream_t st) {
+void launch_build(const TreeBuildLaunch& a, cudaStream_t st) {
   const size_t per_warp = build_warp_bytes(a.D, a.K, a.B);
   const size_t smem = per_warp * kBuildWarps;
   static bool attr_set = false;  // per instantiation, per process
   if (!attr_set) {
-    cudaFuncSetAttribute(ddtree_build_kernel<SMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(ddtree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          200 * 1024);
     attr_set = true;
   }
   dim3 grid(ceil_div(a.n_req, kBuildWarps));
   TraceScope ts("ddtree_build", st);
-  ddtree_build_kernel<SMAX><<<grid, kBuildWarps * 32, smem, st>>>(
+  ddtree_build_kernel<<<grid, kBuildWarps * 32, smem, st>>>(
       a.n_req, a.D, a.K, a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
       a.depth, a.rank, a.mask);
 }
@@ -276,11 +297,7 @@ size_t tree_build_smem_bytes(int D, int K, int B) {
 
 void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st) {
   if (a.n_req <= 0) return;
-  const int slots = a.B + 1;
-  if (slots <= 32 * 4) launch_build_t<4>(a, st);
-  else if (slots <= 32 * 9) launch_build_t<9>(a, st);
-  else if (slots <= 32 * 17) launch_build_t<17>(a, st);
-  else launch_build_t<33>(a, st);
+  launch_build(a, st);
 }
 
 void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st) {

@@ -28,6 +28,7 @@ struct dflash_model {
   dflash_dims dims;
   dflash_weights w;
   bool bf16;
+  RopeFreqs freqs;
   CUtensorMap tm_proj, tm_ukv, tm_lm;
   CUtensorMap tm_qkv[DFLASH_MAX_LAYERS], tm_o[DFLASH_MAX_LAYERS], tm_gu[DFLASH_MAX_LAYERS],
       tm_down[DFLASH_MAX_LAYERS];
@@ -198,6 +199,7 @@ dflash_status dflash_model_create(const dflash_dims* dims, const dflash_weights*
   m->dims = *dims;
   m->w = w;
   m->bf16 = dims->dtype == DFLASH_BF16;
+  m->freqs = rope_freqs(dims->rope_theta, dims->head_dim);
   if (m->bf16) {
     const dflash_dims& d = *dims;
     const int qkv_dim = (d.n_q + 2 * d.n_kv) * d.head_dim;
@@ -256,7 +258,7 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
   CallCtx c{model, static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream),
             static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + L.counters)};
   float2* rope = reinterpret_cast<float2*>(c.ws + L.rope_inj);
-  launch_inject_rope(row_off, pos0, n_req, n_rows, d.head_dim, d.rope_theta, rope, c.st);
+  launch_inject_rope(row_off, pos0, n_req, n_rows, d.head_dim, model->freqs, rope, c.st);
   dflash_status st = check_launch("inject rope");
   if (st) return st;
 
@@ -326,7 +328,7 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
   float2* rope = reinterpret_cast<float2*>(c.ws + W.rope_blk);
 
   BlockPrologueLaunch pa{model->bf16, model->w.embed, model->w.attn_norm[0], anchor, ctx_len,
-                         n_req, L, d.d, d.vocab, d.mask_id, hd, d.rope_theta, x, xn, ssq, rope,
+                         n_req, L, d.d, d.vocab, d.mask_id, hd, model->freqs, x, xn, ssq, rope,
                          c.status};
   launch_block_prologue(pa, c.st);
   dflash_status st = check_launch("block prologue");

@@ -103,11 +103,12 @@ __device__ __forceinline__ int row_request(const int* row_off, int n_req, int ro
   return lo;
 }
 
-// Apply the epilogue to one chunk: rows [crow0, crow0 + nrows) of the tile whose
-// first column is col0.  buf[r * kBufLd + c] holds acc.  `f` is this thread's
-// tile column; all 128 threads of the group call this together (warp-uniform
-// control flow, shuffles inside).  s_scale is indexed by row - srow0.
-// s_red[warp][row - srow0] accumulates RESID sums of squares.
+// Apply the epilogue to one chunk: rows [crow0, crow0 + nrows) (nrows <= 16)
+// of the tile whose first column is col0.  buf[r * kBufLd + c] holds acc.  `f`
+// is this thread's tile column; all 128 threads of the group call this
+// together (warp-uniform control flow, shuffles inside).  s_scale is indexed by
+// row - srow0; s_red[warp][row - srow0] accumulates RESID sums of squares.
+// The rows are unrolled so every global load of the chunk is in flight at once.
 template <typename T>
 __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float* buf, int col0,
                                                 int crow0, int nrows, int f,
@@ -116,89 +117,136 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
   const int col = col0 + f;
   const bool cvalid = col < e.N_feat;
   const int lane = f & 31;
-  for (int r = 0; r < nrows; ++r) {
-    const int row = crow0 + r;
-    const float s = s_scale[row - srow0];
-    const float a = buf[r * kBufLd + f];
-    switch (e.kind) {
-      case EPI_STORE: {
-        if (cvalid) static_cast<T*>(e.out)[(size_t)row * e.ldo + col] = from_f32<T>(a * s);
-        break;
-      }
-      case EPI_QKV: {
-        float v = a * s;
-        if (col < e.rope_cols) {
-          const int half = e.head_dim >> 1;
-          const int i = col % e.head_dim;
-          const int pf = (i < half) ? f + half : f - half;
-          const float pv = buf[r * kBufLd + pf] * s;
-          const float2 cs = e.rope[(size_t)row * half + (i % half)];
-          v = (i < half) ? (v * cs.x - pv * cs.y) : (v * cs.x + pv * cs.y);
-        }
-        if (cvalid) static_cast<T*>(e.out)[(size_t)row * e.ldo + col] = from_f32<T>(v);
-        break;
-      }
-      case EPI_RESID: {
-        float xv = 0.f;
-        if (cvalid) {
-          const size_t idx = (size_t)row * e.N_feat + col;
-          xv = e.x[idx] + a;
-          e.x[idx] = xv;
-          const float g = to_f32<T>(static_cast<const T*>(e.gain)[col]);
-          static_cast<T*>(e.xn)[idx] = from_f32<T>(xv * g);
-        }
-        float sq = xv * xv;
+  float a[kChunk];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        if (lane == 0) s_red[ewarp * s_red_ld + (row - srow0)] += sq;
-        break;
-      }
-      case EPI_SWIGLU: {
-        const float v = a * s;
-        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-        if ((f & 1) == 0 && cvalid) {
-          const float h = silu_f(v) * other;
-          static_cast<T*>(e.out)[(size_t)row * e.ldo + (col >> 1)] = from_f32<T>(h);
-        }
-        break;
-      }
-      case EPI_KV: {
-        if (!cvalid) break;
-        const int kvd = e.n_kv * e.head_dim;
-        const int layer = col / (2 * kvd);
-        const int kind = (col / kvd) & 1;
-        const int c = col % kvd;
-        const int head = c / e.head_dim;
-        const int i = c % e.head_dim;
-        float v = a;
-        if (kind == 0) {
-          const int half = e.head_dim >> 1;
-          const int pf = (i < half) ? f + half : f - half;
-          const float pv = buf[r * kBufLd + pf];
-          const float2 cs = e.rope[(size_t)row * half + (i % half)];
-          v = (i < half) ? (v * cs.x - pv * cs.y) : (v * cs.x + pv * cs.y);
-        }
-        const int req = row_request(e.row_off, e.n_req, row);
-        const int pos = e.pos0[req] + (row - e.row_off[req]);
-        if (pos < 0 || pos >= e.cap) break;  // outside the request's cache slab
-        T* dst = static_cast<T*>(kind == 0 ? e.cache_k[layer] : e.cache_v[layer]);
-        dst[(((size_t)req * e.n_kv + head) * e.cap + pos) * e.head_dim + i] = from_f32<T>(v);
-        break;
-      }
-      case EPI_LOGITS: {
-        const int req = row / e.L;
-        const int j = row - req * e.L;
-        if (j >= 1 && cvalid)
-          e.logits[((size_t)req * (e.L - 1) + (j - 1)) * e.N_feat + col] = a * s;
-        break;
-      }
-      case EPI_STORE_F32: {
-        if (cvalid) e.logits[(size_t)row * e.ldo + col] = a;
-        break;
-      }
-      default:
-        break;
+  for (int r = 0; r < kChunk; ++r) a[r] = (r < nrows) ? buf[r * kBufLd + f] : 0.f;
+  switch (e.kind) {
+    case EPI_STORE: {
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r)
+        if (r < nrows && cvalid)
+          static_cast<T*>(e.out)[(size_t)(crow0 + r) * e.ldo + col] =
+              from_f32<T>(a[r] * s_scale[crow0 + r - srow0]);
+      break;
     }
+    case EPI_STORE_F32: {
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r)
+        if (r < nrows && cvalid) e.logits[(size_t)(crow0 + r) * e.ldo + col] = a[r];
+      break;
+    }
+    case EPI_QKV: {
+      const bool rot = col < e.rope_cols;
+      const int half = e.head_dim >> 1;
+      const int i = col % e.head_dim;
+      const int pf = (i < half) ? f + half : f - half;
+      float2 cs[kChunk];
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r)
+        cs[r] = (rot && r < nrows) ? e.rope[(size_t)(crow0 + r) * half + (i % half)]
+                                   : make_float2(1.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        if (r < nrows && cvalid) {
+          const float s = s_scale[crow0 + r - srow0];
+          float v = a[r] * s;
+          if (rot) {
+            const float pv = buf[r * kBufLd + pf] * s;
+            v = (i < half) ? (v * cs[r].x - pv * cs[r].y) : (v * cs[r].x + pv * cs[r].y);
+          }
+          static_cast<T*>(e.out)[(size_t)(crow0 + r) * e.ldo + col] = from_f32<T>(v);
+        }
+      }
+      break;
+    }
+    case EPI_RESID: {
+      float xv[kChunk];
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r)
+        xv[r] = (r < nrows && cvalid) ? e.x[(size_t)(crow0 + r) * e.N_feat + col] : 0.f;
+      const float g = cvalid ? to_f32<T>(static_cast<const T*>(e.gain)[col]) : 0.f;
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        if (r < nrows && cvalid) {
+          const size_t idx = (size_t)(crow0 + r) * e.N_feat + col;
+          xv[r] += a[r];
+          e.x[idx] = xv[r];
+          static_cast<T*>(e.xn)[idx] = from_f32<T>(xv[r] * g);
+        }
+      }
+      float sq[kChunk];
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) sq[r] = xv[r] * xv[r];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], off);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r)
+          if (r < nrows) s_red[ewarp * s_red_ld + (crow0 + r - srow0)] += sq[r];
+      }
+      break;
+    }
+    case EPI_SWIGLU: {
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const float v = a[r] * ((r < nrows) ? s_scale[crow0 + r - srow0] : 0.f);
+        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+        if (r < nrows && (f & 1) == 0 && cvalid)
+          static_cast<T*>(e.out)[(size_t)(crow0 + r) * e.ldo + (col >> 1)] =
+              from_f32<T>(silu_f(v) * other);
+      }
+      break;
+    }
+    case EPI_KV: {
+      if (!cvalid) break;
+      const int kvd = e.n_kv * e.head_dim;
+      const int layer = col / (2 * kvd);
+      const int kind = (col / kvd) & 1;
+      const int c = col % kvd;
+      const int head = c / e.head_dim;
+      const int i = c % e.head_dim;
+      const int half = e.head_dim >> 1;
+      const int pf = (i < half) ? f + half : f - half;
+      T* dst = static_cast<T*>(kind == 0 ? e.cache_k[layer] : e.cache_v[layer]);
+      int req[kChunk], pos[kChunk];
+      float2 cs[kChunk];
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const int row = crow0 + (r < nrows ? r : 0);
+        req[r] = row_request(e.row_off, e.n_req, row);
+        pos[r] = e.pos0[req[r]] + (row - e.row_off[req[r]]);
+        cs[r] = (kind == 0) ? e.rope[(size_t)row * half + (i % half)] : make_float2(1.f, 0.f);
+      }
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        if (r >= nrows || pos[r] < 0 || pos[r] >= e.cap) continue;  // outside the slab
+        float v = a[r];
+        if (kind == 0) {
+          const float pv = buf[r * kBufLd + pf];
+          v = (i < half) ? (v * cs[r].x - pv * cs[r].y) : (v * cs[r].x + pv * cs[r].y);
+        }
+        dst[(((size_t)req[r] * e.n_kv + head) * e.cap + pos[r]) * e.head_dim + i] =
+            from_f32<T>(v);
+      }
+      break;
+    }
+    case EPI_LOGITS: {
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const int row = crow0 + r;
+        const int rq = row / e.L;
+        const int j = row - rq * e.L;
+        if (r < nrows && j >= 1 && cvalid)
+          e.logits[((size_t)rq * (e.L - 1) + (j - 1)) * e.N_feat + col] =
+              a[r] * s_scale[row - srow0];
+      }
+      break;
+    }
+    default:
+      break;
   }
 }
 

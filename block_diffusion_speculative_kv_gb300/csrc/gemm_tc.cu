@@ -288,12 +288,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
           const float* slots = p.part + (size_t)c_first * p.max_slots * p.n_tile * kTileN;
           for (int c0 = 0; c0 < nrows; c0 += kChunk) {
             const int nr = min(kChunk, nrows - c0);
-            for (int j = 0; j < nr; ++j) {
-              float a = 0.f;
-              for (int s = 0; s < nslots; ++s)
-                a += __ldcg(slots + ((size_t)s * p.n_tile + c0 + j) * kTileN + f);
-              buf[j * kBufLd + f] = a;
+            // fixed slot order; each slot's 16 loads are issued together
+            float acc[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) acc[j] = 0.f;
+            for (int s = 0; s < nslots; ++s) {
+              const float* src = slots + ((size_t)s * p.n_tile + c0) * kTileN + f;
+              float v[kChunk];
+#pragma unroll
+              for (int j = 0; j < kChunk; ++j) v[j] = (j < nr) ? __ldcg(src + (size_t)j * kTileN) : 0.f;
+#pragma unroll
+              for (int j = 0; j < kChunk; ++j) acc[j] += v[j];
             }
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = acc[j];
             ptx::named_bar_sync(1, kEpiThreads);
             epi_apply_chunk<T>(p.epi, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                256, ew);

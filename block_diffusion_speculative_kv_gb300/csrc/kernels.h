@@ -53,6 +53,12 @@ struct TreeAcceptLaunch {
 void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st);
 
 // ---- block prologue and rotary tables (prologue.cu) ----
+// Rotary frequencies theta^(-2i/head_dim), i < head_dim/2, in double precision.
+struct RopeFreqs {
+  double f[64];
+};
+RopeFreqs rope_freqs(float theta, int head_dim);
+
 struct BlockPrologueLaunch {
   bool bf16;
   const void* embed;   // [vocab][d]
@@ -60,7 +66,7 @@ struct BlockPrologueLaunch {
   const int* anchor;   // [n_req]
   const int* ctx_len;  // [n_req]
   int n_req, L, d, vocab, mask_id, head_dim;
-  float theta;
+  RopeFreqs freqs;
   float* x;            // [n_req*L][d] fp32
   void* xn;            // [n_req*L][d] T
   float* ssq;          // [ceil(d/128)][n_req*L]
@@ -69,6 +75,6 @@ struct BlockPrologueLaunch {
 };
 void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st);
 void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_rows, int head_dim,
-                        float theta, float2* rope, cudaStream_t st);
+                        const RopeFreqs& freqs, float2* rope, cudaStream_t st);
 
 }  // namespace dfl

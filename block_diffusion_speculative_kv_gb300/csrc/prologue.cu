@@ -7,8 +7,11 @@
 // sums of squares for the RMS factor; plus the rotary (cos, sin) table of the
 // block positions ctx_len + j.
 // inject_rope: the rotary table of the injected cache positions.
-// Angles are formed and reduced in double precision (pos * theta^(-2i/hd)),
-// then rounded to fp32.
+// The frequencies theta^(-2i/hd) come from the host in double precision; the
+// angle pos * freq is formed and reduced modulo 2*pi in double (three FP64
+// operations), then the reduced angle's sine and cosine are taken in fp32.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,18 +19,21 @@ namespace dfl {
 
 namespace {
 
-__device__ __forceinline__ float2 rope_cs(int pos, int i, int head_dim, float theta) {
-  const double inv = pow(static_cast<double>(theta), -2.0 * i / head_dim);
-  double s, c;
-  sincos(static_cast<double>(pos) * inv, &s, &c);
-  return make_float2(static_cast<float>(c), static_cast<float>(s));
+__device__ __forceinline__ float2 rope_cs(int pos, int i, const RopeFreqs& fr) {
+  const double two_pi = 6.283185307179586476925;
+  const double a = static_cast<double>(pos) * fr.f[i];
+  const double k = rint(a * (1.0 / two_pi));
+  const float r = static_cast<float>(fma(-k, two_pi, a));
+  float s, c;
+  sincosf(r, &s, &c);
+  return make_float2(c, s);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(128)
 block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
                       const int* __restrict__ anchor, const int* __restrict__ ctx_len, int n_req,
-                      int L, int d, int vocab, int mask_id, int head_dim, float theta,
+                      int L, int d, int vocab, int mask_id, int head_dim, const RopeFreqs fr,
                       float* __restrict__ x, T* __restrict__ xn, float* __restrict__ ssq,
                       float2* __restrict__ rope, int* status) {
   __shared__ float red[4];
@@ -59,11 +65,11 @@ block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
   const int half = head_dim / 2;
   const int pos = ctx_len[req] + j;
   for (int i = threadIdx.x; i < half; i += blockDim.x)
-    rope[(size_t)row * half + i] = rope_cs(pos, i, head_dim, theta);
+    rope[(size_t)row * half + i] = rope_cs(pos, i, fr);
 }
 
 __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* __restrict__ pos0,
-                                   int n_req, int n_rows, int head_dim, float theta,
+                                   int n_req, int n_rows, int head_dim, const RopeFreqs fr,
                                    float2* __restrict__ rope) {
   const int half = head_dim / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -76,10 +82,17 @@ __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* _
     else hi = mid - 1;
   }
   const int pos = pos0[lo] + (row - row_off[lo]);
-  rope[idx] = rope_cs(pos, i, head_dim, theta);
+  rope[idx] = rope_cs(pos, i, fr);
 }
 
 }  // namespace
+
+RopeFreqs rope_freqs(float theta, int head_dim) {
+  RopeFreqs r{};
+  for (int i = 0; i < head_dim / 2 && i < 64; ++i)
+    r.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / head_dim);
+  return r;
+}
 
 void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st) {
   const int R = a.n_req * a.L;
@@ -88,23 +101,23 @@ void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st) {
   if (a.bf16) {
     block_prologue_kernel<__nv_bfloat16><<<R, 128, 0, st>>>(
         static_cast<const __nv_bfloat16*>(a.embed), static_cast<const __nv_bfloat16*>(a.gain),
-        a.anchor, a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.theta, a.x,
+        a.anchor, a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
         static_cast<__nv_bfloat16*>(a.xn), a.ssq, a.rope, a.status);
   } else {
     block_prologue_kernel<float><<<R, 128, 0, st>>>(
         static_cast<const float*>(a.embed), static_cast<const float*>(a.gain), a.anchor,
-        a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.theta, a.x,
+        a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
         static_cast<float*>(a.xn), a.ssq, a.rope, a.status);
   }
 }
 
 void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_rows, int head_dim,
-                        float theta, float2* rope, cudaStream_t st) {
+                        const RopeFreqs& freqs, float2* rope, cudaStream_t st) {
   const long long n = (long long)n_rows * (head_dim / 2);
   if (n <= 0) return;
   TraceScope ts("inject_rope", st);
   inject_rope_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(
-      row_off, pos0, n_req, n_rows, head_dim, theta, rope);
+      row_off, pos0, n_req, n_rows, head_dim, freqs, rope);
 }
 
 }  // namespace dfl

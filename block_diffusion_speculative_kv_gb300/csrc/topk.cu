@@ -116,6 +116,10 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) { tv[j] = -CUDART_INF_F; ti[j] = 0x7fffffff; }
 
+  // wthr: the largest per-lane K-th value in the warp.  That lane holds K values
+  // at or above it, so anything strictly below cannot be in the row's top-K;
+  // it is refreshed after every step of the warp-uniform main loop.
+  float wthr = -CUDART_INF_F;
   auto consume = [&](const float* x, int n, int id0) {
     float vmax = x[0];
 #pragma unroll
@@ -130,30 +134,30 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
     }
 #pragma unroll
     for (int e = 0; e < VN; ++e)
-      if (e < n && x[e] > thr) list_insert<KMAX>(tv, ti, K, x[e], id0 + e, thr);
+      if (e < n && x[e] > thr && x[e] >= wthr) list_insert<KMAX>(tv, ti, K, x[e], id0 + e, thr);
   };
 
   if (v1 > v0) {
     const int nvec = (v1 - v0) / VN;
     constexpr int U = 4;
-    int k = tid;
-    for (; k + (U - 1) * kTopkThreads < nvec; k += U * kTopkThreads) {
+    // warp-uniform loop: a warp step covers U*32 consecutive vectors, lane-major
+    for (int kb = warp * 32 * U; kb < nvec; kb += (kTopkThreads / kWarp) * 32 * U) {
       float x[U][VN];
+      bool ok[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const T* p = rp + v0 + (k + u * kTopkThreads) * VN;
-        if constexpr (VECTOR) load_vec<T, VN>(p, x[u]);
-        else x[u][0] = to_f32<T>(p[0]);
+        const int idx = kb + u * 32 + lane;
+        ok[u] = idx < nvec;
+        if (ok[u]) {
+          const T* p = rp + v0 + (size_t)idx * VN;
+          if constexpr (VECTOR) load_vec<T, VN>(p, x[u]);
+          else x[u][0] = to_f32<T>(p[0]);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) consume(x[u], VN, v0 + (k + u * kTopkThreads) * VN);
-    }
-    for (; k < nvec; k += kTopkThreads) {
-      float x[VN];
-      const T* p = rp + v0 + k * VN;
-      if constexpr (VECTOR) load_vec<T, VN>(p, x);
-      else x[0] = to_f32<T>(p[0]);
-      consume(x, VN, v0 + k * VN);
+      for (int u = 0; u < U; ++u)
+        if (ok[u]) consume(x[u], VN, v0 + (kb + u * 32 + lane) * VN);
+      wthr = from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(thr)));
     }
     const int tail0 = v0 + nvec * VN;
     if (tail0 + tid < v1) {
