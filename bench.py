@@ -15,7 +15,8 @@ launching stream, barrier + synchronize on both sides, max over ranks.  Each
 cycle streams ~3.6 GB of weights and cache, far above the 129 MB L2, so no
 flush is needed between steps.  Per-kernel times (roofline, shares) come from
 traced eager cycles: CUDA events recorded around every kernel launch through
-the library's trace hook.  e2e repeats the cycle through the C-ABI calls with
+the library's trace hook, queued behind a GPU sleep so that host latency does
+not leak into them (they run without the graph's launch overlap).  e2e repeats the cycle through the C-ABI calls with
 pinned host inputs and outputs, copies included.
 
 --impl reference times the CPU oracle on the same workload (bounded sample).
@@ -479,11 +480,15 @@ def main():
         raise SystemExit(f"device status {status} after the timed region")
 
     # ---- per-kernel times from traced eager cycles ----
+    # a GPU-side sleep ahead of each traced cycle lets the host queue every
+    # launch (and its events) before the GPU reaches them, so the events time
+    # the kernels and not the host callbacks in between
     tr = Tracer()
-    bd.set_trace_hook(tr)
     for _ in range(3):
+        torch.cuda._sleep(20_000_000)
+        bd.set_trace_hook(tr)
         cyc.run()
-    bd.set_trace_hook(None)
+        bd.set_trace_hook(None)
     dur = tr.durations()
     per_cycle = {k: sum(v) / 3.0 for k, v in dur.items()}
     launches = {k: len(v) // 3 for k, v in dur.items()}

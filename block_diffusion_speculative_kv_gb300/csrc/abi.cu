@@ -1,6 +1,7 @@
 // C ABI of the drafting library: argument validation, workspace layout and
 // kernel launches.  Declarations and contracts are in include/dflash.h.
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <atomic>
@@ -44,6 +45,14 @@ int num_sms() {
 }
 
 size_t ws_header_bytes() { return 256; }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("DFLASH_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 namespace {
 std::atomic<dflash_trace_fn> g_trace_fn{nullptr};

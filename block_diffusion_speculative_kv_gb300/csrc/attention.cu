@@ -102,6 +102,8 @@ attn_split_kernel(const AttnParams p) {
 
   const size_t part_row0 = (((size_t)req * p.n_kv + g) * (p.n_chunks + 1) + chunk_id) * QR;
   if (k_end <= k_begin) {
+    pdl_wait();
+    pdl_trigger();
     for (int r = tid; r < QR; r += blockDim.x) {
       p.part_ml[(part_row0 + r) * 2 + 0] = -CUDART_INF_F;
       p.part_ml[(part_row0 + r) * 2 + 1] = 0.f;
@@ -123,15 +125,6 @@ attn_split_kernel(const AttnParams p) {
     kv_ld = HD;
   }
 
-  // ---- stage Q (rows: head g*G + r/L, token r%L) ----
-  for (int i = tid; i < QRp * NCH; i += blockDim.x) {
-    const int r = i / NCH, ch = i % NCH;
-    const bool valid = r < QR;
-    const int h = g * p.G + (valid ? r / p.L : 0);
-    const int j = valid ? r % p.L : 0;
-    const __nv_bfloat16* src = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD + ch * 8;
-    cp_async16(smem_u32(sQ) + swz<HD>(r, ch), src, valid);
-  }
   auto load_tile = [&](int buf, int key0) {
     uint8_t* dK = sK + buf * kKeyTile * HD * 2;
     uint8_t* dV = sV + buf * kKeyTile * HD * 2;
@@ -144,7 +137,22 @@ attn_split_kernel(const AttnParams p) {
       cp_async16(smem_u32(dV) + swz<HD>(r, ch), vbase + off, valid);
     }
   };
-  load_tile(0, k_begin);
+  // the context part of the cache is written only by the injection, several
+  // kernels back: its first tile is requested before waiting for the QKV GEMM
+  if (!is_block) load_tile(0, k_begin);
+  pdl_wait();
+  pdl_trigger();
+  if (is_block) load_tile(0, k_begin);
+
+  // ---- stage Q (rows: head g*G + r/L, token r%L) ----
+  for (int i = tid; i < QRp * NCH; i += blockDim.x) {
+    const int r = i / NCH, ch = i % NCH;
+    const bool valid = r < QR;
+    const int h = g * p.G + (valid ? r / p.L : 0);
+    const int j = valid ? r % p.L : 0;
+    const __nv_bfloat16* src = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD + ch * 8;
+    cp_async16(smem_u32(sQ) + swz<HD>(r, ch), src, valid);
+  }
   cp_async_commit();
 
   const int qrow0 = warp * 16;
@@ -306,6 +314,8 @@ attn_combine_kernel(const AttnParams p) {
   const int req = blockIdx.z, g = blockIdx.y;
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   if (r >= QR) return;
   const int nparts = p.n_chunks + 1;
   const size_t base = ((size_t)req * p.n_kv + g) * nparts * QR;
@@ -366,6 +376,8 @@ attn_f32_kernel(const AttnParamsF32 p) {
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int total = p.n_req * p.n_q * p.L;
+  pdl_wait();
+  pdl_trigger();
   if (wid >= total) return;
   const int j = wid % p.L;
   const int h = (wid / p.L) % p.n_q;
@@ -444,10 +456,10 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     }
     {
       TraceScope ts("attn_split", st);
-      attn_split_kernel<128><<<grid, 128, smem, st>>>(p);
+      launch_k(attn_split_kernel<128>, grid, dim3(128), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
-    attn_combine_kernel<128><<<cgrid, 128, 0, st>>>(p);
+    launch_k(attn_combine_kernel<128>, cgrid, dim3(128), 0, st, p);
   } else if (head_dim == 64) {
     static bool set = false;
     if (!set) {
@@ -457,10 +469,10 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     }
     {
       TraceScope ts("attn_split", st);
-      attn_split_kernel<64><<<grid, 128, smem, st>>>(p);
+      launch_k(attn_split_kernel<64>, grid, dim3(128), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
-    attn_combine_kernel<64><<<cgrid, 128, 0, st>>>(p);
+    launch_k(attn_combine_kernel<64>, cgrid, dim3(128), 0, st, p);
   } else {
     return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
   }
@@ -471,8 +483,8 @@ dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStr
   const int total = p.n_req * p.n_q * p.L;
   const int blocks = (total + 3) / 4;
   TraceScope ts("attn_f32", st);
-  if (head_dim == 128) attn_f32_kernel<128><<<blocks, 128, 0, st>>>(p);
-  else if (head_dim == 64) attn_f32_kernel<64><<<blocks, 128, 0, st>>>(p);
+  if (head_dim == 128) launch_k(attn_f32_kernel<128>, dim3(blocks), dim3(128), 0, st, p);
+  else if (head_dim == 64) launch_k(attn_f32_kernel<64>, dim3(blocks), dim3(128), 0, st, p);
   else return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
   return check_launch("attention_f32");
 }

@@ -5,7 +5,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/dflash.h"
+#include <utility>
+
+#include "dflash.h"
 
 namespace dfl {
 
@@ -63,6 +65,40 @@ __host__ __device__ __forceinline__ size_t align_up(size_t a, size_t b) {
 
 // Number of SMs of the current device (cached per device on the host).
 int num_sms();
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Kernels of one call are launched so that the
+// next kernel may start while the previous one finishes.  Every kernel calls
+// pdl_wait() before it touches memory written by an earlier kernel of the
+// stream (and before any global write), then pdl_trigger(); work done before
+// pdl_wait() only reads data no kernel of the call writes (weights, the
+// context part of the KV cache) into the CTA's own shared memory.  Because a
+// kernel triggers only after its own wait, when a kernel starts its
+// predecessor's predecessor has completed.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+bool pdl_enabled();  // DFLASH_PDL=0 in the environment turns it off
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launch tracing (dflash_set_trace_hook): host callbacks around each launch.
 void trace(const char* kernel, int phase, cudaStream_t st);

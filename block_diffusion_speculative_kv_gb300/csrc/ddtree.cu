@@ -10,16 +10,15 @@
 // one per "open" parent: the parent's next unpopped child rank (children of a
 // node are popped in rank order, since a sibling is offered only after its
 // predecessor pops).  So the heap is kept as a set of slots in shared memory,
-// one per open parent; slot s belongs to lane s % 32, and every lane keeps the
-// best key among its own slots in a register.  Keys are 64-bit:
+// one per open parent; slot s belongs to lane s % 32, and a lane's slots are
+// scanned by that lane at every pop.  Keys are 64-bit:
 // order-preserving score bits, then the complemented creation counter, so
 // equal scores pop in creation order.  A pop is a warp-wide maximum of the
 // lanes' bests (redux.sync on the high word, and on the low word only when the
 // high word ties); the popped slot advances to its next rank in place (or
-// closes), a new slot opens for the popped node's first child, and the winning
-// lane's best is recomputed by the whole warp (each lane reads one of that
-// lane's slots, then one more warp maximum), so a pop costs O(1) warp
-// instructions whatever the budget.  Candidate scores are the parent score plus
+// closes) and a new slot opens for the popped node's first child.  A pop has
+// no divergent single-lane branches: the new keys are computed by every lane
+// and written by predicated stores.  Candidate scores are the parent score plus
 // one log-probability, a single fp32 add, so the result is bit-identical to a
 // plain binary-heap implementation of the same rule.
 #include "common.cuh"
@@ -95,6 +94,8 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int req = blockIdx.x * kBuildWarps + wib;
+  pdl_wait();
+  pdl_trigger();
   if (req >= n_req) return;
   const int W = (B + 1 + 31) / 32;
 
@@ -122,82 +123,72 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   __syncwarp();
 
   // ---- Algorithm 1 ----
-  uint64_t lbest = 0;  // best key among this lane's slots
-  int lbs = 0;         // its slot index
+  // Every pop: each lane scans its own slots (independent shared loads), one
+  // warp-wide argmax picks the winner, all lanes read the winner's slot and the
+  // log-probabilities it needs (broadcast loads), every lane computes the same
+  // new keys, and the node/slot writes go out as one predicated scattered store
+  // per width - no divergent single-lane branches on the critical path.
   int n = 0, n_slots = 0;
   uint32_t seq = 0;
   if (B > 0) {
     if (lane == 0) {
-      const uint64_t k0 = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
-      sm.key[0] = k0;
+      sm.key[0] = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
       sm.info[0] = pack_info(0, 1, 1);
       sm.psc[0] = 0.f;
-      lbest = k0;
-      lbs = 0;
     }
     n_slots = 1;
     seq = 1;
   }
   __syncwarp();
   while (n < B) {
+    uint64_t best = 0;
+    int bslot = 0;
+    for (int sl = lane; sl < n_slots; sl += 32) {
+      const uint64_t k = sm.key[sl];
+      if (k > best) { best = k; bslot = sl; }
+    }
     uint64_t kmax;
-    const int w = warp_argmax_key(lbest, kmax);
+    const int w = warp_argmax_key(best, kmax);
     if (kmax == 0) break;  // no candidate left
-    const int slot = __shfl_sync(0xffffffffu, lbs, w);
+    const int slot = __shfl_sync(0xffffffffu, bslot, w);
     const uint32_t winfo = sm.info[slot];
     const float wpsc = sm.psc[slot];
     const float wscore = from_ordered_bits(static_cast<uint32_t>(kmax >> 32));
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
     const int r = (winfo >> 16) & 0x3F;
+    const float lp_sib = sm.lp[(d - 1) * K + (r < K ? r : K - 1)];
+    const float lp_child = sm.lp[(d < D ? d : D - 1) * K];
+    const int tokv = sm.ids[(d - 1) * K + (r - 1)];
     ++n;
-    if (lane == 0) {
-      sm.tok[n] = sm.ids[(d - 1) * K + (r - 1)];
-      sm.par[n] = p; sm.dep[n] = d; sm.rnk[n] = r;
-    }
-    // next sibling: the popped slot advances in place (or closes)
-    if (lane == w) {
-      if (r < K) {
-        sm.key[slot] = make_key(__fadd_rn(wpsc, sm.lp[(d - 1) * K + r]), seq);
-        sm.info[slot] = pack_info(p, d, r + 1);
-      } else {
-        sm.key[slot] = 0;
+    const bool has_sib = r < K;
+    const bool has_child = d < D;
+    const uint64_t sib_key = has_sib ? make_key(__fadd_rn(wpsc, lp_sib), seq) : 0ull;
+    seq += has_sib ? 1u : 0u;
+    const uint64_t child_key = make_key(__fadd_rn(wscore, lp_child), seq);
+    seq += has_child ? 1u : 0u;
+    const int cslot = n_slots;
+    n_slots += has_child ? 1 : 0;
+    // 32-bit writes: lane 0..3 the node, lane 4 the popped slot's rank, lanes 5-6 the child slot
+    {
+      uint32_t* addr = nullptr;
+      uint32_t val = 0;
+      switch (lane) {
+        case 0: addr = reinterpret_cast<uint32_t*>(sm.tok + n); val = static_cast<uint32_t>(tokv); break;
+        case 1: addr = reinterpret_cast<uint32_t*>(sm.par + n); val = static_cast<uint32_t>(p); break;
+        case 2: addr = reinterpret_cast<uint32_t*>(sm.dep + n); val = static_cast<uint32_t>(d); break;
+        case 3: addr = reinterpret_cast<uint32_t*>(sm.rnk + n); val = static_cast<uint32_t>(r); break;
+        case 4: if (has_sib) { addr = sm.info + slot; val = pack_info(p, d, r + 1); } break;
+        case 5: if (has_child) { addr = sm.info + cslot; val = pack_info(n, d + 1, 1); } break;
+        case 6: if (has_child) { addr = reinterpret_cast<uint32_t*>(sm.psc + cslot); val = __float_as_uint(wscore); } break;
+        default: break;
       }
+      if (addr) *addr = val;
     }
-    if (r < K) ++seq;
-    // first child: a new slot for the popped node
-    int child_lane = -1;
-    uint64_t ck = 0;
-    int cslot = 0;
-    if (d < D) {
-      cslot = n_slots++;
-      child_lane = cslot & 31;
-      ck = make_key(__fadd_rn(wscore, sm.lp[d * K]), seq);
-      if (lane == child_lane) {
-        sm.key[cslot] = ck;
-        sm.info[cslot] = pack_info(n, d + 1, 1);
-        sm.psc[cslot] = wscore;
-      }
-      ++seq;
-    }
+    // 64-bit writes: lane 0 the popped slot's new key (0 closes it), lane 1 the child's key
+    if (lane == 0) sm.key[slot] = sib_key;
+    if (lane == 1 && has_child) sm.key[cslot] = child_key;
     __syncwarp();
-    // the winning lane's best, recomputed by the whole warp over its slots
-    uint64_t mine = 0;
-    int mslot = w;
-    for (int s_read = w + 32 * lane; s_read < n_slots; s_read += 32 * 32) {
-      const uint64_t k = sm.key[s_read];
-      if (k > mine) { mine = k; mslot = s_read; }
-    }
-    uint64_t nb;
-    const int t = warp_argmax_key(mine, nb);
-    const int nslot = __shfl_sync(0xffffffffu, mslot, t);
-    if (lane == w) {
-      lbest = nb;
-      lbs = nslot;
-    } else if (lane == child_lane && ck > lbest) {
-      lbest = ck;
-      lbs = cslot;
-    }
   }
   __syncwarp();
 
@@ -245,9 +236,9 @@ void launch_build(const TreeBuildLaunch& a, cudaStream_t st) {
   }
   dim3 grid(ceil_div(a.n_req, kBuildWarps));
   TraceScope ts("ddtree_build", st);
-  ddtree_build_kernel<<<grid, kBuildWarps * 32, smem, st>>>(
-      a.n_req, a.D, a.K, a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
-      a.depth, a.rank, a.mask);
+  launch_k(ddtree_build_kernel, grid, dim3(kBuildWarps * 32), smem, st, a.n_req, a.D, a.K, a.B,
+           a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank,
+           a.mask);
 }
 
 // ---------------------------------------------------------------------------
@@ -263,6 +254,8 @@ __global__ void ddtree_accept_kernel(int n_req, int D, int B, const int32_t* __r
                                      int32_t* __restrict__ accepted, int32_t* __restrict__ bonus) {
   const int lane = threadIdx.x & 31;
   const int req = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (req >= n_req) return;
   const unsigned FULL = 0xffffffffu;
   const size_t nb = (size_t)req * (B + 1);
@@ -304,9 +297,9 @@ void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st) {
   if (a.n_req <= 0) return;
   const int warps = 4;
   TraceScope ts("ddtree_accept", st);
-  ddtree_accept_kernel<<<ceil_div(a.n_req, warps), warps * 32, 0, st>>>(
-      a.n_req, a.D, a.B, a.n_nodes, a.tok, a.parent, a.target, a.accept_len, a.accepted,
-      a.bonus);
+  launch_k(ddtree_accept_kernel, dim3(ceil_div(a.n_req, warps)), dim3(warps * 32), 0, st,
+           a.n_req, a.D, a.B, a.n_nodes, a.tok, a.parent, a.target, a.accept_len, a.accepted,
+           a.bonus);
 }
 
 }  // namespace dfl

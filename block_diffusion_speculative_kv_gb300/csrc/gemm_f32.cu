@@ -30,6 +30,8 @@ gemm_f32_kernel(const float* __restrict__ X, long long ldx, const float* __restr
   const int row0 = blockIdx.y * kChunk;
   const int col0 = ftile * kTileN;
   const int nrows = min(kChunk, M_rows - row0);
+  pdl_wait();
+  pdl_trigger();
 
   float acc[kChunk];
 #pragma unroll
@@ -77,7 +79,7 @@ dflash_status launch_gemm_f32(const float* X, long long ldx, const float* W, int
   if (M_rows <= 0) return DFLASH_OK;
   dim3 grid(ceil_div(N_feat, kTileN), ceil_div(M_rows, kChunk));
   TraceScope ts("gemm_f32", st);
-  gemm_f32_kernel<<<grid, 128, 0, st>>>(X, ldx, W, M_rows, N_feat, K, epi);
+  launch_k(gemm_f32_kernel, grid, dim3(128), 0, st, X, ldx, W, M_rows, N_feat, K, epi);
   return check_launch("gemm_f32");
 }
 

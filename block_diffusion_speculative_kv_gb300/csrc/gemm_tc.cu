@@ -70,13 +70,13 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile) {
   const uint32_t bar_bytes = (2 * stages + 3) * 8 + 16 + 16;
   L.buf_off = (L.bar_off + bar_bytes + 15) / 16 * 16;
   L.scale_off = L.buf_off + kChunk * kBufLd * 4;
-  L.red_off = L.scale_off + 256 * 4;
-  L.total = L.red_off + 4 * 256 * 4 + 1024;  // + alignment slack for the 1024-B base
+  L.red_off = L.scale_off + n_tile * 4;
+  L.total = L.red_off + 4 * n_tile * 4 + 1024;  // + alignment slack for the 1024-B base
   return L;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -131,6 +131,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const bool producer = (warp == 0 && lane == 0);
+  if (!producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -141,7 +146,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t issued_phase_mask = 0;  // bit s: stage s has an issued copy
       uint32_t last_phase[32];
-      for (long long u = u_begin; u < u_end; ++u) {
+      // Weights are never written by a kernel: the first ring slots' weight
+      // tiles are requested before waiting for the previous kernel, the
+      // activation tiles (its output) after.
+      const int pre = static_cast<int>(
+          (u_end - u_begin) < p.stages ? (u_end - u_begin) : p.stages);
+      for (int i = 0; i < pre; ++i) {
+        const long long u = u_begin + i;
+        const int t = static_cast<int>(u / KB);
+        const int kb = static_cast<int>(u - (long long)t * KB);
+        const int ftile = t / p.n_rtiles;
+        ptx::mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
+        ptx::tma_load_2d(sA + i * kABytes, &tmW, &full[i], kb * 64, ftile * kTileN, pol_w);
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < pre; ++i) {
+        const long long u = u_begin + i;
+        const int t = static_cast<int>(u / KB);
+        const int kb = static_cast<int>(u - (long long)t * KB);
+        const int ftile = t / p.n_rtiles;
+        const int rtile = t - ftile * p.n_rtiles;
+        ptx::tma_load_2d(sB + i * b_bytes, &tmX, &full[i], kb * 64, rtile * p.n_tile, pol_x);
+        issued_phase_mask |= 1u << i;
+        last_phase[i] = 0;
+      }
+      stage = pre % p.stages;
+      phase = (pre == p.stages) ? 1u : 0u;
+      for (long long u = u_begin + pre; u < u_end; ++u) {
         const int t = static_cast<int>(u / KB);
         const int kb = static_cast<int>(u - (long long)t * KB);
         const int ftile = t / p.n_rtiles;
@@ -245,7 +277,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 
       if (single) {
         epi_row_scales(p.epi, row0, nrows, s_scale, etid, kEpiThreads);
-        for (int i = etid; i < 4 * 256; i += kEpiThreads) s_red[i] = 0.f;
+        for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
       }
       float* my_part = p.part + ((size_t)c_first * p.max_slots + (c - c_first)) *
                                     (size_t)p.n_tile * kTileN;
@@ -258,7 +290,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
           for (int j = 0; j < 16; ++j) buf[j * kBufLd + f] = v[j];
           ptx::named_bar_sync(1, kEpiThreads);
           epi_apply_chunk<T>(p.epi, buf, ftile * kTileN, row0 + c0, min(kChunk, nrows - c0), f,
-                             s_scale, row0, s_red, 256, ew);
+                             s_scale, row0, s_red, p.n_tile, ew);
           ptx::named_bar_sync(1, kEpiThreads);
         } else {
 #pragma unroll
@@ -271,7 +303,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       if (single) {
         if (p.epi.kind == EPI_RESID) {
           ptx::named_bar_sync(1, kEpiThreads);
-          epi_resid_flush(p.epi, ftile, row0, nrows, s_red, 256, 4, etid, kEpiThreads);
+          epi_resid_flush(p.epi, ftile, row0, nrows, s_red, p.n_tile, 4, etid, kEpiThreads);
         }
       } else {
         __threadfence();
@@ -284,31 +316,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         if (flags[1]) {
           __threadfence();
           epi_row_scales(p.epi, row0, nrows, s_scale, etid, kEpiThreads);
-          for (int i = etid; i < 4 * 256; i += kEpiThreads) s_red[i] = 0.f;
+          for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
           const float* slots = p.part + (size_t)c_first * p.max_slots * p.n_tile * kTileN;
           for (int c0 = 0; c0 < nrows; c0 += kChunk) {
             const int nr = min(kChunk, nrows - c0);
-            // fixed slot order; each slot's 16 loads are issued together
+            // fixed slot order; four slots' loads (16 rows each) are in flight together
             float acc[kChunk];
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) acc[j] = 0.f;
-            for (int s = 0; s < nslots; ++s) {
-              const float* src = slots + ((size_t)s * p.n_tile + c0) * kTileN + f;
-              float v[kChunk];
+            for (int s0 = 0; s0 < nslots; s0 += 4) {
+              float v[4][kChunk];
 #pragma unroll
-              for (int j = 0; j < kChunk; ++j) v[j] = (j < nr) ? __ldcg(src + (size_t)j * kTileN) : 0.f;
+              for (int q = 0; q < 4; ++q) {
+                const float* src = slots + ((size_t)(s0 + q) * p.n_tile + c0) * kTileN + f;
 #pragma unroll
-              for (int j = 0; j < kChunk; ++j) acc[j] += v[j];
+                for (int j = 0; j < kChunk; ++j)
+                  v[q][j] = (s0 + q < nslots && j < nr) ? __ldcg(src + (size_t)j * kTileN) : 0.f;
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < kChunk; ++j) acc[j] += v[q][j];
             }
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = acc[j];
             ptx::named_bar_sync(1, kEpiThreads);
             epi_apply_chunk<T>(p.epi, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
-                               256, ew);
+                               p.n_tile, ew);
             ptx::named_bar_sync(1, kEpiThreads);
           }
           if (p.epi.kind == EPI_RESID)
-            epi_resid_flush(p.epi, ftile, row0, nrows, s_red, 256, 4, etid, kEpiThreads);
+            epi_resid_flush(p.epi, ftile, row0, nrows, s_red, p.n_tile, 4, etid, kEpiThreads);
           if (etid == 0) p.counters[c_first] = 0;
         }
         ptx::named_bar_sync(1, kEpiThreads);
@@ -400,8 +438,14 @@ TcPlan tc_plan(int M_rows, int N_feat, int K, int grid_max) {
   pl.max_slots = ms;
   pl.part_bytes = (size_t)pl.grid * ms * pl.n_tile * kTileN * sizeof(float);
   const int b_bytes = pl.n_tile * 128;
+  // Small row tiles stream weights: a ring of ~80 KB in flight per CTA keeps
+  // HBM busy, and staying under half of the SM's shared memory lets the next
+  // GEMM's CTAs become resident (and start fetching weights) while this one
+  // drains.  The vocabulary-sized LM head and large row tiles take the deepest ring.
+  const bool co_resident = pl.n_tile <= 64 && (long long)N_feat * K < (400LL << 20);
+  const int smem_cap = co_resident ? 112 * 1024 : 227 * 1024;
   int stages = 1;
-  while (stages < 24 && smem_layout(stages + 1, pl.n_tile).total <= 227 * 1024) ++stages;
+  while (stages < 24 && smem_layout(stages + 1, pl.n_tile).total <= (uint32_t)smem_cap) ++stages;
   pl.stages = stages;
   pl.smem_bytes = smem_layout(stages, pl.n_tile).total;
   (void)b_bytes;
@@ -427,7 +471,8 @@ dflash_status launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, con
   p.epi = epi;
   set_smem_attr_once<__nv_bfloat16>(pl.smem_bytes);
   TraceScope ts("gemm_tc", st);
-  gemm_tc_kernel<__nv_bfloat16><<<pl.grid, kThreads, pl.smem_bytes, st>>>(tmW, tmX, p);
+  launch_k(gemm_tc_kernel<__nv_bfloat16>, dim3(pl.grid), dim3(kThreads), pl.smem_bytes, st, tmW,
+           tmX, p);
   return check_launch("gemm_tc");
 }
 

@@ -40,6 +40,8 @@ block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
   const int R = n_req * L;
   const int row = blockIdx.x;
   const int req = row / L, j = row % L;
+  pdl_wait();
+  pdl_trigger();
   int tok = (j == 0) ? anchor[req] : mask_id;
   if (tok < 0 || tok >= vocab) {
     if (threadIdx.x == 0) record_status(status, DFLASH_ERR_INVALID_ARG);
@@ -73,6 +75,8 @@ __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* _
                                    float2* __restrict__ rope) {
   const int half = head_dim / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (idx >= (long long)n_rows * half) return;
   const int row = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
   int lo = 0, hi = n_req - 1;
@@ -99,15 +103,15 @@ void launch_block_prologue(const BlockPrologueLaunch& a, cudaStream_t st) {
   if (R <= 0) return;
   TraceScope ts("block_prologue", st);
   if (a.bf16) {
-    block_prologue_kernel<__nv_bfloat16><<<R, 128, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(a.embed), static_cast<const __nv_bfloat16*>(a.gain),
-        a.anchor, a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
-        static_cast<__nv_bfloat16*>(a.xn), a.ssq, a.rope, a.status);
+    launch_k(block_prologue_kernel<__nv_bfloat16>, dim3(R), dim3(128), 0, st,
+             static_cast<const __nv_bfloat16*>(a.embed), static_cast<const __nv_bfloat16*>(a.gain),
+             a.anchor, a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
+             static_cast<__nv_bfloat16*>(a.xn), a.ssq, a.rope, a.status);
   } else {
-    block_prologue_kernel<float><<<R, 128, 0, st>>>(
-        static_cast<const float*>(a.embed), static_cast<const float*>(a.gain), a.anchor,
-        a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
-        static_cast<float*>(a.xn), a.ssq, a.rope, a.status);
+    launch_k(block_prologue_kernel<float>, dim3(R), dim3(128), 0, st,
+             static_cast<const float*>(a.embed), static_cast<const float*>(a.gain), a.anchor,
+             a.ctx_len, a.n_req, a.L, a.d, a.vocab, a.mask_id, a.head_dim, a.freqs, a.x,
+             static_cast<float*>(a.xn), a.ssq, a.rope, a.status);
   }
 }
 
@@ -116,8 +120,8 @@ void launch_inject_rope(const int* row_off, const int* pos0, int n_req, int n_ro
   const long long n = (long long)n_rows * (head_dim / 2);
   if (n <= 0) return;
   TraceScope ts("inject_rope", st);
-  inject_rope_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(
-      row_off, pos0, n_req, n_rows, head_dim, freqs, rope);
+  launch_k(inject_rope_kernel, dim3(static_cast<int>((n + 255) / 256)), dim3(256), 0, st,
+           row_off, pos0, n_req, n_rows, head_dim, freqs, rope);
 }
 
 }  // namespace dfl

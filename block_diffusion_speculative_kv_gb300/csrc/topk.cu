@@ -109,6 +109,8 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
   const int v0 = split * chunk;
   const int v1 = min(vocab, v0 + chunk);
   const T* rp = logits + (long long)row * ld;
+  pdl_wait();
+  pdl_trigger();
 
   float m = -CUDART_INF_F, s = 0.f, thr = -CUDART_INF_F;
   float tv[KMAX];
@@ -273,13 +275,13 @@ void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
   dim3 grid(a.rows * a.splits);
   TraceScope ts("lse_topk", st);
   if (vec_ok) {
-    topk_kernel<T, KMAX, true><<<grid, kTopkThreads, 0, st>>>(
-        static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
-        a.counters, a.ids, a.logp);
+    launch_k(topk_kernel<T, KMAX, true>, grid, dim3(kTopkThreads), 0, st,
+             static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
+             a.counters, a.ids, a.logp);
   } else {
-    topk_kernel<T, KMAX, false><<<grid, kTopkThreads, 0, st>>>(
-        static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
-        a.counters, a.ids, a.logp);
+    launch_k(topk_kernel<T, KMAX, false>, grid, dim3(kTopkThreads), 0, st,
+             static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
+             a.counters, a.ids, a.logp);
   }
   (void)VN;
 }
