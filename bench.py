@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
-                                       "tree_stress", "tree_b1"],
+                                       "topk_b1", "tree_stress", "tree_b1"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -403,9 +403,11 @@ def run_case(args):
             bd.linear_bf16(X, Ws[fn_i[0] % copies], Y, ws)
             fn_i[0] += 1
         nbytes = 2 * N * K + 2 * M * K + 4 * M * N
-    elif args.case == "topk_stress":
+    elif args.case in ("topk_stress", "topk_b1"):
         wl = WORKLOADS[4]
         logits, _ = synth.stress_logits(wl.n_req, wl.D, wl.vocab, wl.seed, device="cuda")
+        if args.case == "topk_b1":   # the 8B batch-1 drafter's 15 rows of fp32 logits
+            logits = logits[:15].float().contiguous()
         rows = logits.shape[0]
         ids = torch.empty(rows, wl.K, dtype=torch.int32, device="cuda")
         lp = torch.empty(rows, wl.K, device="cuda")

@@ -29,6 +29,7 @@ namespace dfl {
 namespace {
 
 constexpr int kKeyTile = 64;
+constexpr int kStages = 6;   // K/V tiles in flight per CTA (~192 KB at head_dim 128)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -87,7 +88,7 @@ attn_split_kernel(const AttnParams p) {
   const int QRp = (QR + 15) / 16 * 16;
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QRp * HD * 2;
-  uint8_t* sV = sK + 2 * kKeyTile * HD * 2;
+  uint8_t* sV = sK + kStages * kKeyTile * HD * 2;
 
   const int chunk_id = blockIdx.x;
   const int g = blockIdx.y;
@@ -137,12 +138,19 @@ attn_split_kernel(const AttnParams p) {
       cp_async16(smem_u32(dV) + swz<HD>(r, ch), vbase + off, valid);
     }
   };
-  // the context part of the cache is written only by the injection, several
-  // kernels back: its first tile is requested before waiting for the QKV GEMM
-  if (!is_block) load_tile(0, k_begin);
+  const int ntiles = (k_end - k_begin + kKeyTile - 1) / kKeyTile;
+  // The context part of the cache is written only by the injection, several
+  // kernels back: its first ring of tiles is requested before waiting for the
+  // QKV GEMM (each tile is its own cp.async group).
+  const int npre = ntiles < kStages - 1 ? ntiles : kStages - 1;
+  if (!is_block) {
+    for (int t = 0; t < npre; ++t) {
+      load_tile(t, k_begin + t * kKeyTile);
+      cp_async_commit();
+    }
+  }
   pdl_wait();
   pdl_trigger();
-  if (is_block) load_tile(0, k_begin);
 
   // ---- stage Q (rows: head g*G + r/L, token r%L) ----
   for (int i = tid; i < QRp * NCH; i += blockDim.x) {
@@ -153,7 +161,16 @@ attn_split_kernel(const AttnParams p) {
     const __nv_bfloat16* src = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD + ch * 8;
     cp_async16(smem_u32(sQ) + swz<HD>(r, ch), src, valid);
   }
-  cp_async_commit();
+  if (is_block) {
+    // block keys come from the QKV output: after the wait; Q joins this group
+    for (int t = 0; t < npre; ++t) {
+      load_tile(t, k_begin + t * kKeyTile);
+      cp_async_commit();
+    }
+  } else {
+    cp_async_commit();   // Q in its own group
+  }
+  // groups issued so far: npre tiles (+ the Q group for context chunks)
 
   const int qrow0 = warp * 16;
   const bool warp_active = qrow0 < QR;
@@ -164,12 +181,19 @@ attn_split_kernel(const AttnParams p) {
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   uint32_t qa[HD / 16][4];
 
-  const int ntiles = (k_end - k_begin + kKeyTile - 1) / kKeyTile;
   for (int t = 0; t < ntiles; ++t) {
     const int key0 = k_begin + t * kKeyTile;
-    if (t + 1 < ntiles) load_tile((t + 1) & 1, key0 + kKeyTile);
+    // keep kStages-1 tiles in flight: issue tile t+npre (its buffer was freed
+    // by the barrier at the end of the previous iteration), then wait until
+    // tile t (and Q) have landed
+    if (t + npre < ntiles) load_tile((t + npre) % kStages, k_begin + (t + npre) * kKeyTile);
     cp_async_commit();
-    cp_async_wait<1>();
+    // groups complete in commit order.  At t = 0 the Q group sits behind the
+    // prefetched tiles, so wait for all but the group just committed; later, a
+    // tile issued inside the loop has kStages-1 newer groups at most (and when
+    // fewer tiles than kStages-1 exist, all were waited for at t = 0)
+    if (t == 0) cp_async_wait<1>();
+    else cp_async_wait<kStages - 1>();
     __syncthreads();
     if (t == 0 && warp_active) {
 #pragma unroll
@@ -180,8 +204,8 @@ attn_split_kernel(const AttnParams p) {
       }
     }
     if (warp_active) {
-      const uint32_t kb = smem_u32(sK + (t & 1) * kKeyTile * HD * 2);
-      const uint32_t vb = smem_u32(sV + (t & 1) * kKeyTile * HD * 2);
+      const uint32_t kb = smem_u32(sK + (t % kStages) * kKeyTile * HD * 2);
+      const uint32_t vb = smem_u32(sV + (t % kStages) * kKeyTile * HD * 2);
       float s[kKeyTile / 8][4];
 #pragma unroll
       for (int n = 0; n < kKeyTile / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
@@ -334,24 +358,25 @@ attn_combine_kernel(const AttnParams p) {
 #pragma unroll
   for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
   float Lsum = 0.f;
-  constexpr int U = 4;
+  constexpr int U = 8;   // chunk partials in flight per lane (16 B each)
+  static_assert(DPL == 4 || DPL == 2, "head_dim 128 or 64");
   for (int c0 = 0; c0 < nparts; c0 += U) {
     float w[U], l[U], v[U][DPL];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + u;
-      w[u] = 0.f;
-      l[u] = 0.f;
-      if (c < nparts) {
-        const size_t row = base + (size_t)c * QR + r;
-        l[u] = p.part_ml[row * 2 + 1];
-        w[u] = (l[u] > 0.f) ? exp2f(p.part_ml[row * 2] - M) : 0.f;
-        const float* src = p.part_o + row * HD + lane * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) v[u][i] = (l[u] > 0.f) ? src[i] : 0.f;
+      const size_t row = base + (size_t)(c < nparts ? c : 0) * QR + r;
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + row * 2);
+      l[u] = (c < nparts) ? ml.y : 0.f;
+      w[u] = (l[u] > 0.f) ? exp2f(ml.x - M) : 0.f;
+      const float* src = p.part_o + row * HD + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 t = (l[u] > 0.f) ? *reinterpret_cast<const float4*>(src)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
       } else {
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) v[u][i] = 0.f;
+        const float2 t = (l[u] > 0.f) ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y;
       }
     }
 #pragma unroll
@@ -426,7 +451,8 @@ attn_f32_kernel(const AttnParamsF32 p) {
 }  // namespace
 
 int attn_chunk(int max_ctx, int n_kv, int n_req) {
-  const long long target = 2LL * num_sms();
+  // one CTA per SM: each holds a deep ring of K/V tiles
+  const long long target = num_sms();
   long long work = (long long)max_ctx * n_kv * n_req;
   long long c = (work + target - 1) / target;
   c = (c + kKeyTile - 1) / kKeyTile * kKeyTile;
@@ -437,7 +463,7 @@ int attn_chunk(int max_ctx, int n_kv, int n_req) {
 
 size_t attn_smem_bytes(int G, int L, int HD) {
   const int QRp = (G * L + 15) / 16 * 16;
-  return (size_t)QRp * HD * 2 + 4 * kKeyTile * HD * 2;
+  return (size_t)QRp * HD * 2 + 2 * kStages * kKeyTile * HD * 2;
 }
 
 dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStream_t st) {
@@ -451,7 +477,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     static bool set = false;
     if (!set) {
       cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024);
+                           227 * 1024);
       set = true;
     }
     {
@@ -464,7 +490,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     static bool set = false;
     if (!set) {
       cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024);
+                           227 * 1024);
       set = true;
     }
     {

@@ -10,15 +10,13 @@
 // one per "open" parent: the parent's next unpopped child rank (children of a
 // node are popped in rank order, since a sibling is offered only after its
 // predecessor pops).  So the heap is kept as a set of slots in shared memory,
-// one per open parent; slot s belongs to lane s % 32, and a lane's slots are
-// scanned by that lane at every pop.  Keys are 64-bit:
+// one per open parent; slot s belongs to lane s % 32, which keeps the best key
+// among its slots in a register.  Keys are 64-bit:
 // order-preserving score bits, then the complemented creation counter, so
 // equal scores pop in creation order.  A pop is a warp-wide maximum of the
 // lanes' bests (redux.sync on the high word, and on the low word only when the
 // high word ties); the popped slot advances to its next rank in place (or
-// closes) and a new slot opens for the popped node's first child.  A pop has
-// no divergent single-lane branches: the new keys are computed by every lane
-// and written by predicated stores.  Candidate scores are the parent score plus
+// closes) and a new slot opens for the popped node's first child.  Candidate scores are the parent score plus
 // one log-probability, a single fp32 add, so the result is bit-identical to a
 // plain binary-heap implementation of the same rule.
 #include "common.cuh"
@@ -42,25 +40,18 @@ __device__ __forceinline__ uint32_t pack_info(int parent, int depth, int rank) {
 struct WarpSmem {
   float* lp;        // [D*K]
   int* ids;         // [D*K]
-  int* tok;         // [B+1]
-  int* par;         // [B+1]
-  int* dep;         // [B+1]
-  int* rnk;         // [B+1]
-  uint64_t* key;    // [B+1] slot keys (0 = closed)
-  uint32_t* info;   // [B+1] slot (parent, depth, rank)
-  float* psc;       // [B+1] slot parent score
+  uint32_t* node;   // [B+1][4]: tok, parent, depth, rank
+  uint32_t* slot;   // [B+1][4]: key low, key high (0 = closed), info, parent score bits
   uint32_t* stage;  // [32][W]
 };
 
 __host__ __device__ inline size_t build_warp_bytes(int D, int K, int B) {
   const int W = (B + 1 + 31) / 32;
   size_t b = 0;
-  b += align_up(sizeof(uint64_t) * (B + 1), 16);
+  b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
+  b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
   b += align_up(sizeof(float) * D * K, 16);
   b += align_up(sizeof(int) * D * K, 16);
-  b += 4 * align_up(sizeof(int) * (B + 1), 16);
-  b += align_up(sizeof(uint32_t) * (B + 1), 16);
-  b += align_up(sizeof(float) * (B + 1), 16);
   b += align_up(sizeof(uint32_t) * 32 * W, 16);
   return b;
 }
@@ -103,63 +94,64 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   WarpSmem sm;
   {
     size_t off = 0;
-    sm.key = reinterpret_cast<uint64_t*>(base + off); off += align_up(sizeof(uint64_t) * (B + 1), 16);
+    sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
+    sm.slot = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
     sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
     sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
-    sm.tok = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
-    sm.par = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
-    sm.dep = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
-    sm.rnk = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * (B + 1), 16);
-    sm.info = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * (B + 1), 16);
-    sm.psc = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * (B + 1), 16);
     sm.stage = reinterpret_cast<uint32_t*>(base + off);
   }
   const float* lp_r = lp_g + (size_t)req * D * K;
   const int32_t* ids_r = ids_g + (size_t)req * D * K;
   for (int i = lane; i < D * K; i += 32) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
   if (lane == 0) {
-    sm.tok[0] = root_tok[req]; sm.par[0] = -1; sm.dep[0] = 0; sm.rnk[0] = 0;
+    sm.node[0] = static_cast<uint32_t>(root_tok[req]);
+    sm.node[1] = 0xFFFFFFFFu;  // parent -1
+    sm.node[2] = 0;
+    sm.node[3] = 0;
   }
   __syncwarp();
 
   // ---- Algorithm 1 ----
-  // Every pop: each lane scans its own slots (independent shared loads), one
-  // warp-wide argmax picks the winner, all lanes read the winner's slot and the
-  // log-probabilities it needs (broadcast loads), every lane computes the same
-  // new keys, and the node/slot writes go out as one predicated scattered store
-  // per width - no divergent single-lane branches on the critical path.
+  // Each lane keeps the best key among its own slots.  A pop: warp argmax of
+  // the lanes' bests; every lane reads the winner's slot record and the
+  // log-probabilities it needs (broadcast loads) and computes the same new
+  // keys; the node record and both slot updates go out as one predicated
+  // scattered store; every lane then rescans the winner's slots (broadcast
+  // loads, identical results), and the winner and the child's owner update
+  // their bests with selects.  No divergent branch and no extra warp
+  // reduction sits on the per-pop critical path.
+  uint64_t lbest = 0;  // best key among this lane's slots
+  int lbs = 0;         // its slot
   int n = 0, n_slots = 0;
   uint32_t seq = 0;
   if (B > 0) {
+    const uint64_t k0 = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
     if (lane == 0) {
-      sm.key[0] = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
-      sm.info[0] = pack_info(0, 1, 1);
-      sm.psc[0] = 0.f;
+      sm.slot[0] = static_cast<uint32_t>(k0);
+      sm.slot[1] = static_cast<uint32_t>(k0 >> 32);
+      sm.slot[2] = pack_info(0, 1, 1);
+      sm.slot[3] = __float_as_uint(0.f);
     }
+    lbest = (lane == 0) ? k0 : 0ull;
     n_slots = 1;
     seq = 1;
   }
   __syncwarp();
   while (n < B) {
-    uint64_t best = 0;
-    int bslot = 0;
-    for (int sl = lane; sl < n_slots; sl += 32) {
-      const uint64_t k = sm.key[sl];
-      if (k > best) { best = k; bslot = sl; }
-    }
     uint64_t kmax;
-    const int w = warp_argmax_key(best, kmax);
+    const int w = warp_argmax_key(lbest, kmax);
     if (kmax == 0) break;  // no candidate left
-    const int slot = __shfl_sync(0xffffffffu, bslot, w);
-    const uint32_t winfo = sm.info[slot];
-    const float wpsc = sm.psc[slot];
+    const int slot = __shfl_sync(0xffffffffu, lbs, w);
+    const uint4 rec = *reinterpret_cast<const uint4*>(sm.slot + 4 * slot);
+    const uint32_t winfo = rec.z;
+    const float wpsc = __uint_as_float(rec.w);
     const float wscore = from_ordered_bits(static_cast<uint32_t>(kmax >> 32));
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
     const int r = (winfo >> 16) & 0x3F;
     const float lp_sib = sm.lp[(d - 1) * K + (r < K ? r : K - 1)];
     const float lp_child = sm.lp[(d < D ? d : D - 1) * K];
-    const int tokv = sm.ids[(d - 1) * K + (r - 1)];
+    const uint32_t tokv = static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]);
     ++n;
     const bool has_sib = r < K;
     const bool has_child = d < D;
@@ -169,42 +161,58 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     seq += has_child ? 1u : 0u;
     const int cslot = n_slots;
     n_slots += has_child ? 1 : 0;
-    // 32-bit writes: lane 0..3 the node, lane 4 the popped slot's rank, lanes 5-6 the child slot
-    {
-      uint32_t* addr = nullptr;
-      uint32_t val = 0;
-      switch (lane) {
-        case 0: addr = reinterpret_cast<uint32_t*>(sm.tok + n); val = static_cast<uint32_t>(tokv); break;
-        case 1: addr = reinterpret_cast<uint32_t*>(sm.par + n); val = static_cast<uint32_t>(p); break;
-        case 2: addr = reinterpret_cast<uint32_t*>(sm.dep + n); val = static_cast<uint32_t>(d); break;
-        case 3: addr = reinterpret_cast<uint32_t*>(sm.rnk + n); val = static_cast<uint32_t>(r); break;
-        case 4: if (has_sib) { addr = sm.info + slot; val = pack_info(p, d, r + 1); } break;
-        case 5: if (has_child) { addr = sm.info + cslot; val = pack_info(n, d + 1, 1); } break;
-        case 6: if (has_child) { addr = reinterpret_cast<uint32_t*>(sm.psc + cslot); val = __float_as_uint(wscore); } break;
-        default: break;
-      }
-      if (addr) *addr = val;
-    }
-    // 64-bit writes: lane 0 the popped slot's new key (0 closes it), lane 1 the child's key
-    if (lane == 0) sm.key[slot] = sib_key;
-    if (lane == 1 && has_child) sm.key[cslot] = child_key;
+    // lanes 0-3: node record; 4-6: popped slot (key low, key high, info);
+    // 8-11: child slot (key low, key high, info, parent score)
+    const int q = lane & 3;
+    const uint32_t node_v = q == 0 ? tokv : q == 1 ? static_cast<uint32_t>(p)
+                          : q == 2 ? static_cast<uint32_t>(d) : static_cast<uint32_t>(r);
+    const uint32_t sib_v = q == 0 ? static_cast<uint32_t>(sib_key)
+                         : q == 1 ? static_cast<uint32_t>(sib_key >> 32) : pack_info(p, d, r + 1);
+    const uint32_t ch_v = q == 0 ? static_cast<uint32_t>(child_key)
+                        : q == 1 ? static_cast<uint32_t>(child_key >> 32)
+                        : q == 2 ? pack_info(n, d + 1, 1) : __float_as_uint(wscore);
+    const uint32_t val = lane < 4 ? node_v : (lane < 8 ? sib_v : ch_v);
+    const int idx = lane < 4 ? 4 * n + q : (lane < 8 ? 4 * slot + q : 4 * cslot + q);
+    uint32_t* dst = lane < 4 ? sm.node : sm.slot;
+    const bool wr = lane < 4 || lane == 4 || lane == 5 || (lane == 6 && has_sib) ||
+                    (lane >= 8 && lane < 12 && has_child);
+    if (wr) dst[idx] = val;
     __syncwarp();
+    // the winner's new best, computed by every lane (broadcast loads)
+    uint64_t nb = 0;
+    int nbs = w;
+    for (int s0 = w; s0 < n_slots; s0 += 128) {
+      uint64_t k[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sl = s0 + 32 * u;
+        k[u] = sl < n_slots ? *reinterpret_cast<const unsigned long long*>(sm.slot + 4 * sl) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (k[u] > nb) { nb = k[u]; nbs = s0 + 32 * u; }
+    }
+    const bool is_w = lane == w;
+    const bool take_child = has_child && lane == (cslot & 31) && !is_w && child_key > lbest;
+    lbest = is_w ? nb : (take_child ? child_key : lbest);
+    lbs = is_w ? nbs : (take_child ? cslot : lbs);
   }
   __syncwarp();
 
   // ---- flattened tree (coalesced, -1 past the last node) ----
-  const size_t nb = (size_t)req * (B + 1);
+  const size_t nb_out = (size_t)req * (B + 1);
   for (int i = lane; i <= B; i += 32) {
     const bool live = i <= n;
-    tok_out[nb + i] = live ? sm.tok[i] : -1;
-    parent_out[nb + i] = live ? sm.par[i] : -1;
-    depth_out[nb + i] = live ? sm.dep[i] : -1;
-    rank_out[nb + i] = live ? sm.rnk[i] : -1;
+    const uint4 rec = live ? *reinterpret_cast<const uint4*>(sm.node + 4 * i) : make_uint4(0, 0, 0, 0);
+    tok_out[nb_out + i] = live ? static_cast<int32_t>(rec.x) : -1;
+    parent_out[nb_out + i] = live ? static_cast<int32_t>(rec.y) : -1;
+    depth_out[nb_out + i] = live ? static_cast<int32_t>(rec.z) : -1;
+    rank_out[nb_out + i] = live ? static_cast<int32_t>(rec.w) : -1;
   }
   if (lane == 0) n_nodes_out[req] = n;
 
   // ---- ancestor mask, 32 rows at a time staged in shared memory ----
-  uint32_t* mrow = mask_out + nb * W;
+  uint32_t* mrow = mask_out + nb_out * W;
   for (int i0 = 0; i0 <= B; i0 += 32) {
     for (int t = lane; t < 32 * W; t += 32) sm.stage[t] = 0u;
     __syncwarp();
@@ -215,7 +223,7 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
       while (true) {
         st[j >> 5] |= 1u << (j & 31);
         if (j == 0) break;
-        j = sm.par[j];
+        j = static_cast<int>(sm.node[4 * j + 1]);
       }
     }
     __syncwarp();

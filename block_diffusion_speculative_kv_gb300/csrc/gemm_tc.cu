@@ -76,7 +76,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -438,14 +438,11 @@ TcPlan tc_plan(int M_rows, int N_feat, int K, int grid_max) {
   pl.max_slots = ms;
   pl.part_bytes = (size_t)pl.grid * ms * pl.n_tile * kTileN * sizeof(float);
   const int b_bytes = pl.n_tile * 128;
-  // Small row tiles stream weights: a ring of ~80 KB in flight per CTA keeps
-  // HBM busy, and staying under half of the SM's shared memory lets the next
-  // GEMM's CTAs become resident (and start fetching weights) while this one
-  // drains.  The vocabulary-sized LM head and large row tiles take the deepest ring.
-  const bool co_resident = pl.n_tile <= 64 && (long long)N_feat * K < (400LL << 20);
-  const int smem_cap = co_resident ? 112 * 1024 : 227 * 1024;
+  // Weight streaming is bound by the bytes in flight: under load a TMA request
+  // takes ~4 us, so keeping HBM busy takes ~27 MB in flight across the GPU,
+  // i.e. the deepest ring that fits in shared memory.
   int stages = 1;
-  while (stages < 24 && smem_layout(stages + 1, pl.n_tile).total <= (uint32_t)smem_cap) ++stages;
+  while (stages < 24 && smem_layout(stages + 1, pl.n_tile).total <= 227u * 1024u) ++stages;
   pl.stages = stages;
   pl.smem_bytes = smem_layout(stages, pl.n_tile).total;
   (void)b_bytes;

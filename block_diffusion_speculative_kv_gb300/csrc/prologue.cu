@@ -36,10 +36,10 @@ block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
                       int L, int d, int vocab, int mask_id, int head_dim, const RopeFreqs fr,
                       float* __restrict__ x, T* __restrict__ xn, float* __restrict__ ssq,
                       float2* __restrict__ rope, int* status) {
-  __shared__ float red[4];
   const int R = n_req * L;
   const int row = blockIdx.x;
   const int req = row / L, j = row % L;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_trigger();
   int tok = (j == 0) ? anchor[req] : mask_id;
@@ -47,23 +47,42 @@ block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
     if (threadIdx.x == 0) record_status(status, DFLASH_ERR_INVALID_ARG);
     tok = 0;
   }
+  // warp w takes the 128-column parts w, w+4, ...; lane l the 4 columns 4l..4l+3
   const int parts = (d + 127) / 128;
-  for (int p = 0; p < parts; ++p) {
-    const int c = p * 128 + threadIdx.x;
-    float v = 0.f;
-    if (c < d) {
-      v = to_f32<T>(embed[(size_t)tok * d + c]);
-      x[(size_t)row * d + c] = v;
-      xn[(size_t)row * d + c] = from_f32<T>(v * to_f32<T>(gain[c]));
-    }
-    float sq = v * v;
+  constexpr int kMaxParts = 64;  // d <= 8192
+  const T* erow = embed + (size_t)tok * d;
+  for (int p0 = warp; p0 < parts; p0 += 4 * 8) {
+    float v[8][4], g[8][4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
-    __syncthreads();
-    if (threadIdx.x == 0) ssq[(size_t)p * R + row] = red[0] + red[1] + red[2] + red[3];
-    __syncthreads();
+    for (int u = 0; u < 8; ++u) {
+      const int p = p0 + 4 * u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = p * 128 + lane * 4 + e;
+        const bool ok = p < parts && c < d;
+        v[u][e] = ok ? to_f32<T>(erow[c]) : 0.f;
+        g[u][e] = ok ? to_f32<T>(gain[c]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = p0 + 4 * u;
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = p * 128 + lane * 4 + e;
+        if (p < parts && c < d) {
+          x[(size_t)row * d + c] = v[u][e];
+          xn[(size_t)row * d + c] = from_f32<T>(v[u][e] * g[u][e]);
+        }
+        sq += v[u][e] * v[u][e];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0 && p < parts) ssq[(size_t)p * R + row] = sq;
+    }
   }
+  (void)kMaxParts;
   const int half = head_dim / 2;
   const int pos = ctx_len[req] + j;
   for (int i = threadIdx.x; i < half; i += blockDim.x)

@@ -143,6 +143,7 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
     const int nvec = (v1 - v0) / VN;
     constexpr int U = 4;
     // warp-uniform loop: a warp step covers U*32 consecutive vectors, lane-major
+    bool first = true;
     for (int kb = warp * 32 * U; kb < nvec; kb += (kTopkThreads / kWarp) * 32 * U) {
       float x[U][VN];
       bool ok[U];
@@ -154,12 +155,33 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
           const T* p = rp + v0 + (size_t)idx * VN;
           if constexpr (VECTOR) load_vec<T, VN>(p, x[u]);
           else x[u][0] = to_f32<T>(p[0]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VN; ++e) x[u][e] = -CUDART_INF_F;
         }
+      }
+      if (first) {
+        // seed: the K-th largest of the lanes' maxima over this first step is
+        // met or beaten by K distinct values, so it bounds the row's K-th value
+        float lm = -CUDART_INF_F;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < VN; ++e) lm = fmaxf(lm, x[u][e]);
+        float seed = -CUDART_INF_F;
+        for (int r = 0; r < K; ++r) {
+          const uint32_t mb = __reduce_max_sync(0xffffffffu, ordered_bits(lm));
+          seed = from_ordered_bits(mb);
+          const unsigned holders = __ballot_sync(0xffffffffu, ordered_bits(lm) == mb);
+          if (lane == __ffs(holders) - 1) lm = -CUDART_INF_F;
+        }
+        wthr = seed;
+        first = false;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u]) consume(x[u], VN, v0 + (kb + u * 32 + lane) * VN);
-      wthr = from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(thr)));
+      wthr = fmaxf(wthr, from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(thr))));
     }
     const int tail0 = v0 + nvec * VN;
     if (tail0 + tid < v1) {
