@@ -6,10 +6,10 @@
 // query attention, the G = n_q / n_kv query heads of a KV head share its keys,
 // so a KV head's work is G * L query rows (64 for 32/8 heads and L = 16).
 //
-// bf16 path (split-KV, HBM-bound): grid (chunk, kv head, request).  Chunk c <
-// n_chunks covers context positions [c*chunk, (c+1)*chunk) of the request
-// (empty chunks past ctx_len exit at once); the last chunk holds the block's
-// own L keys.  A CTA keeps its query rows in shared memory, streams 64-key
+// bf16 path (split-KV): grid (chunk, kv head, request), sized to one wave.
+// Chunk c covers context positions [c*chunk, (c+1)*chunk) of the request
+// (empty chunks past ctx_len exit at once); the last chunk also takes the
+// block's own L keys as one extra tile.  A CTA keeps its query rows in shared memory, streams 64-key
 // tiles of K and V through a double-buffered cp.async ring (XOR-swizzled 16 B
 // chunks, conflict-free for ldmatrix), computes S = Q K^T and O += P V with
 // bf16 mma.sync (fp32 accumulators) and an online softmax in base 2, and
@@ -80,7 +80,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256, 1)
 attn_split_kernel(const AttnParams p) {
   constexpr int NCH = HD / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) uint8_t smem[];
@@ -95,14 +95,14 @@ attn_split_kernel(const AttnParams p) {
   const int req = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  const bool is_block = chunk_id == p.n_chunks;
+  const bool has_block = chunk_id == p.n_chunks - 1;
   const int ctx = min(max(p.ctx_len[req], 0), p.cap);  // never read past the cache slab
-  int k_begin, k_end;
-  if (is_block) { k_begin = 0; k_end = p.L; }
-  else { k_begin = chunk_id * p.chunk; k_end = min(ctx, k_begin + p.chunk); }
+  const int k_begin = chunk_id * p.chunk;
+  const int k_end = min(ctx, k_begin + p.chunk);
+  const int nct = k_end > k_begin ? (k_end - k_begin + kKeyTile - 1) / kKeyTile : 0;
 
-  const size_t part_row0 = (((size_t)req * p.n_kv + g) * (p.n_chunks + 1) + chunk_id) * QR;
-  if (k_end <= k_begin) {
+  const size_t part_row0 = (((size_t)req * p.n_kv + g) * p.n_chunks + chunk_id) * QR;
+  if (nct == 0 && !has_block) {
     pdl_wait();
     pdl_trigger();
     for (int r = tid; r < QR; r += blockDim.x) {
@@ -112,42 +112,45 @@ attn_split_kernel(const AttnParams p) {
     return;
   }
 
-  const __nv_bfloat16* kbase;
-  const __nv_bfloat16* vbase;
-  long long kv_ld;
-  if (is_block) {
-    kbase = p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + g) * HD;
-    vbase = p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + p.n_kv + g) * HD;
-    kv_ld = p.qkv_ld;
-  } else {
-    const size_t off = ((size_t)req * p.n_kv + g) * p.cap * HD;
-    kbase = p.cache_k + off;
-    vbase = p.cache_v + off;
-    kv_ld = HD;
-  }
+  const __nv_bfloat16* cbase_k = p.cache_k + ((size_t)req * p.n_kv + g) * p.cap * HD;
+  const __nv_bfloat16* cbase_v = p.cache_v + ((size_t)req * p.n_kv + g) * p.cap * HD;
+  const __nv_bfloat16* bbase_k = p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + g) * HD;
+  const __nv_bfloat16* bbase_v =
+      p.qkv + (size_t)req * p.L * p.qkv_ld + (size_t)(p.n_q + p.n_kv + g) * HD;
 
-  auto load_tile = [&](int buf, int key0) {
+  // tile t < nct: context keys k_begin + 64t ...; tile nct (last chunk only):
+  // the block's L keys, read from the QKV output
+  auto load_tile = [&](int buf, int t) {
     uint8_t* dK = sK + buf * kKeyTile * HD * 2;
     uint8_t* dV = sV + buf * kKeyTile * HD * 2;
+    const bool blk = t >= nct;
+    const int key0 = blk ? 0 : k_begin + t * kKeyTile;
+    const int kend = blk ? p.L : k_end;
+    const __nv_bfloat16* kb = blk ? bbase_k : cbase_k;
+    const __nv_bfloat16* vb = blk ? bbase_v : cbase_v;
+    const long long ld = blk ? p.qkv_ld : HD;
     for (int i = tid; i < kKeyTile * NCH; i += blockDim.x) {
       const int r = i / NCH, ch = i % NCH;
       const int key = key0 + r;
-      const bool valid = key < k_end;
-      const size_t off = (size_t)(valid ? key : k_begin) * kv_ld + ch * 8;
-      cp_async16(smem_u32(dK) + swz<HD>(r, ch), kbase + off, valid);
-      cp_async16(smem_u32(dV) + swz<HD>(r, ch), vbase + off, valid);
+      const bool valid = key < kend;
+      const size_t off = (size_t)(valid ? key : key0) * ld + ch * 8;
+      cp_async16(smem_u32(dK) + swz<HD>(r, ch), kb + off, valid);
+      cp_async16(smem_u32(dV) + swz<HD>(r, ch), vb + off, valid);
     }
   };
-  const int ntiles = (k_end - k_begin + kKeyTile - 1) / kKeyTile;
+  const int ntiles = nct + (has_block ? 1 : 0);
+  // Two groups of four warps take alternate tiles (group 0 even, group 1 odd)
+  // from one ring; each warp owns 16 query rows.  kStages-2 tiles run ahead.
+  constexpr int kAhead = kStages - 2;
+  const int npre = ntiles < kAhead ? ntiles : kAhead;
   // The context part of the cache is written only by the injection, several
-  // kernels back: its first ring of tiles is requested before waiting for the
-  // QKV GEMM (each tile is its own cp.async group).
-  const int npre = ntiles < kStages - 1 ? ntiles : kStages - 1;
-  if (!is_block) {
-    for (int t = 0; t < npre; ++t) {
-      load_tile(t, k_begin + t * kKeyTile);
-      cp_async_commit();
-    }
+  // kernels back: the first context tiles are requested before waiting for
+  // the QKV GEMM, the block tile after.  Each tile is its own cp.async group.
+  int issued = 0;
+  while (issued < npre && issued < nct) {
+    load_tile(issued, issued);
+    cp_async_commit();
+    ++issued;
   }
   pdl_wait();
   pdl_trigger();
@@ -161,18 +164,15 @@ attn_split_kernel(const AttnParams p) {
     const __nv_bfloat16* src = p.qkv + ((size_t)req * p.L + j) * p.qkv_ld + (size_t)h * HD + ch * 8;
     cp_async16(smem_u32(sQ) + swz<HD>(r, ch), src, valid);
   }
-  if (is_block) {
-    // block keys come from the QKV output: after the wait; Q joins this group
-    for (int t = 0; t < npre; ++t) {
-      load_tile(t, k_begin + t * kKeyTile);
-      cp_async_commit();
-    }
-  } else {
-    cp_async_commit();   // Q in its own group
+  cp_async_commit();   // Q in its own group
+  while (issued < npre) {   // a block tile among the first ring slots
+    load_tile(issued, issued);
+    cp_async_commit();
+    ++issued;
   }
-  // groups issued so far: npre tiles (+ the Q group for context chunks)
 
-  const int qrow0 = warp * 16;
+  const int grp = warp >> 2;
+  const int qrow0 = (warp & 3) * 16;
   const bool warp_active = qrow0 < QR;
   const int gq = lane >> 2, tq = lane & 3;
   float o[HD / 8][4];
@@ -181,21 +181,23 @@ attn_split_kernel(const AttnParams p) {
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   uint32_t qa[HD / 16][4];
 
-  for (int t = 0; t < ntiles; ++t) {
-    const int key0 = k_begin + t * kKeyTile;
-    // keep kStages-1 tiles in flight: issue tile t+npre (its buffer was freed
-    // by the barrier at the end of the previous iteration), then wait until
-    // tile t (and Q) have landed
-    if (t + npre < ntiles) load_tile((t + npre) % kStages, k_begin + (t + npre) * kKeyTile);
-    cp_async_commit();
-    // groups complete in commit order.  At t = 0 the Q group sits behind the
-    // prefetched tiles, so wait for all but the group just committed; later, a
-    // tile issued inside the loop has kStages-1 newer groups at most (and when
-    // fewer tiles than kStages-1 exist, all were waited for at t = 0)
-    if (t == 0) cp_async_wait<1>();
-    else cp_async_wait<kStages - 1>();
+  for (int it = 0; 2 * it < ntiles; ++it) {
+    // issue the two tiles kAhead ahead (their buffers were last read in
+    // iteration it-1, released by that iteration's closing barrier)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int tn = 2 * it + npre + e;
+      if (tn < ntiles) load_tile(tn % kStages, tn);
+      cp_async_commit();
+    }
+    // groups complete in commit order.  In the first iteration Q sits among
+    // the first groups: wait for all but the two groups just committed.
+    // Later, tiles 2it and 2it+1 have at most kAhead newer groups.
+    if (it == 0) cp_async_wait<2>();
+    else cp_async_wait<kAhead>();
     __syncthreads();
-    if (t == 0 && warp_active) {
+    const int t = 2 * it + grp;
+    if (it == 0 && warp_active) {
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         const int r = qrow0 + (lane & 15);
@@ -203,7 +205,10 @@ attn_split_kernel(const AttnParams p) {
         ldsm_x4(smem_u32(sQ) + swz<HD>(r, ch), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
     }
-    if (warp_active) {
+    if (warp_active && t < ntiles) {
+      const bool blk = t >= nct;
+      const int key0 = blk ? 0 : k_begin + t * kKeyTile;
+      const int kend = blk ? p.L : k_end;
       const uint32_t kb = smem_u32(sK + (t % kStages) * kKeyTile * HD * 2);
       const uint32_t vb = smem_u32(sV + (t % kStages) * kKeyTile * HD * 2);
       float s[kKeyTile / 8][4];
@@ -224,15 +229,15 @@ attn_split_kernel(const AttnParams p) {
       }
       // scale, mask, online softmax (base 2)
       const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
-      const bool iso0 = is_block && !p.anchor_sees_block && (rq0 % p.L) == 0;
-      const bool iso1 = is_block && !p.anchor_sees_block && (rq1 % p.L) == 0;
+      const bool iso0 = blk && !p.anchor_sees_block && (rq0 % p.L) == 0;
+      const bool iso1 = blk && !p.anchor_sees_block && (rq1 % p.L) == 0;
       float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
       for (int n = 0; n < kKeyTile / 8; ++n) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int key = key0 + n * 8 + 2 * tq + e;
-          const bool ok = key < k_end;
+          const bool ok = key < kend;
           float v0 = s[n][e] * p.scale_log2;
           float v1 = s[n][2 + e] * p.scale_log2;
           if (!ok || (iso0 && key > 0)) v0 = -CUDART_INF_F;
@@ -293,11 +298,53 @@ attn_split_kernel(const AttnParams p) {
     __syncthreads();
   }
 
-  // row sums: reduce over the quad
+  // row sums: reduce over the quad (each group its own)
 #pragma unroll
   for (int off = 1; off <= 2; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  // ---- merge the two groups' states (group 1 -> shared memory -> group 0) ----
+  float* mo = reinterpret_cast<float*>(sK);   // [QRp][HD]; the ring is free now
+  float* mml = mo + QRp * HD;                   // [QRp][2] running max and sum
+  if (grp == 1 && warp_active) {
+    const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      const int dc = n * 8 + 2 * tq;
+      mo[rq0 * HD + dc] = o[n][0];
+      mo[rq0 * HD + dc + 1] = o[n][1];
+      mo[rq1 * HD + dc] = o[n][2];
+      mo[rq1 * HD + dc + 1] = o[n][3];
+    }
+    if (tq == 0) {
+      mml[rq0 * 2] = m0; mml[rq0 * 2 + 1] = l0;
+      mml[rq1 * 2] = m1; mml[rq1 * 2 + 1] = l1;
+    }
+  }
+  __syncthreads();
+  if (grp == 1) return;
+  if (warp_active) {
+    const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
+    const float om0 = mml[rq0 * 2], ol0 = mml[rq0 * 2 + 1];
+    const float om1 = mml[rq1 * 2], ol1 = mml[rq1 * 2 + 1];
+    const float nm0 = fmaxf(m0, om0), nm1 = fmaxf(m1, om1);
+    const float b0 = (nm0 == -CUDART_INF_F) ? 0.f : nm0;
+    const float b1 = (nm1 == -CUDART_INF_F) ? 0.f : nm1;
+    const float a0 = exp2f(m0 - b0), c0 = exp2f(om0 - b0);
+    const float a1 = exp2f(m1 - b1), c1 = exp2f(om1 - b1);
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      const int dc = n * 8 + 2 * tq;
+      o[n][0] = o[n][0] * a0 + mo[rq0 * HD + dc] * c0;
+      o[n][1] = o[n][1] * a0 + mo[rq0 * HD + dc + 1] * c0;
+      o[n][2] = o[n][2] * a1 + mo[rq1 * HD + dc] * c1;
+      o[n][3] = o[n][3] * a1 + mo[rq1 * HD + dc + 1] * c1;
+    }
+    l0 = l0 * a0 + ol0 * c0;
+    l1 = l1 * a1 + ol1 * c1;
+    m0 = nm0;
+    m1 = nm1;
   }
   if (warp_active) {
     const int rq0 = qrow0 + gq, rq1 = rq0 + 8;
@@ -341,7 +388,7 @@ attn_combine_kernel(const AttnParams p) {
   pdl_wait();
   pdl_trigger();
   if (r >= QR) return;
-  const int nparts = p.n_chunks + 1;
+  const int nparts = p.n_chunks;
   const size_t base = ((size_t)req * p.n_kv + g) * nparts * QR;
   float M = -CUDART_INF_F;
   for (int c0 = 0; c0 < nparts; c0 += 32) {
@@ -451,13 +498,16 @@ attn_f32_kernel(const AttnParamsF32 p) {
 }  // namespace
 
 int attn_chunk(int max_ctx, int n_kv, int n_req) {
-  // one CTA per SM: each holds a deep ring of K/V tiles
-  const long long target = num_sms();
-  long long work = (long long)max_ctx * n_kv * n_req;
-  long long c = (work + target - 1) / target;
+  // One CTA per SM holds a deep ring: when a wave covers every (request, KV
+  // head) pair, size the chunks so the whole grid is one wave; otherwise aim
+  // for several waves of short chunks so ragged contexts balance.
+  const long long sms = num_sms();
+  const long long pairs = (long long)n_kv * n_req;
+  long long n_chunks = pairs <= sms ? sms / pairs : (4 * sms + pairs - 1) / pairs;
+  if (n_chunks < 1) n_chunks = 1;
+  long long c = (max_ctx + n_chunks - 1) / n_chunks;
   c = (c + kKeyTile - 1) / kKeyTile * kKeyTile;
   if (c < kKeyTile) c = kKeyTile;
-  if (c > 8192) c = 8192;
   return static_cast<int>(c);
 }
 
@@ -471,7 +521,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
   const int warps = (QR + 15) / 16;
   if (warps > 4) return set_error(DFLASH_ERR_UNSUPPORTED, "attention: G*L > 64 query rows");
   const size_t smem = attn_smem_bytes(p.G, p.L, head_dim);
-  dim3 grid(p.n_chunks + 1, p.n_kv, p.n_req);
+  dim3 grid(p.n_chunks, p.n_kv, p.n_req);
   dim3 cgrid((QR + 3) / 4, p.n_kv, p.n_req);
   if (head_dim == 128) {
     static bool set = false;
@@ -482,7 +532,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     }
     {
       TraceScope ts("attn_split", st);
-      launch_k(attn_split_kernel<128>, grid, dim3(128), smem, st, p);
+      launch_k(attn_split_kernel<128>, grid, dim3(256), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
     launch_k(attn_combine_kernel<128>, cgrid, dim3(128), 0, st, p);
@@ -495,7 +545,7 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
     }
     {
       TraceScope ts("attn_split", st);
-      launch_k(attn_split_kernel<64>, grid, dim3(128), smem, st, p);
+      launch_k(attn_split_kernel<64>, grid, dim3(256), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
     launch_k(attn_combine_kernel<64>, cgrid, dim3(128), 0, st, p);

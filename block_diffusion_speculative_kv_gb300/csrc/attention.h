@@ -20,11 +20,11 @@ struct AttnParams {
   int cap;
   int n_req, n_q, n_kv, G, L;
   int chunk;      // context keys per CTA (multiple of 64)
-  int n_chunks;   // context chunks per (request, KV head); one more holds the block
+  int n_chunks;   // chunks per (request, KV head); the last also takes the block keys
   float scale_log2;
   int anchor_sees_block;
-  float* part_o;   // [n_req][n_kv][n_chunks+1][G*L][hd]
-  float* part_ml;  // [n_req][n_kv][n_chunks+1][G*L][2]
+  float* part_o;   // [n_req][n_kv][n_chunks][G*L][hd]
+  float* part_ml;  // [n_req][n_kv][n_chunks][G*L][2]
   __nv_bfloat16* out;
   long long out_ld;
 };

@@ -96,9 +96,9 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
   }
   w.gpart = take(gp);
   // attention partials: enough chunks for ~2 CTAs per SM plus the block chunk
-  int cap_chunks = (2 * sms + d.n_kv * n_req - 1) / (d.n_kv * n_req) + 2;
+  int cap_chunks = (4 * sms + d.n_kv * n_req - 1) / (d.n_kv * n_req) + 2;
   w.attn_chunks_cap = cap_chunks;
-  const size_t arows = (size_t)n_req * d.n_kv * (cap_chunks + 1) * G * L;
+  const size_t arows = (size_t)n_req * d.n_kv * cap_chunks * G * L;
   w.apart_o = take(m.bf16 ? sizeof(float) * arows * d.head_dim : 0);
   w.apart_ml = take(m.bf16 ? sizeof(float) * arows * 2 : 0);
   w.tpart = take(topk_part_bytes(n_req * D, 32));
@@ -334,9 +334,10 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
   dflash_status st = check_launch("block prologue");
   if (st) return st;
 
-  // attention decomposition
+  // attention decomposition: the last chunk also takes the block keys, so
+  // there is at least one chunk even without context
   int chunk = attn_chunk(max_ctx > 0 ? max_ctx : 1, d.n_kv, n_req);
-  int n_chunks = (max_ctx + chunk - 1) / chunk;
+  int n_chunks = max_ctx > 0 ? (max_ctx + chunk - 1) / chunk : 1;
   if (n_chunks > W.attn_chunks_cap) {
     chunk = ((max_ctx + W.attn_chunks_cap - 1) / W.attn_chunks_cap + 63) / 64 * 64;
     n_chunks = (max_ctx + chunk - 1) / chunk;
