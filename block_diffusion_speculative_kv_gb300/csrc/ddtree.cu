@@ -9,16 +9,23 @@
 // GPU formulation of the heap.  The candidates alive at any time are exactly
 // one per "open" parent: the parent's next unpopped child rank (children of a
 // node are popped in rank order, since a sibling is offered only after its
-// predecessor pops).  So the heap is kept as a set of slots in shared memory,
-// one per open parent; slot s belongs to lane s % 32, which keeps the best key
-// among its slots in a register.  Keys are 64-bit:
-// order-preserving score bits, then the complemented creation counter, so
-// equal scores pop in creation order.  A pop is a warp-wide maximum of the
-// lanes' bests (redux.sync on the high word, and on the low word only when the
-// high word ties); the popped slot advances to its next rank in place (or
-// closes) and a new slot opens for the popped node's first child.  Candidate scores are the parent score plus
-// one log-probability, a single fp32 add, so the result is bit-identical to a
-// plain binary-heap implementation of the same rule.
+// predecessor pops).  So the heap is a set of slots, one per open parent; slot
+// s = 32*i + l lives in register i of lane l (its 64-bit key) and in shared
+// memory (parent, depth, rank and the parent's score).  A key is
+//   [63:32] order-preserving score bits
+//   [31:11] MAX - creation counter (equal scores pop in creation order)
+//   [10:5]  register index i,  [4:0] lane l
+// so keys are unique and the maximum key names its own slot: a pop is two
+// warp reductions (redux.sync on the high word, then on the low word among
+// lanes that hold the high maximum), with no ballot or shuffle to find the
+// winner.  Each lane keeps the maximum of its keys and, precomputed from its
+// slot record while the next reductions run, the two scores that popping that
+// candidate would create (its next sibling, its first child); the winner's two
+// come over in shuffles.  The popped slot advances to its next rank in place
+// (or closes) and a new slot opens for the popped node's first child.
+// Candidate scores are the parent score plus one log-probability, a single
+// fp32 add, so the result is bit-identical to a plain binary-heap
+// implementation of the same rule.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,10 +34,12 @@ namespace dfl {
 namespace {
 
 constexpr int kBuildWarps = 4;
+constexpr uint32_t kSeqMax = (1u << 21) - 1;   // creation counter field
 
-__device__ __forceinline__ uint64_t make_key(float score, uint32_t seq) {
+__device__ __forceinline__ uint64_t make_key(float score, uint32_t seq, int reg, int lane) {
   return (static_cast<uint64_t>(ordered_bits(score)) << 32) |
-         static_cast<uint64_t>(0xFFFFFFFFu - seq);
+         static_cast<uint64_t>(((kSeqMax - seq) << 11) | (static_cast<uint32_t>(reg) << 5) |
+                               static_cast<uint32_t>(lane));
 }
 __device__ __forceinline__ uint32_t pack_info(int parent, int depth, int rank) {
   return static_cast<uint32_t>(parent) | (static_cast<uint32_t>(depth) << 11) |
@@ -41,7 +50,8 @@ struct WarpSmem {
   float* lp;        // [D*K]
   int* ids;         // [D*K]
   uint32_t* node;   // [B+1][4]: tok, parent, depth, rank
-  uint32_t* slot;   // [B+1][4]: key low, key high (0 = closed), info, parent score bits
+  uint32_t* sinfo;  // [B+1] slot: parent | depth << 11 | next rank << 16
+  float* spsc;      // [B+1] slot: parent score
   uint32_t* stage;  // [32][W]
 };
 
@@ -49,32 +59,32 @@ __host__ __device__ inline size_t build_warp_bytes(int D, int K, int B) {
   const int W = (B + 1 + 31) / 32;
   size_t b = 0;
   b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
-  b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
+  b += align_up(sizeof(uint32_t) * (B + 1), 16);
+  b += align_up(sizeof(float) * (B + 1), 16);
   b += align_up(sizeof(float) * D * K, 16);
   b += align_up(sizeof(int) * D * K, 16);
   b += align_up(sizeof(uint32_t) * 32 * W, 16);
   return b;
 }
 
-// Warp-wide maximum of 64-bit keys; returns the lane holding it (keys unique
-// unless all are 0) and the key.
-__device__ __forceinline__ int warp_argmax_key(uint64_t k, uint64_t& kmax) {
-  const unsigned FULL = 0xffffffffu;
-  const uint32_t hi = static_cast<uint32_t>(k >> 32);
-  const uint32_t lo = static_cast<uint32_t>(k);
-  const uint32_t mhi = __reduce_max_sync(FULL, hi);
-  unsigned b = __ballot_sync(FULL, hi == mhi);
-  uint32_t mlo;
-  if (__popc(b) == 1) {
-    mlo = __shfl_sync(FULL, lo, __ffs(b) - 1);
-  } else {
-    mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
-    b = __ballot_sync(FULL, hi == mhi && lo == mlo);
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// Maximum of a lane's NSL keys (pairwise tree).
+template <int NSL>
+__device__ __forceinline__ uint64_t max_keys(const uint64_t (&key)[NSL]) {
+  uint64_t t[NSL];
+#pragma unroll
+  for (int i = 0; i < NSL; ++i) t[i] = key[i];
+#pragma unroll
+  for (int s = 1; s < NSL; s *= 2) {
+#pragma unroll
+    for (int i = 0; i + s < NSL; i += 2 * s) t[i] = umax64(t[i], t[i + s]);
   }
-  kmax = (static_cast<uint64_t>(mhi) << 32) | mlo;
-  return __ffs(b) - 1;
+  return t[0];
 }
 
+// One request per warp; NSL = key registers per lane, 32 * NSL >= B + 1 slots.
+template <int NSL>
 __global__ void __launch_bounds__(kBuildWarps * 32)
 ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
                     const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
@@ -82,6 +92,7 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
                     int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
                     int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int req = blockIdx.x * kBuildWarps + wib;
@@ -95,7 +106,8 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   {
     size_t off = 0;
     sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
-    sm.slot = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
+    sm.sinfo = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * (B + 1), 16);
+    sm.spsc = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * (B + 1), 16);
     sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
     sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
     sm.stage = reinterpret_cast<uint32_t*>(base + off);
@@ -108,94 +120,86 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     sm.node[1] = 0xFFFFFFFFu;  // parent -1
     sm.node[2] = 0;
     sm.node[3] = 0;
+    sm.sinfo[0] = pack_info(0, 1, 1);
+    sm.spsc[0] = 0.f;
   }
   __syncwarp();
 
   // ---- Algorithm 1 ----
-  // Each lane keeps the best key among its own slots.  A pop: warp argmax of
-  // the lanes' bests; every lane reads the winner's slot record and the
-  // log-probabilities it needs (broadcast loads) and computes the same new
-  // keys; the node record and both slot updates go out as one predicated
-  // scattered store; every lane then rescans the winner's slots (broadcast
-  // loads, identical results), and the winner and the child's owner update
-  // their bests with selects.  No divergent branch and no extra warp
-  // reduction sits on the per-pop critical path.
-  uint64_t lbest = 0;  // best key among this lane's slots
-  int lbs = 0;         // its slot
+  uint64_t key[NSL];
+#pragma unroll
+  for (int i = 0; i < NSL; ++i) key[i] = 0ull;
   int n = 0, n_slots = 0;
   uint32_t seq = 0;
   if (B > 0) {
-    const uint64_t k0 = make_key(__fadd_rn(0.f, sm.lp[0]), 0u);
-    if (lane == 0) {
-      sm.slot[0] = static_cast<uint32_t>(k0);
-      sm.slot[1] = static_cast<uint32_t>(k0 >> 32);
-      sm.slot[2] = pack_info(0, 1, 1);
-      sm.slot[3] = __float_as_uint(0.f);
-    }
-    lbest = (lane == 0) ? k0 : 0ull;
+    if (lane == 0) key[0] = make_key(__fadd_rn(0.f, sm.lp[0]), 0u, 0, 0);
     n_slots = 1;
     seq = 1;
   }
-  __syncwarp();
+  uint64_t lbest = key[0];
+  // the scores that popping this lane's best candidate would create
+  float b_sib = 0.f, b_child = 0.f;
+  uint32_t b_info = 0;
+  auto precompute = [&]() {
+    const int slot = static_cast<int>((static_cast<uint32_t>(lbest) >> 5) & 63u) * 32 + lane;
+    const int sl = lbest != 0ull ? slot : 0;
+    b_info = sm.sinfo[sl];
+    const float psc = sm.spsc[sl];
+    const int d = (b_info >> 11) & 0x1F;
+    const int r = (b_info >> 16) & 0x3F;
+    const float score = from_ordered_bits(static_cast<uint32_t>(lbest >> 32));
+    const int is = (d - 1) * K + (r < K ? r : K - 1);
+    const int ic = (d < D ? d : D - 1) * K;
+    b_sib = __fadd_rn(psc, sm.lp[is > 0 ? is : 0]);
+    b_child = __fadd_rn(score, sm.lp[ic > 0 ? ic : 0]);
+  };
+  precompute();
   while (n < B) {
-    uint64_t kmax;
-    const int w = warp_argmax_key(lbest, kmax);
-    if (kmax == 0) break;  // no candidate left
-    const int slot = __shfl_sync(0xffffffffu, lbs, w);
-    const uint4 rec = *reinterpret_cast<const uint4*>(sm.slot + 4 * slot);
-    const uint32_t winfo = rec.z;
-    const float wpsc = __uint_as_float(rec.w);
-    const float wscore = from_ordered_bits(static_cast<uint32_t>(kmax >> 32));
+    const uint32_t hi = static_cast<uint32_t>(lbest >> 32);
+    const uint32_t lo = static_cast<uint32_t>(lbest);
+    const uint32_t mhi = __reduce_max_sync(FULL, hi);
+    const uint32_t mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
+    if (mlo == 0u) break;  // no candidate left
+    const int w = static_cast<int>(mlo & 31u);
+    const int wi = static_cast<int>((mlo >> 5) & 63u);
+    const float s_sib = __shfl_sync(FULL, b_sib, w);
+    const float s_child = __shfl_sync(FULL, b_child, w);
+    const uint32_t winfo = __shfl_sync(FULL, b_info, w);
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
     const int r = (winfo >> 16) & 0x3F;
-    const float lp_sib = sm.lp[(d - 1) * K + (r < K ? r : K - 1)];
-    const float lp_child = sm.lp[(d < D ? d : D - 1) * K];
-    const uint32_t tokv = static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]);
     ++n;
     const bool has_sib = r < K;
     const bool has_child = d < D;
-    const uint64_t sib_key = has_sib ? make_key(__fadd_rn(wpsc, lp_sib), seq) : 0ull;
+    const uint64_t sib_key = has_sib ? make_key(s_sib, seq, wi, w) : 0ull;
     seq += has_sib ? 1u : 0u;
-    const uint64_t child_key = make_key(__fadd_rn(wscore, lp_child), seq);
-    seq += has_child ? 1u : 0u;
     const int cslot = n_slots;
+    const int co = cslot & 31, ci = cslot >> 5;
+    const uint64_t child_key = has_child ? make_key(s_child, seq, ci, co) : 0ull;
+    seq += has_child ? 1u : 0u;
     n_slots += has_child ? 1 : 0;
-    // lanes 0-3: node record; 4-6: popped slot (key low, key high, info);
-    // 8-11: child slot (key low, key high, info, parent score)
-    const int q = lane & 3;
-    const uint32_t node_v = q == 0 ? tokv : q == 1 ? static_cast<uint32_t>(p)
-                          : q == 2 ? static_cast<uint32_t>(d) : static_cast<uint32_t>(r);
-    const uint32_t sib_v = q == 0 ? static_cast<uint32_t>(sib_key)
-                         : q == 1 ? static_cast<uint32_t>(sib_key >> 32) : pack_info(p, d, r + 1);
-    const uint32_t ch_v = q == 0 ? static_cast<uint32_t>(child_key)
-                        : q == 1 ? static_cast<uint32_t>(child_key >> 32)
-                        : q == 2 ? pack_info(n, d + 1, 1) : __float_as_uint(wscore);
-    const uint32_t val = lane < 4 ? node_v : (lane < 8 ? sib_v : ch_v);
-    const int idx = lane < 4 ? 4 * n + q : (lane < 8 ? 4 * slot + q : 4 * cslot + q);
-    uint32_t* dst = lane < 4 ? sm.node : sm.slot;
-    const bool wr = lane < 4 || lane == 4 || lane == 5 || (lane == 6 && has_sib) ||
-                    (lane >= 8 && lane < 12 && has_child);
-    if (wr) dst[idx] = val;
-    __syncwarp();
-    // the winner's new best, computed by every lane (broadcast loads)
-    uint64_t nb = 0;
-    int nbs = w;
-    for (int s0 = w; s0 < n_slots; s0 += 128) {
-      uint64_t k[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sl = s0 + 32 * u;
-        k[u] = sl < n_slots ? *reinterpret_cast<const unsigned long long*>(sm.slot + 4 * sl) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (k[u] > nb) { nb = k[u]; nbs = s0 + 32 * u; }
+    // records: the node (lane 0), the advanced slot (winner), the new slot (owner)
+    if (lane == 0) {
+      const uint4 rec = make_uint4(static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]),
+                                   static_cast<uint32_t>(p), static_cast<uint32_t>(d),
+                                   static_cast<uint32_t>(r));
+      *reinterpret_cast<uint4*>(sm.node + 4 * n) = rec;
     }
     const bool is_w = lane == w;
-    const bool take_child = has_child && lane == (cslot & 31) && !is_w && child_key > lbest;
-    lbest = is_w ? nb : (take_child ? child_key : lbest);
-    lbs = is_w ? nbs : (take_child ? cslot : lbs);
+    const bool is_o = has_child && lane == co;
+    if (is_w && has_sib) sm.sinfo[wi * 32 + w] = pack_info(p, d, r + 1);
+    if (is_o) {
+      sm.sinfo[cslot] = pack_info(n, d + 1, 1);
+      sm.spsc[cslot] = from_ordered_bits(mhi);
+    }
+#pragma unroll
+    for (int i = 0; i < NSL; ++i) {
+      if (is_w && i == wi) key[i] = sib_key;
+      if (is_o && i == ci) key[i] = child_key;
+    }
+    const uint64_t rescan = max_keys<NSL>(key);
+    lbest = is_w ? rescan : (is_o ? umax64(lbest, child_key) : lbest);
+    if (is_w || is_o) precompute();
   }
   __syncwarp();
 
@@ -233,20 +237,31 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   }
 }
 
-void launch_build(const TreeBuildLaunch& a, cudaStream_t st) {
-  const size_t per_warp = build_warp_bytes(a.D, a.K, a.B);
-  const size_t smem = per_warp * kBuildWarps;
+template <int NSL>
+void launch_build_t(const TreeBuildLaunch& a, size_t smem, cudaStream_t st) {
   static bool attr_set = false;  // per instantiation, per process
   if (!attr_set) {
-    cudaFuncSetAttribute(ddtree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(ddtree_build_kernel<NSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          200 * 1024);
     attr_set = true;
   }
   dim3 grid(ceil_div(a.n_req, kBuildWarps));
   TraceScope ts("ddtree_build", st);
-  launch_k(ddtree_build_kernel, grid, dim3(kBuildWarps * 32), smem, st, a.n_req, a.D, a.K, a.B,
-           a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank,
+  launch_k(ddtree_build_kernel<NSL>, grid, dim3(kBuildWarps * 32), smem, st, a.n_req, a.D, a.K,
+           a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank,
            a.mask);
+}
+
+void launch_build(const TreeBuildLaunch& a, cudaStream_t st) {
+  const size_t smem = build_warp_bytes(a.D, a.K, a.B) * kBuildWarps;
+  const int slots = a.B + 1;
+  if (slots <= 32) launch_build_t<1>(a, smem, st);
+  else if (slots <= 64) launch_build_t<2>(a, smem, st);
+  else if (slots <= 96) launch_build_t<3>(a, smem, st);
+  else if (slots <= 160) launch_build_t<5>(a, smem, st);
+  else if (slots <= 288) launch_build_t<9>(a, smem, st);
+  else if (slots <= 544) launch_build_t<17>(a, smem, st);
+  else launch_build_t<33>(a, smem, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -78,17 +78,39 @@ struct EpiParams {
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
 // Row scales of the rows [row0, row0 + n) into s_scale (s = 1 without ssq).
+// A row's partial sums are split over tpr threads of one warp (tpr a power of
+// two), each adding every tpr-th part with several loads in flight, then
+// folded with shuffles.  Every thread of the group must call this (nthreads a
+// multiple of 32).
 __device__ __forceinline__ void epi_row_scales(const EpiParams& e, int row0, int n,
                                                float* s_scale, int tid, int nthreads) {
-  for (int r = tid; r < n; r += nthreads) {
-    float s = 1.f;
+  if (e.ssq_in == nullptr) {
+    for (int r = tid; r < n; r += nthreads) s_scale[r] = 1.f;
+    return;
+  }
+  int tpr = 1;
+  while (tpr < 32 && tpr * 2 * n <= nthreads) tpr *= 2;
+  const int per_pass = nthreads / tpr;
+  const int q = tid % tpr;
+  for (int rb = 0; rb < n; rb += per_pass) {
+    const int r = rb + tid / tpr;
     const int row = row0 + r;
-    if (e.ssq_in != nullptr && row < e.M_rows) {
-      float acc = 0.f;
-      for (int p = 0; p < e.ssq_parts; ++p) acc += e.ssq_in[(size_t)p * e.M_rows + row];
-      s = rsqrtf(acc * e.inv_d + e.eps);
+    const bool valid = r < n && row < e.M_rows;
+    float acc = 0.f;
+    if (valid) {
+      const float* src = e.ssq_in + row;
+      int p = q;
+      for (; p + 3 * tpr < e.ssq_parts; p += 4 * tpr) {
+        const float v0 = src[(size_t)p * e.M_rows];
+        const float v1 = src[(size_t)(p + tpr) * e.M_rows];
+        const float v2 = src[(size_t)(p + 2 * tpr) * e.M_rows];
+        const float v3 = src[(size_t)(p + 3 * tpr) * e.M_rows];
+        acc += (v0 + v1) + (v2 + v3);
+      }
+      for (; p < e.ssq_parts; p += tpr) acc += src[(size_t)p * e.M_rows];
     }
-    s_scale[r] = s;
+    for (int off = tpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (r < n && q == 0) s_scale[r] = valid ? rsqrtf(acc * e.inv_d + e.eps) : 1.f;
   }
 }
 

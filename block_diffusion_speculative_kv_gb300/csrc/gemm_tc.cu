@@ -19,7 +19,9 @@
 // memory ring (weights evict-first, activations evict-last in L2); warp 1
 // owns the TMEM allocation and its lane 0 issues tcgen05.mma (128 x n_tile x 16,
 // four per 64-wide K block) and tcgen05.commit to release ring slots; warps
-// 2-5 drain TMEM (tcgen05.ld, 32 lanes each) and run the epilogue.  Every
+// 2-5 drain TMEM (tcgen05.ld, 32 lanes each) and run the epilogue.  A CTA's
+// tiles alternate between two TMEM accumulators, so the MMAs of the next tile
+// never wait for the epilogue of the previous one.  Every
 // mbarrier wait is bounded in time; on expiry the CTA records
 // DFLASH_ERR_TIMEOUT in the status word, drains its outstanding copies and
 // MMAs (again bounded), frees TMEM and exits.
@@ -67,7 +69,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile) {
   L.a_off = 0;
   L.b_off = stages * kABytes;
   L.bar_off = L.b_off + stages * b_bytes;
-  const uint32_t bar_bytes = (2 * stages + 3) * 8 + 16 + 16;
+  const uint32_t bar_bytes = (2 * stages + 5) * 8 + 16 + 16;
   L.buf_off = (L.bar_off + bar_bytes + 15) / 16 * 16;
   L.scale_off = L.buf_off + kChunk * kBufLd * 4;
   L.red_off = L.scale_off + n_tile * 4;
@@ -88,9 +90,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   uint8_t* sB = smem + SL.b_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL.bar_off);
   uint64_t* empty = full + p.stages;
-  uint64_t* accf = empty + p.stages;
-  uint64_t* acce = accf + 1;
-  uint64_t* drain = acce + 1;
+  uint64_t* accf = empty + p.stages;   // [2] accumulator a holds a finished tile
+  uint64_t* acce = accf + 2;           // [2] accumulator a has been drained
+  uint64_t* drain = acce + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [0] abort, [1] last
   float* buf = reinterpret_cast<float*>(smem + SL.buf_off);
@@ -105,15 +107,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   const long long u_begin = (long long)c * U / G;
   const long long u_end = (long long)(c + 1) * U / G;
   const int KB = p.kblocks;
-  const uint32_t tmem_cols = p.n_tile < 32 ? 32u : static_cast<uint32_t>(p.n_tile);
+  // two accumulators of n_tile columns: the MMAs of a CTA's next tile run while
+  // the epilogue drains the previous one
+  const uint32_t tmem_cols = 2 * p.n_tile < 32 ? 32u : static_cast<uint32_t>(2 * p.n_tile);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    ptx::mbar_init(accf, 1);
-    ptx::mbar_init(acce, kEpiThreads);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&accf[a], 1);
+      ptx::mbar_init(&acce[a], kEpiThreads);
+    }
     ptx::mbar_init(drain, 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -204,14 +210,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_bf16_f32(128, p.n_tile);
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0;
+      int tile_i = 0;   // tiles of this CTA so far: accumulator tile_i & 1
       bool issued_any = false;
       long long u = u_begin;
       while (u < u_end && !flags[0]) {
         const int t = static_cast<int>(u / KB);
         const int kb0 = static_cast<int>(u - (long long)t * KB);
         const int n = static_cast<int>((KB - kb0) < (u_end - u) ? (KB - kb0) : (u_end - u));
-        if (!ptx::mbar_wait_bounded(acce, acc_phase ^ 1u, kTimeoutNs, flags)) {
+        const int acc = tile_i & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.n_tile);
+        if (!ptx::mbar_wait_bounded(&acce[acc], acc_phase ^ 1u, kTimeoutNs, flags)) {
           record_status(p.status, DFLASH_ERR_TIMEOUT);
           flags[0] = 1;
           break;
@@ -230,15 +240,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
           const uint64_t b_desc = ptx::sw128_kmajor_desc(ptx::smem_addr(sB + stage * b_bytes));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            ptx::mma_bf16(tmem_base, a_desc + 2 * k, b_desc + 2 * k, idesc,
+            ptx::mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
                           (i > 0 || k > 0) ? 1u : 0u);
           ptx::mma_commit(&empty[stage]);
           issued_any = true;
           if (++stage == p.stages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        ptx::mma_commit(accf);
-        acc_phase ^= 1u;
+        ptx::mma_commit(&accf[acc]);
+        ++tile_i;
         u += n;
       }
       if (flags[0] && issued_any) {
@@ -252,9 +262,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int ew = warp & 3;            // TMEM lane quarter this warp may access
     const int f = ew * 32 + lane;       // tile column (weight row) of this thread
     const int etid = threadIdx.x - 64;  // 0..127
-    uint32_t acc_phase = 0;
+    int tile_i = 0;
     long long u = u_begin;
     while (u < u_end) {
+      const int acc = tile_i & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
       const int t = static_cast<int>(u / KB);
       const int kb0 = static_cast<int>(u - (long long)t * KB);
       const int n = static_cast<int>((KB - kb0) < (u_end - u) ? (KB - kb0) : (u_end - u));
@@ -267,7 +279,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       const int nslots = c_last - c_first + 1;
       const bool single = nslots == 1;
 
-      const bool ok = ptx::mbar_wait_bounded(accf, acc_phase, kTimeoutNs, flags);
+      const bool ok = ptx::mbar_wait_bounded(&accf[acc], acc_phase, kTimeoutNs, flags);
       if (!ok) {
         record_status(p.status, DFLASH_ERR_TIMEOUT);
         flags[0] = 1;
@@ -284,7 +296,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       for (int c0 = 0; c0 < nrows; c0 += kChunk) {
         float v[16];
         __syncwarp();
-        ptx::tmem_ld_32x16(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + c0, v);
+        ptx::tmem_ld_32x16(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                               static_cast<uint32_t>(acc * p.n_tile + c0), v);
         if (single) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) buf[j * kBufLd + f] = v[j];
@@ -298,7 +311,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(acce);
+      ptx::mbar_arrive(&acce[acc]);
 
       if (single) {
         if (p.epi.kind == EPI_RESID) {
@@ -351,7 +364,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         }
         ptx::named_bar_sync(1, kEpiThreads);
       }
-      acc_phase ^= 1u;
+      ++tile_i;
       u += n;
     }
   }
