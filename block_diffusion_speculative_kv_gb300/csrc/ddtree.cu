@@ -11,18 +11,19 @@
 // node are popped in rank order, since a sibling is offered only after its
 // predecessor pops).  So the heap is a set of slots, one per open parent; slot
 // s = 32*i + l lives in register i of lane l (its 64-bit key) and in shared
-// memory (parent, depth, rank and the parent's score).  A key is
+// memory (parent, depth, rank, and the two log-probability terms popping it
+// needs: its next sibling's score and its child's log-probability).  A key is
 //   [63:32] order-preserving score bits
 //   [31:11] MAX - creation counter (equal scores pop in creation order)
 //   [10:5]  register index i,  [4:0] lane l
 // so keys are unique and the maximum key names its own slot: a pop is two
 // warp reductions (redux.sync on the high word, then on the low word among
 // lanes that hold the high maximum), with no ballot or shuffle to find the
-// winner.  Each lane keeps the maximum of its keys and, precomputed from its
-// slot record while the next reductions run, the two scores that popping that
-// candidate would create (its next sibling, its first child); the winner's two
-// come over in shuffles.  The popped slot advances to its next rank in place
-// (or closes) and a new slot opens for the popped node's first child.
+// winner.  Each lane keeps the maximum of its keys and loads that slot's record
+// while the next reductions run; the winner's record comes over in shuffles.
+// The popped slot advances to its next rank in place (or closes) and a new
+// slot opens for the popped node's first child.  Every lane runs the same
+// branch-free sequence, so no lane holds the reductions back.
 // Candidate scores are the parent score plus one log-probability, a single
 // fp32 add, so the result is bit-identical to a plain binary-heap
 // implementation of the same rule.
@@ -50,8 +51,8 @@ struct WarpSmem {
   float* lp;        // [D*K]
   int* ids;         // [D*K]
   uint32_t* node;   // [B+1][4]: tok, parent, depth, rank
-  uint32_t* sinfo;  // [B+1] slot: parent | depth << 11 | next rank << 16
-  float* spsc;      // [B+1] slot: parent score
+  uint4* slot;      // [B+1]: info (parent | depth << 11 | rank << 16), parent score,
+                    //        next sibling's score, log-prob of the first child
   uint32_t* stage;  // [32][W]
 };
 
@@ -59,8 +60,7 @@ __host__ __device__ inline size_t build_warp_bytes(int D, int K, int B) {
   const int W = (B + 1 + 31) / 32;
   size_t b = 0;
   b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
-  b += align_up(sizeof(uint32_t) * (B + 1), 16);
-  b += align_up(sizeof(float) * (B + 1), 16);
+  b += align_up(sizeof(uint4) * (B + 1), 16);
   b += align_up(sizeof(float) * D * K, 16);
   b += align_up(sizeof(int) * D * K, 16);
   b += align_up(sizeof(uint32_t) * 32 * W, 16);
@@ -106,8 +106,7 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   {
     size_t off = 0;
     sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
-    sm.sinfo = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * (B + 1), 16);
-    sm.spsc = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * (B + 1), 16);
+    sm.slot = reinterpret_cast<uint4*>(base + off); off += align_up(sizeof(uint4) * (B + 1), 16);
     sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
     sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
     sm.stage = reinterpret_cast<uint32_t*>(base + off);
@@ -115,13 +114,23 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   const float* lp_r = lp_g + (size_t)req * D * K;
   const int32_t* ids_r = ids_g + (size_t)req * D * K;
   for (int i = lane; i < D * K; i += 32) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
+  __syncwarp();
+  // log-probability at (depth d, 0-based rank i), 0 outside the table (the
+  // callers only use such values when the matching candidate does not exist)
+  auto lpat = [&](int d, int i) {
+    const bool in = d >= 1 && d <= D && i < K;
+    const float v = sm.lp[in ? (d - 1) * K + i : 0];   // index kept in range
+    return in ? v : 0.f;
+  };
   if (lane == 0) {
     sm.node[0] = static_cast<uint32_t>(root_tok[req]);
     sm.node[1] = 0xFFFFFFFFu;  // parent -1
     sm.node[2] = 0;
     sm.node[3] = 0;
-    sm.sinfo[0] = pack_info(0, 1, 1);
-    sm.spsc[0] = 0.f;
+    // slot 0: the root's children (depth 1), candidate rank 1
+    sm.slot[0] = make_uint4(pack_info(0, 1, 1), __float_as_uint(0.f),
+                            __float_as_uint(__fadd_rn(0.f, lpat(1, 1))),
+                            __float_as_uint(lpat(2, 0)));
   }
   __syncwarp();
 
@@ -137,23 +146,12 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     seq = 1;
   }
   uint64_t lbest = key[0];
-  // the scores that popping this lane's best candidate would create
-  float b_sib = 0.f, b_child = 0.f;
-  uint32_t b_info = 0;
-  auto precompute = [&]() {
-    const int slot = static_cast<int>((static_cast<uint32_t>(lbest) >> 5) & 63u) * 32 + lane;
-    const int sl = lbest != 0ull ? slot : 0;
-    b_info = sm.sinfo[sl];
-    const float psc = sm.spsc[sl];
-    const int d = (b_info >> 11) & 0x1F;
-    const int r = (b_info >> 16) & 0x3F;
-    const float score = from_ordered_bits(static_cast<uint32_t>(lbest >> 32));
-    const int is = (d - 1) * K + (r < K ? r : K - 1);
-    const int ic = (d < D ? d : D - 1) * K;
-    b_sib = __fadd_rn(psc, sm.lp[is > 0 ? is : 0]);
-    b_child = __fadd_rn(score, sm.lp[ic > 0 ? ic : 0]);
+  // record of this lane's best slot (loaded ahead of the reductions that may pick it)
+  auto load_rec = [&]() {
+    const int sl = static_cast<int>((static_cast<uint32_t>(lbest) >> 5) & 63u) * 32 + lane;
+    return sm.slot[lbest != 0ull ? sl : 0];
   };
-  precompute();
+  uint4 brec = load_rec();
   while (n < B) {
     const uint32_t hi = static_cast<uint32_t>(lbest >> 32);
     const uint32_t lo = static_cast<uint32_t>(lbest);
@@ -162,15 +160,19 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     if (mlo == 0u) break;  // no candidate left
     const int w = static_cast<int>(mlo & 31u);
     const int wi = static_cast<int>((mlo >> 5) & 63u);
-    const float s_sib = __shfl_sync(FULL, b_sib, w);
-    const float s_child = __shfl_sync(FULL, b_child, w);
-    const uint32_t winfo = __shfl_sync(FULL, b_info, w);
+    // the popped candidate: its slot record, from the winner lane
+    const uint32_t winfo = __shfl_sync(FULL, brec.x, w);
+    const float wpsc = __uint_as_float(__shfl_sync(FULL, brec.y, w));
+    const float s_sib = __uint_as_float(__shfl_sync(FULL, brec.z, w));
+    const float lp_child = __uint_as_float(__shfl_sync(FULL, brec.w, w));
+    const float wscore = from_ordered_bits(mhi);
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
     const int r = (winfo >> 16) & 0x3F;
     ++n;
     const bool has_sib = r < K;
     const bool has_child = d < D;
+    const float s_child = __fadd_rn(wscore, lp_child);
     const uint64_t sib_key = has_sib ? make_key(s_sib, seq, wi, w) : 0ull;
     seq += has_sib ? 1u : 0u;
     const int cslot = n_slots;
@@ -178,20 +180,22 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     const uint64_t child_key = has_child ? make_key(s_child, seq, ci, co) : 0ull;
     seq += has_child ? 1u : 0u;
     n_slots += has_child ? 1 : 0;
-    // records: the node (lane 0), the advanced slot (winner), the new slot (owner)
-    if (lane == 0) {
-      const uint4 rec = make_uint4(static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]),
-                                   static_cast<uint32_t>(p), static_cast<uint32_t>(d),
-                                   static_cast<uint32_t>(r));
-      *reinterpret_cast<uint4*>(sm.node + 4 * n) = rec;
-    }
+    // records: the node (lane 0); the advanced slot (winner): rank r+1, its next
+    // sibling at rank r+2; the new slot (owner): the popped node's children
+    const uint4 adv = make_uint4(pack_info(p, d, r + 1), __float_as_uint(wpsc),
+                                 __float_as_uint(__fadd_rn(wpsc, lpat(d, r + 1))),
+                                 __float_as_uint(lp_child));
+    const uint4 opn = make_uint4(pack_info(n, d + 1, 1), __float_as_uint(wscore),
+                                 __float_as_uint(__fadd_rn(wscore, lpat(d + 1, 1))),
+                                 __float_as_uint(lpat(d + 2, 0)));
     const bool is_w = lane == w;
     const bool is_o = has_child && lane == co;
-    if (is_w && has_sib) sm.sinfo[wi * 32 + w] = pack_info(p, d, r + 1);
-    if (is_o) {
-      sm.sinfo[cslot] = pack_info(n, d + 1, 1);
-      sm.spsc[cslot] = from_ordered_bits(mhi);
-    }
+    if (lane == 0)
+      *reinterpret_cast<uint4*>(sm.node + 4 * n) =
+          make_uint4(static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]),
+                     static_cast<uint32_t>(p), static_cast<uint32_t>(d), static_cast<uint32_t>(r));
+    if (is_w && has_sib) sm.slot[wi * 32 + w] = adv;
+    if (is_o) sm.slot[cslot] = opn;
 #pragma unroll
     for (int i = 0; i < NSL; ++i) {
       if (is_w && i == wi) key[i] = sib_key;
@@ -199,7 +203,7 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     }
     const uint64_t rescan = max_keys<NSL>(key);
     lbest = is_w ? rescan : (is_o ? umax64(lbest, child_key) : lbest);
-    if (is_w || is_o) precompute();
+    brec = load_rec();
   }
   __syncwarp();
 
