@@ -62,7 +62,8 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
     off = align_up(off + bytes, 256);
     return o;
   };
-  const int n_counters = 4096 > R ? 4096 : R;
+  int n_counters = 4096 > R ? 4096 : R;
+  if (n_counters < gemm_counter_ints()) n_counters = gemm_counter_ints();
   w.counters = take(sizeof(int) * n_counters);
   w.x = take(sizeof(float) * (size_t)R * d.d);
   w.xn = take(es * (size_t)R * d.d);
@@ -158,20 +159,34 @@ struct CallCtx {
   int* counters;
 };
 
-// One GEMM: acc = X . W^T with epilogue e.  X [M][K] (row stride ldx, elements).
-dflash_status gemm(const CallCtx& c, const CUtensorMap* tmW, const void* W, const void* X,
-                   long long ldx, int M, int N, int K, const EpiParams& e) {
+// One GEMM of a chain: acc = X . W^T with epilogue e.  X [M][K] (row stride
+// ldx, elements).
+struct Step {
+  const CUtensorMap* tmW;
+  const void* W;
+  const void* X;
+  long long ldx;
+  int N, K;
+  EpiParams e;
+};
+
+// A chain of dependent GEMMs over the same M activation rows: one launch on
+// the tensor-core path, one launch per GEMM on the fp32 path.
+dflash_status run_chain(const CallCtx& c, const Step* s, int n, int M) {
   if (M <= 0) return DFLASH_OK;
   if (c.m->bf16) {
-    const TcPlan pl = tc_plan(M, N, K, num_sms());
-    CUtensorMap tmX;
-    if (!encode_kmajor_map(&tmX, X, M, K, ldx, pl.n_tile))
-      return set_error(DFLASH_ERR_CUDA, "cannot encode the activation TMA descriptor");
-    return launch_gemm_tc(*tmW, tmX, pl, M, N, K, reinterpret_cast<float*>(c.ws + c.L.gpart),
-                          c.counters, c.status, e, c.st);
+    GemmPhase ph[kMaxPhases];
+    for (int i = 0; i < n; ++i) ph[i] = GemmPhase{s[i].tmW, s[i].X, s[i].ldx, s[i].N, s[i].K, s[i].e};
+    return launch_gemm_chain(ph, n, M, reinterpret_cast<float*>(c.ws + c.L.gpart), c.counters,
+                             c.status, c.st);
   }
-  return launch_gemm_f32(static_cast<const float*>(X), ldx, static_cast<const float*>(W), M, N,
-                         K, e, c.st);
+  for (int i = 0; i < n; ++i) {
+    const dflash_status st =
+        launch_gemm_f32(static_cast<const float*>(s[i].X), s[i].ldx,
+                        static_cast<const float*>(s[i].W), M, s[i].N, s[i].K, s[i].e, c.st);
+    if (st) return st;
+  }
+  return DFLASH_OK;
 }
 
 }  // namespace
@@ -269,9 +284,6 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
   e1.ssq_in = nullptr;
   e1.out = f;
   e1.ldo = d.d;
-  st = gemm(c, &model->tm_proj, model->w.w_proj, feats, (long long)d.n_feat * d.d_feat, n_rows,
-            d.d, d.n_feat * d.d_feat, e1);
-  if (st) return st;
   // a2: [K|V] of every layer = f . U^T, K rotated, scattered into the cache
   EpiParams e2 = epi_base(*model, n_rows, d.n_layers * 2 * d.n_kv * d.head_dim);
   e2.kind = EPI_KV;
@@ -286,8 +298,11 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
   e2.n_req = n_req;
   e2.row_off = row_off;
   e2.pos0 = pos0;
-  return gemm(c, &model->tm_ukv, model->w.u_kv, f, d.d, n_rows,
-              d.n_layers * 2 * d.n_kv * d.head_dim, d.d, e2);
+  const Step chain[2] = {
+      {&model->tm_proj, model->w.w_proj, feats, (long long)d.n_feat * d.d_feat, d.d,
+       d.n_feat * d.d_feat, e1},
+      {&model->tm_ukv, model->w.u_kv, f, d.d, d.n_layers * 2 * d.n_kv * d.head_dim, d.d, e2}};
+  return run_chain(c, chain, 2, n_rows);
 }
 
 dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache, int n_req,
@@ -343,8 +358,10 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     n_chunks = (max_ctx + chunk - 1) / chunk;
   }
 
-  for (int l = 0; l < d.n_layers; ++l) {
-    // Q, K, V of the block rows
+  // GEMM steps of the pass.  A chain runs the dependent GEMMs between two
+  // attention calls in one launch: [QKV_0], attention_0, [O_0, gate/up_0,
+  // down_0, QKV_1], attention_1, ..., [O_n-1, gate/up_n-1, down_n-1, LM head].
+  auto qkv_step = [&](int l) {
     EpiParams eq = epi_base(*model, R, qkv_dim);
     eq.kind = EPI_QKV;
     eq.ssq_in = ssq;
@@ -352,8 +369,22 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     eq.ldo = qkv_dim;
     eq.rope = rope;
     eq.rope_cols = (d.n_q + d.n_kv) * hd;
-    st = gemm(c, &model->tm_qkv[l], model->w.w_qkv[l], xn, d.d, R, qkv_dim, d.d, eq);
+    return Step{&model->tm_qkv[l], model->w.w_qkv[l], xn, d.d, qkv_dim, d.d, eq};
+  };
+  auto lm_step = [&]() {
+    EpiParams el = epi_base(*model, R, d.vocab);
+    el.kind = EPI_LOGITS;
+    el.ssq_in = ssq;
+    el.logits = lg;
+    el.L = L;
+    return Step{&model->tm_lm, model->w.lm_head, xn, d.d, d.vocab, d.d, el};
+  };
+  {
+    const Step first = qkv_step(0);
+    st = run_chain(c, &first, 1, R);
     if (st) return st;
+  }
+  for (int l = 0; l < d.n_layers; ++l) {
     // attention over [context ; block]
     if (model->bf16) {
       AttnParams ap{};
@@ -403,16 +434,12 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     eo.xn = xn;
     eo.gain = model->w.mlp_norm[l];
     eo.ssq_out = ssq;
-    st = gemm(c, &model->tm_o[l], model->w.wo[l], ao, qd, R, d.d, qd, eo);
-    if (st) return st;
     // h = silu(g) * u
     EpiParams eg = epi_base(*model, R, 2 * d.d_ff);
     eg.kind = EPI_SWIGLU;
     eg.ssq_in = ssq;
     eg.out = hbuf;
     eg.ldo = d.d_ff;
-    st = gemm(c, &model->tm_gu[l], model->w.w_gate_up[l], xn, d.d, R, 2 * d.d_ff, d.d, eg);
-    if (st) return st;
     // x += h . W_down^T ; xn = x * g_next
     EpiParams ed = epi_base(*model, R, d.d);
     ed.kind = EPI_RESID;
@@ -421,17 +448,16 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     ed.xn = xn;
     ed.gain = (l + 1 < d.n_layers) ? model->w.attn_norm[l + 1] : model->w.final_norm;
     ed.ssq_out = ssq;
-    st = gemm(c, &model->tm_down[l], model->w.w_down[l], hbuf, d.d_ff, R, d.d, d.d_ff, ed);
+    // then the next layer's Q, K, V, or the LM head on the mask rows
+    const Step chain[4] = {
+        {&model->tm_o[l], model->w.wo[l], ao, qd, d.d, qd, eo},
+        {&model->tm_gu[l], model->w.w_gate_up[l], xn, d.d, 2 * d.d_ff, d.d, eg},
+        {&model->tm_down[l], model->w.w_down[l], hbuf, d.d_ff, d.d, d.d_ff, ed},
+        (l + 1 < d.n_layers) ? qkv_step(l + 1) : lm_step()};
+    st = run_chain(c, chain, 4, R);
     if (st) return st;
   }
-  // LM head on the mask rows, then log-softmax + top-K
-  EpiParams el = epi_base(*model, R, d.vocab);
-  el.kind = EPI_LOGITS;
-  el.ssq_in = ssq;
-  el.logits = lg;
-  el.L = L;
-  st = gemm(c, &model->tm_lm, model->w.lm_head, xn, d.d, R, d.vocab, d.d, el);
-  if (st) return st;
+  // log-softmax + top-K
   TopkLaunch tk{};
   tk.logits = lg;
   tk.rows = n_req * D;
@@ -451,7 +477,7 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
 size_t dflash_linear_workspace_bytes(int M, int N, int K) {
   if (M < 0 || N <= 0 || K <= 0 || K % 64 || N % 128) return 0;
   const TcPlan pl = tc_plan(M > 0 ? M : 1, N, K, num_sms());
-  const int n_counters = pl.grid > 4096 ? pl.grid : 4096;
+  const int n_counters = gemm_counter_ints() > 4096 ? gemm_counter_ints() : 4096;
   return 256 + align_up(sizeof(int) * n_counters, 256) + align_up(pl.part_bytes, 256);
 }
 
@@ -466,9 +492,8 @@ dflash_status dflash_linear_bf16(int M, int N, int K, const void* X, const void*
   if (!ws || ws_bytes < need)
     return set_error(DFLASH_ERR_WORKSPACE, "linear workspace needs %zu bytes, got %zu", need,
                      ws_bytes);
-  const TcPlan pl = tc_plan(M, N, K, num_sms());
-  CUtensorMap tmW, tmX;
-  if (!encode_kmajor_map(&tmW, W, N, K, K, 128) || !encode_kmajor_map(&tmX, X, M, K, K, pl.n_tile))
+  CUtensorMap tmW;
+  if (!encode_kmajor_map(&tmW, W, N, K, K, 128))
     return set_error(DFLASH_ERR_CUDA, "cannot encode TMA descriptors");
   EpiParams e{};
   e.kind = EPI_STORE_F32;
@@ -477,11 +502,12 @@ dflash_status dflash_linear_bf16(int M, int N, int K, const void* X, const void*
   e.logits = Y;
   e.ldo = N;
   char* w = static_cast<char*>(ws);
-  const int n_counters = pl.grid > 4096 ? pl.grid : 4096;
+  const int n_counters = gemm_counter_ints() > 4096 ? gemm_counter_ints() : 4096;
   int* counters = reinterpret_cast<int*>(w + 256);
   float* part = reinterpret_cast<float*>(w + 256 + align_up(sizeof(int) * n_counters, 256));
-  return launch_gemm_tc(tmW, tmX, pl, M, N, K, part, counters, static_cast<int*>(ws), e,
-                        static_cast<cudaStream_t>(stream));
+  const GemmPhase ph{&tmW, X, K, N, K, e};
+  return launch_gemm_chain(&ph, 1, M, part, counters, static_cast<int*>(ws),
+                           static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
