@@ -11,9 +11,10 @@
 // (tile, 64-wide K block) pairs; the grid is one CTA per SM and CTA c owns the
 // contiguous unit range [c*U/G, (c+1)*U/G) (stream-K), so every SM streams the
 // same number of weight bytes whatever the matrix shape.  A tile whose K range
-// is split over several CTAs is reduced by the last CTA to arrive (an atomic
-// counter; no CTA ever waits for another), adding the partial sums in a fixed
-// order so results do not depend on timing.
+// is split over several CTAs is finished by the CTA holding its first K blocks
+// (they end that CTA's range, so it is among the last to get there): the
+// others post fp32 partial sums and a release-add on the tile's counter, and
+// it adds them, in a fixed order, to its own accumulator.
 //
 // Chains.  One launch runs up to kMaxPhases dependent GEMMs ("phases", e.g.
 // W_o -> W_gate|up -> W_down -> next layer's W_qkv), each GEMM's activations
@@ -319,9 +320,18 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           break;
         }
       }
+      // With one row tile, the RMS row scales of the phase are computed once,
+      // ahead of its first accumulator.
+      const bool scales_once = P.n_rtiles == 1;
+      if (scales_once) {
+        epi_row_scales(E, 0, min(p.n_tile, E.M_rows), s_scale, etid, kEpiThreads);
+        ptx::named_bar_sync(1, kEpiThreads);
+      }
       while (u < u_end) {
         const int acc = tile_i & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                              static_cast<uint32_t>(acc * p.n_tile);
         const int t = static_cast<int>(u / KB);
         const int kb0 = static_cast<int>(u - (long long)t * KB);
         const int n = static_cast<int>((KB - kb0) < (u_end - u) ? (KB - kb0) : (u_end - u));
@@ -332,7 +342,13 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int c_first = cta_of_unit((long long)t * KB, U, Gk);
         const int c_last = cta_of_unit((long long)t * KB + KB - 1, U, Gk);
         const int nslots = c_last - c_first + 1;
+        // A tile split over several CTAs is finished by c_first: the tile's
+        // first K blocks close c_first's unit range, so it is among the last to
+        // finish its share.  The others post partial sums (slot c - c_first)
+        // and a release-add; c_first adds them, in slot order, to its own
+        // accumulator read straight from TMEM.
         const bool single = nslots == 1;
+        const bool reducer = !single && c == c_first;
 
         const bool ok = ptx::mbar_wait_bounded(&accf[acc], acc_phase, kTimeoutNs, flags);
         if (!ok) {
@@ -345,81 +361,66 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         ptx::tc_fence_after();
 
-        if (single) {
-          epi_row_scales(E, row0, nrows, s_scale, etid, kEpiThreads);
-          for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
-        }
-        float* my_part = p.part + ((size_t)c_first * P.max_slots + (c - c_first)) *
-                                      (size_t)p.n_tile * kTileN;
-        for (int c0 = 0; c0 < nrows; c0 += kChunk) {
-          float v[16];
-          __syncwarp();
-          ptx::tmem_ld_32x16(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                                 static_cast<uint32_t>(acc * p.n_tile + c0), v);
-          if (single) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) buf[j * kBufLd + f] = v[j];
-            ptx::named_bar_sync(1, kEpiThreads);
-            epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, min(kChunk, nrows - c0), f,
-                               s_scale, row0, s_red, p.n_tile, ew);
-            ptx::named_bar_sync(1, kEpiThreads);
-          } else {
+        if (!single && !reducer) {
+          float* my_part = p.part + ((size_t)c_first * P.max_slots + (c - c_first)) *
+                                        (size_t)p.n_tile * kTileN;
+          for (int c0 = 0; c0 < nrows; c0 += kChunk) {
+            float v[16];
+            __syncwarp();
+            ptx::tmem_ld_32x16(tacc + static_cast<uint32_t>(c0), v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kTileN + f] = v[j];
           }
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&acce[acc]);
-
-        if (single) {
-          if (E.kind == EPI_RESID) {
-            ptx::named_bar_sync(1, kEpiThreads);
-            epi_resid_flush(E, ftile, row0, nrows, s_red, p.n_tile, 4, etid, kEpiThreads);
-          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&acce[acc]);
+          ptx::named_bar_sync(1, kEpiThreads);
+          if (etid == 0) red_release_add(&P.counters[c_first], 1);
         } else {
-          __threadfence();
-          ptx::named_bar_sync(1, kEpiThreads);
-          if (etid == 0) {
-            const int prev = atomicAdd(&P.counters[c_first], 1);
-            flags[1] = (prev == nslots - 1) ? 1 : 0;
+          if (!scales_once) epi_row_scales(E, row0, nrows, s_scale, etid, kEpiThreads);
+          for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
+          if (reducer) {
+            bool got = true;
+            if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
+            if (ptx::named_bar_or(1, kEpiThreads, !got)) {
+              record_status(p.status, DFLASH_ERR_TIMEOUT);
+              flags[0] = 1;
+              stop = true;
+              break;
+            }
           }
-          ptx::named_bar_sync(1, kEpiThreads);
-          if (flags[1]) {
-            __threadfence();
-            epi_row_scales(E, row0, nrows, s_scale, etid, kEpiThreads);
-            for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
-            const float* slots = p.part + (size_t)c_first * P.max_slots * p.n_tile * kTileN;
-            for (int c0 = 0; c0 < nrows; c0 += kChunk) {
-              const int nr = min(kChunk, nrows - c0);
-              // fixed slot order; four slots' loads (16 rows each) are in flight together
-              float sum[kChunk];
+          const float* slots = p.part + (size_t)c_first * P.max_slots * p.n_tile * kTileN;
+          for (int c0 = 0; c0 < nrows; c0 += kChunk) {
+            const int nr = min(kChunk, nrows - c0);
+            float sum[kChunk];
+            __syncwarp();
+            ptx::tmem_ld_32x16(tacc + static_cast<uint32_t>(c0), sum);
+            // slots 1.. in order; four slots' loads (16 rows each) in flight together
+            for (int s0 = 1; s0 < nslots; s0 += 4) {
+              float v[4][kChunk];
 #pragma unroll
-              for (int j = 0; j < kChunk; ++j) sum[j] = 0.f;
-              for (int s0 = 0; s0 < nslots; s0 += 4) {
-                float v[4][kChunk];
+              for (int q = 0; q < 4; ++q) {
+                const float* src = slots + ((size_t)(s0 + q) * p.n_tile + c0) * kTileN + f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const float* src = slots + ((size_t)(s0 + q) * p.n_tile + c0) * kTileN + f;
-#pragma unroll
-                  for (int j = 0; j < kChunk; ++j)
-                    v[q][j] = (s0 + q < nslots && j < nr) ? __ldcg(src + (size_t)j * kTileN) : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < kChunk; ++j) sum[j] += v[q][j];
+                for (int j = 0; j < kChunk; ++j)
+                  v[q][j] = (s0 + q < nslots && j < nr) ? __ldcg(src + (size_t)j * kTileN) : 0.f;
               }
 #pragma unroll
-              for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = sum[j];
-              ptx::named_bar_sync(1, kEpiThreads);
-              epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
-                                 p.n_tile, ew);
-              ptx::named_bar_sync(1, kEpiThreads);
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < kChunk; ++j) sum[j] += v[q][j];
             }
-            if (E.kind == EPI_RESID)
-              epi_resid_flush(E, ftile, row0, nrows, s_red, p.n_tile, 4, etid, kEpiThreads);
-            if (etid == 0) P.counters[c_first] = 0;
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = sum[j];
+            ptx::named_bar_sync(1, kEpiThreads);
+            epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
+                               p.n_tile, ew);
+            ptx::named_bar_sync(1, kEpiThreads);
           }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&acce[acc]);
+          if (E.kind == EPI_RESID)
+            epi_resid_flush(E, ftile, row0, nrows, s_red, p.n_tile, 4, etid, kEpiThreads);
+          if (reducer && etid == 0) P.counters[c_first] = 0;   // for the next launch
           ptx::named_bar_sync(1, kEpiThreads);
         }
         ++tile_i;
