@@ -358,7 +358,7 @@ def run_reference(args, rank, world):
     times = []
     t_start = time.perf_counter()
     steps_done = 0
-    warm = min(args.warmup, 1)
+    warm = max(args.warmup, 3)
     for i in range(warm + args.steps):
         b = cpu_baseline(cyc, args.cpu_budget_s)
         if i >= warm:
