@@ -40,7 +40,8 @@ size_t esize(const dflash_dims& d) { return d.dtype == DFLASH_BF16 ? 2 : 4; }
 
 // Workspace regions of a model-sized workspace (byte offsets).
 struct WsLayout {
-  size_t counters, x, xn, ssq, qkv, attn_o, h, logits, gpart, apart_o, apart_ml, tpart, rope_blk,
+  size_t counters, x, xn, ssq, qkv, attn_o, h, logits, gpart, apart_o, apart_ml, tpart, tkpart,
+      rope_blk,
       f, rope_inj, total;
   int attn_chunks_cap;
 };
@@ -103,6 +104,8 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
   w.apart_o = take(m.bf16 ? sizeof(float) * arows * d.head_dim : 0);
   w.apart_ml = take(m.bf16 ? sizeof(float) * arows * 2 : 0);
   w.tpart = take(topk_part_bytes(n_req * D, 32));
+  // records of the top-K fused into the LM head (batch-1 row tile)
+  w.tkpart = take(m.bf16 && tc_row_tile(R) == 16 ? sizeof(float) * sms * R * kTkStride : 0);
   w.rope_blk = take(sizeof(float2) * (size_t)R * (d.head_dim / 2));
   w.f = take(es * (size_t)max_inject_rows * d.d);
   w.rope_inj = take(sizeof(float2) * (size_t)max_inject_rows * (d.head_dim / 2));
@@ -371,12 +374,18 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     eq.rope_cols = (d.n_q + d.n_kv) * hd;
     return Step{&model->tm_qkv[l], model->w.w_qkv[l], xn, d.d, qkv_dim, d.d, eq};
   };
+  // With one 16-row tile the log-softmax / top-K rides in the LM head's
+  // epilogue (per-CTA records, merged by a small kernel); the logits are then
+  // stored only if the caller asked for them.
+  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16;
   auto lm_step = [&]() {
     EpiParams el = epi_base(*model, R, d.vocab);
     el.kind = EPI_LOGITS;
     el.ssq_in = ssq;
-    el.logits = lg;
+    el.logits = fused_topk ? logits : lg;
     el.L = L;
+    el.tk_part = fused_topk ? reinterpret_cast<float*>(c.ws + W.tkpart) : nullptr;
+    el.tk_K = K;
     return Step{&model->tm_lm, model->w.lm_head, xn, d.d, d.vocab, d.d, el};
   };
   {
@@ -458,6 +467,11 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     if (st) return st;
   }
   // log-softmax + top-K
+  if (fused_topk) {
+    launch_topk_merge(reinterpret_cast<const float*>(c.ws + W.tkpart), num_sms(), n_req * D, K,
+                      topk_ids, topk_logp, c.st);
+    return check_launch("top-K merge");
+  }
   TopkLaunch tk{};
   tk.logits = lg;
   tk.rows = n_req * D;

@@ -15,7 +15,10 @@
 //           scaled by s(row)                                       (W_gate|W_up)
 //   KV      columns [layer][K|V][n_kv*hd]: K rotated at the row's cache
 //           position, written to that layer's cache slot           (U_K|U_V)
-//   LOGITS  logits[req][j-1][col] = acc * s(row) for block rows j >= 1 (LM head)
+//   LOGITS  logits[req][j-1][col] = acc * s(row) for block rows j >= 1 (LM head);
+//           logits == nullptr skips the store.  With tk_part set the GEMM also
+//           folds every value into a running top-K and log-sum-exp per row and
+//           publishes one record per CTA and row (gemm_tc.cu)
 //   STORE_F32  logits[row][col] = acc (fp32, plain dense product)
 //
 // s(row) = rsqrt(sum of the row's per-tile x^2 partials / d + eps) is the
@@ -73,7 +76,14 @@ struct EpiParams {
   // LOGITS
   float* logits;
   int L;
+  // fused top-K of the logits rows: per-CTA records [grid][n_req*(L-1)][kTkStride]
+  float* tk_part;
+  int tk_K;
 };
+
+// Record of a fused top-K: max, sum of exp(x - max), K values (desc), K ids.
+constexpr int kTkMax = 32;
+constexpr int kTkStride = 2 + 2 * kTkMax;
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
@@ -261,7 +271,7 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
         const int row = crow0 + r;
         const int rq = row / e.L;
         const int j = row - rq * e.L;
-        if (r < nrows && j >= 1 && cvalid)
+        if (r < nrows && j >= 1 && cvalid && e.logits)
           e.logits[((size_t)rq * (e.L - 1) + (j - 1)) * e.N_feat + col] =
               a[r] * s_scale[row - srow0];
       }

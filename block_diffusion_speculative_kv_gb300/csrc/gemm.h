@@ -20,7 +20,7 @@ struct TcPlan {
 };
 
 int tc_row_tile(int M_rows);
-TcPlan tc_plan(int M_rows, int N_feat, int K, int grid);
+TcPlan tc_plan(int M_rows, int N_feat, int K, int grid, int tk_kpad = 0);
 
 // 2-D TMA map of a K-major bf16 matrix [rows][K] (row stride in elements),
 // box = 64 x box_rows, 128-byte swizzle.  False if the driver entry point is

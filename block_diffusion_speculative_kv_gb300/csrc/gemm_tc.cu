@@ -39,6 +39,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <math_constants.h>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "gemm.h"
@@ -64,6 +66,7 @@ struct TcPhase {
 
 struct TcParams {
   int M_rows, n_tile, stages, n_phases;
+  int tk_kpad;     // list length of a fused top-K (0: none in this chain)
   float* part;     // split-tile partial sums [grid][max_slots][n_tile][128]
   int* sync;       // [kMaxPhases] phase-done counters, then the exit counter
   int* status;
@@ -80,10 +83,16 @@ __host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, in
 }
 
 struct SmemLayout {
-  uint32_t a_off, b_off, bar_off, buf_off, scale_off, red_off, total;
+  uint32_t a_off, b_off, bar_off, buf_off, scale_off, red_off, tk_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile) {
+// Fused top-K state: per epilogue warp and tile row, max, sum of exp and a
+// sorted list of kpad (value, id) pairs.
+__host__ __device__ inline uint32_t tk_state_floats(int n_tile, int kpad) {
+  return kpad ? static_cast<uint32_t>(4 * n_tile * (2 + 2 * kpad)) : 0u;
+}
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile, int tk_kpad = 0) {
   SmemLayout L;
   const uint32_t b_bytes = n_tile * 128;
   L.a_off = 0;
@@ -93,7 +102,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile) {
   L.buf_off = (L.bar_off + bar_bytes + 15) / 16 * 16;
   L.scale_off = L.buf_off + kChunk * kBufLd * 4;
   L.red_off = L.scale_off + n_tile * 4;
-  L.total = L.red_off + 4 * n_tile * 4 + 1024;  // + alignment slack for the 1024-B base
+  L.tk_off = L.red_off + 4 * n_tile * 4;
+  L.total = L.tk_off + tk_state_floats(n_tile, tk_kpad) * 4 + 1024;  // + slack for the 1024-B base
   return L;
 }
 
@@ -119,13 +129,168 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, const vol
   }
 }
 
+__device__ __forceinline__ bool tk_better(float v, int i, float ov, int oi) {
+  return v > ov || (v == ov && i < oi);
+}
+
+// Sort the warp's 32 (value, id) pairs into lanes 0..31 by (value desc, id asc)
+// (bitonic network over shuffles).
+__device__ __forceinline__ void warp_sort_desc(float& v, int& id, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, j);
+      const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
+      if (keep_better == tk_better(ov, oi, v, id)) { v = ov; id = oi; }
+    }
+  }
+}
+
+// Fold one epilogue chunk of LM-head values (rows c0.. of the tile, this
+// thread's column col) into warp ew's per-row state: online max / sum of exp,
+// and the sorted list (value desc, id asc).  A CTA meets its tiles in column
+// order, so a value equal to the K-th kept one never displaces it.  Warp-
+// uniform; K <= kpad <= 32.
+__device__ __forceinline__ void tk_update(const EpiParams& E, float* tk, int kpad, int n_tile,
+                                          const float* buf, const float* s_scale, int c0, int nr,
+                                          int f, int col, bool cvalid, int ew, int lane) {
+  const unsigned FULL = 0xffffffffu;
+  const int K = E.tk_K;
+  const int stride = 2 + 2 * kpad;
+  for (int j = 0; j < nr; ++j) {
+    const int row = c0 + j;
+    if (row % E.L == 0) continue;   // anchor rows have no logits
+    float* st = tk + (ew * n_tile + row) * stride;
+    const float v = cvalid ? buf[j * kBufLd + f] * s_scale[row] : -CUDART_INF_F;
+    const float mx = from_ordered_bits(__reduce_max_sync(FULL, ordered_bits(v)));
+    const float m_old = st[0], s_old = st[1];
+    const float M = fmaxf(m_old, mx);
+    float e = (v == -CUDART_INF_F) ? 0.f : exp2f((v - M) * 1.4426950408889634f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(FULL, e, off);
+    __syncwarp();
+    if (lane == 0 && M != -CUDART_INF_F) {
+      st[0] = M;
+      st[1] = (m_old == -CUDART_INF_F ? 0.f : s_old * exp2f((m_old - M) * 1.4426950408889634f)) + e;
+    }
+    const float thr = st[2 + K - 1];
+    unsigned cand = __ballot_sync(FULL, v > thr);
+    if (__popc(cand) > 2 && K <= 16) {
+      // many candidates (a warp's first tiles): sort them, then sort the list
+      // together with the best 32-K of them; with K <= 16 those hold the top K
+      float sv = v > thr ? v : -CUDART_INF_F;
+      int si = v > thr ? col : 0x7fffffff;
+      warp_sort_desc(sv, si, lane);
+      const float cv = __shfl_sync(FULL, sv, lane >= K ? lane - K : 0);
+      const int ci = __shfl_sync(FULL, si, lane >= K ? lane - K : 0);
+      float uv = lane < K ? st[2 + lane] : cv;
+      int ui = lane < K ? __float_as_int(st[2 + kpad + lane]) : ci;
+      warp_sort_desc(uv, ui, lane);
+      __syncwarp();
+      if (lane < K) {
+        st[2 + lane] = uv;
+        st[2 + kpad + lane] = __int_as_float(ui);
+      }
+      cand = 0;
+    }
+    while (cand) {
+      const int b = __ffs(cand) - 1;
+      cand &= cand - 1;
+      const float bv = __shfl_sync(FULL, v, b);
+      const int bi = __shfl_sync(FULL, col, b);
+      const float ev = lane < K ? st[2 + lane] : -CUDART_INF_F;
+      const int ei = lane < K ? __float_as_int(st[2 + kpad + lane]) : 0x7fffffff;
+      const unsigned ahead = __ballot_sync(FULL, lane < K && tk_better(ev, ei, bv, bi));
+      const int pos = __popc(ahead);
+      const float pv = __shfl_up_sync(FULL, ev, 1);
+      const int pi = __shfl_up_sync(FULL, ei, 1);
+      __syncwarp();
+      if (pos < K) {
+        if (lane < K && lane > pos) {
+          st[2 + lane] = pv;
+          st[2 + kpad + lane] = __int_as_float(pi);
+        }
+        if (lane == pos) {
+          st[2 + lane] = bv;
+          st[2 + kpad + lane] = __int_as_float(bi);
+        }
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+  }
+}
+
+// The same fold for K <= 8 with one lane per tile row: lane j walks the warp's
+// 32 columns of chunk row j in column order with its state in registers (one
+// exp per value, a register insert only when the value beats the K-th kept).
+__device__ __forceinline__ void tk_update_rows(const EpiParams& E, float* tk, int kpad, int n_tile,
+                                               const float* buf, const float* s_scale, int c0,
+                                               int nr, int col0, int ew, int lane) {
+  constexpr int KM = 8;
+  const int K = E.tk_K;
+  const int row = c0 + lane;
+  if (lane >= nr || row % E.L == 0) return;
+  float* st = tk + (ew * n_tile + row) * (2 + 2 * kpad);
+  float m = st[0], sum = st[1];
+  float tv[KM];
+  int ti[KM];
+#pragma unroll
+  for (int q = 0; q < KM; ++q) {
+    tv[q] = q < K ? st[2 + q] : -CUDART_INF_F;
+    ti[q] = q < K ? __float_as_int(st[2 + kpad + q]) : 0x7fffffff;
+  }
+  float thr = tv[0];
+#pragma unroll
+  for (int q = 0; q < KM; ++q)
+    if (q == K - 1) thr = tv[q];
+  const float sc = s_scale[row];
+  const float* src = buf + lane * kBufLd + ew * 32;
+  const int ncol = min(32, E.N_feat - (col0 + ew * 32));
+  for (int q = 0; q < ncol; ++q) {
+    const float v = src[q] * sc;
+    if (v > m) {
+      sum = (m == -CUDART_INF_F ? 0.f : sum * exp2f((m - v) * 1.4426950408889634f)) + 1.f;
+      m = v;
+    } else {
+      sum += exp2f((v - m) * 1.4426950408889634f);
+    }
+    if (v > thr) {
+      // sorted insert (value desc; an equal value stays ahead: it came first)
+      const int id = col0 + ew * 32 + q;
+#pragma unroll
+      for (int j = KM - 1; j >= 0; --j) {
+        if (j < K) {
+          const float pv = j > 0 ? tv[j > 0 ? j - 1 : 0] : CUDART_INF_F;
+          const int pi = j > 0 ? ti[j > 0 ? j - 1 : 0] : 0;
+          if (v > pv) { tv[j] = pv; ti[j] = pi; }
+          else if (v > tv[j]) { tv[j] = v; ti[j] = id; }
+        }
+      }
+#pragma unroll
+      for (int q2 = 0; q2 < KM; ++q2)
+        if (q2 == K - 1) thr = tv[q2];
+    }
+  }
+  st[0] = m;
+  st[1] = sum;
+#pragma unroll
+  for (int q = 0; q < KM; ++q)
+    if (q < K) {
+      st[2 + q] = tv[q];
+      st[2 + kpad + q] = __int_as_float(ti[q]);
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout SL = smem_layout(p.stages, p.n_tile);
+  const SmemLayout SL = smem_layout(p.stages, p.n_tile, p.tk_kpad);
   const uint32_t b_bytes = p.n_tile * 128;
   uint8_t* sA = smem + SL.a_off;
   uint8_t* sB = smem + SL.b_off;
@@ -139,6 +304,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   float* buf = reinterpret_cast<float*>(smem + SL.buf_off);
   float* s_scale = reinterpret_cast<float*>(smem + SL.scale_off);
   float* s_red = reinterpret_cast<float*>(smem + SL.red_off);
+  float* tk = reinterpret_cast<float*>(smem + SL.tk_off);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -327,6 +493,18 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         epi_row_scales(E, 0, min(p.n_tile, E.M_rows), s_scale, etid, kEpiThreads);
         ptx::named_bar_sync(1, kEpiThreads);
       }
+      // fused top-K (one row tile only): empty per-warp state
+      const bool fused_tk = E.kind == EPI_LOGITS && E.tk_part != nullptr && p.tk_kpad > 0;
+      const int tk_stride = 2 + 2 * p.tk_kpad;
+      if (fused_tk) {
+        for (int i = etid; i < 4 * p.n_tile * tk_stride; i += kEpiThreads) {
+          const int q = i % tk_stride;
+          tk[i] = q == 0 ? -CUDART_INF_F
+                : q == 1 ? 0.f
+                : q < 2 + p.tk_kpad ? -CUDART_INF_F : __int_as_float(0x7fffffff);
+        }
+        ptx::named_bar_sync(1, kEpiThreads);
+      }
       while (u < u_end) {
         const int acc = tile_i & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
@@ -414,6 +592,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             ptx::named_bar_sync(1, kEpiThreads);
             epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                p.n_tile, ew);
+            if (fused_tk) {
+              if (E.tk_K <= 8)
+                tk_update_rows(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, ftile * kTileN,
+                               ew, lane);
+              else
+                tk_update(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, f, ftile * kTileN + f,
+                          ftile * kTileN + f < E.N_feat, ew, lane);
+              __syncwarp();
+            }
             ptx::named_bar_sync(1, kEpiThreads);
           }
           ptx::tc_fence_before();
@@ -427,6 +614,52 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         u += n;
       }
       if (stop) break;
+      if (fused_tk) {
+        // this CTA's record of every mask row: merge the four warps' states
+        ptx::named_bar_sync(1, kEpiThreads);
+        const int K = E.tk_K;
+        const int n_out = E.M_rows / E.L * (E.L - 1);
+        for (int row = ew; row < min(p.n_tile, E.M_rows); row += 4) {
+          if (row % E.L == 0) continue;
+          const int orow = row / E.L * (E.L - 1) + row % E.L - 1;
+          float* rec = E.tk_part + ((size_t)c * n_out + orow) * kTkStride;
+          const float* st = tk + ((lane & 3) * p.n_tile + row) * tk_stride;
+          float m = lane < 4 ? st[0] : -CUDART_INF_F;
+          float sm = lane < 4 ? st[1] : 0.f;
+#pragma unroll
+          for (int off = 1; off < 4; off <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, sm, off);
+            const float M = fmaxf(m, m2);
+            sm = (M == -CUDART_INF_F) ? 0.f
+                 : (m == -CUDART_INF_F ? 0.f : sm * exp2f((m - M) * 1.4426950408889634f)) +
+                       (m2 == -CUDART_INF_F ? 0.f : s2 * exp2f((m2 - M) * 1.4426950408889634f));
+            m = M;
+          }
+          int ptr = 0;   // lanes 0-3: next entry of warp (lane)'s list
+          for (int r = 0; r < K; ++r) {
+            float bv = (lane < 4 && ptr < K) ? st[2 + ptr] : -CUDART_INF_F;
+            int bi = (lane < 4 && ptr < K) ? __float_as_int(st[2 + p.tk_kpad + ptr]) : 0x7fffffff;
+            const float ov = bv;
+            const int oi = bi;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+              const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+              const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+              if (tk_better(v2, i2, bv, bi)) { bv = v2; bi = i2; }
+            }
+            if (lane < 4 && ptr < K && ov == bv && oi == bi) ++ptr;
+            if (lane == 0) {
+              rec[2 + r] = bv;
+              rec[2 + kTkMax + r] = __int_as_float(bi);
+            }
+          }
+          if (lane == 0) {
+            rec[0] = m;
+            rec[1] = sm;
+          }
+        }
+      }
       // this CTA's share of phase k is written: publish it
       ptx::named_bar_sync(1, kEpiThreads);
       if (etid == 0) red_release_add(&p.sync[k], 1);
@@ -507,7 +740,7 @@ int tc_row_tile(int M_rows) {
   return n;
 }
 
-TcPlan tc_plan(int M_rows, int N_feat, int K, int grid) {
+TcPlan tc_plan(int M_rows, int N_feat, int K, int grid, int tk_kpad) {
   TcPlan pl{};
   pl.n_tile = tc_row_tile(M_rows);
   pl.n_rtiles = ceil_div(M_rows, pl.n_tile);
@@ -528,9 +761,9 @@ TcPlan tc_plan(int M_rows, int N_feat, int K, int grid) {
   // the deepest ring that fits: it also carries the weight stream across the
   // hand-over between the phases of a chain
   int stages = 1;
-  while (stages < 24 && smem_layout(stages + 1, pl.n_tile).total <= 227u * 1024u) ++stages;
+  while (stages < 24 && smem_layout(stages + 1, pl.n_tile, tk_kpad).total <= 227u * 1024u) ++stages;
   pl.stages = stages;
-  pl.smem_bytes = smem_layout(stages, pl.n_tile).total;
+  pl.smem_bytes = smem_layout(stages, pl.n_tile, tk_kpad).total;
   return pl;
 }
 
@@ -548,11 +781,16 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
   p.sync = counters + kMaxPhases * G;
   p.status = status;
   int smem = 0;
+  for (int k = 0; k < n_phases; ++k)
+    if (ph[k].epi.kind == EPI_LOGITS && ph[k].epi.tk_part != nullptr)
+      p.tk_kpad = (ph[k].epi.tk_K + 7) / 8 * 8;
   for (int k = 0; k < n_phases; ++k) {
-    const TcPlan pl = tc_plan(M_rows, ph[k].N, ph[k].K, G);
+    const TcPlan pl = tc_plan(M_rows, ph[k].N, ph[k].K, G, p.tk_kpad);
     p.n_tile = pl.n_tile;
     p.stages = pl.stages;
     smem = pl.smem_bytes;
+    if (p.tk_kpad && pl.n_rtiles != 1)
+      return set_error(DFLASH_ERR_UNSUPPORTED, "fused top-K needs one row tile");
     TcPhase& P = p.ph[k];
     P.N_feat = ph[k].N;
     P.K = ph[k].K;
