@@ -122,15 +122,16 @@ def _check_logits_topk(ref_logits, gpu_logits, gpu_ids, gpu_lp, K, tolerance):
         assert np.all(np.diff(gpu_lp[r]) <= 0)
 
 
-def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None):
+def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None, K=None):
     wl = WORKLOADS[wid]
     s = wl.shape
+    K = wl.K if K is None else K
     w = synth.drafter_weights(s, wl.seed, device=DEV)
     if gains:
         w.update(synth.random_gains(s, wl.seed, device=DEV))
     ctx = synth.context_lengths(wl)
     max_ctx = int(ctx.max())
-    dr = Drafter(s, w, n_req=wl.n_req, cap=wl.cap, max_inject_rows=0, L=wl.L, K=wl.K,
+    dr = Drafter(s, w, n_req=wl.n_req, cap=wl.cap, max_inject_rows=0, L=wl.L, K=K,
                  anchor_sees_block=anchor_sees_block)
     ks, vs = synth.cache_prefix(s, wl.n_req, wl.cap, wl.seed, device=DEV)
     for l in range(s.n_layers):
@@ -139,8 +140,8 @@ def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None):
     del ks, vs
     anchors = synth.anchors(wl.n_req, s.vocab, s.mask_id, wl.seed)
     D = wl.L - 1
-    ids = torch.empty(wl.n_req, D, wl.K, dtype=torch.int32, device=DEV)
-    lp = torch.empty(wl.n_req, D, wl.K, dtype=torch.float32, device=DEV)
+    ids = torch.empty(wl.n_req, D, K, dtype=torch.int32, device=DEV)
+    lp = torch.empty(wl.n_req, D, K, dtype=torch.float32, device=DEV)
     logits = torch.empty(wl.n_req, D, s.vocab, dtype=torch.float32, device=DEV)
     dr.draft_block(_i32(anchors), _i32(ctx), max_ctx, ids, lp, logits)
     ids2, lp2 = torch.empty_like(ids), torch.empty_like(lp)
@@ -157,7 +158,7 @@ def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None):
         ref = od.drafter_block(ow, dims, ck, cv, int(ctx[r]), int(anchors[r]), wl.L,
                                anchor_sees_block=anchor_sees_block)
         _check_logits_topk(ref, logits[r].cpu().numpy().astype(np.float64),
-                           ids[r].cpu().numpy(), lp[r].cpu().numpy(), wl.K, tol(s))
+                           ids[r].cpu().numpy(), lp[r].cpu().numpy(), K, tol(s))
 
 
 def test_draft_tiny_fp32():
@@ -171,6 +172,13 @@ def test_draft_tiny_fp32_gains_and_anchor_isolation():
 
 def test_draft_qwen3_4b_shape():
     _draft_case(1)
+
+
+@pytest.mark.parametrize("K", [5, 16, 32])
+def test_draft_qwen3_4b_shape_fused_topk_widths(K):
+    # batch 1: the top-K rides in the LM-head epilogue; K <= 8 takes the
+    # row-per-lane fold, larger K the warp-wide one (sorted merges up to 16)
+    _draft_case(1, K=K)
 
 
 def test_draft_qwen3_8b_shape_long_context():
