@@ -83,38 +83,11 @@ __device__ __forceinline__ uint64_t max_keys(const uint64_t (&key)[NSL]) {
   return t[0];
 }
 
-// One request per warp; NSL = key registers per lane, 32 * NSL >= B + 1 slots.
+// Algorithm 1, one pop after another, on one warp (shared-memory records in
+// sm, inputs already in sm.lp / sm.ids).  Fills sm.node[0..n]; returns n.
 template <int NSL>
-__global__ void __launch_bounds__(kBuildWarps * 32)
-ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
-                    const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
-                    int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
-                    int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
-                    int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ int seq_build(const WarpSmem& sm, int D, int K, int B, int lane, int32_t root) {
   const unsigned FULL = 0xffffffffu;
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int req = blockIdx.x * kBuildWarps + wib;
-  pdl_wait();
-  pdl_trigger();
-  if (req >= n_req) return;
-  const int W = (B + 1 + 31) / 32;
-
-  unsigned char* base = smem_raw + build_warp_bytes(D, K, B) * wib;
-  WarpSmem sm;
-  {
-    size_t off = 0;
-    sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
-    sm.slot = reinterpret_cast<uint4*>(base + off); off += align_up(sizeof(uint4) * (B + 1), 16);
-    sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
-    sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
-    sm.stage = reinterpret_cast<uint32_t*>(base + off);
-  }
-  const float* lp_r = lp_g + (size_t)req * D * K;
-  const int32_t* ids_r = ids_g + (size_t)req * D * K;
-  for (int i = lane; i < D * K; i += 32) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
-  __syncwarp();
   // log-probability at (depth d, 0-based rank i), 0 outside the table (the
   // callers only use such values when the matching candidate does not exist)
   auto lpat = [&](int d, int i) {
@@ -123,7 +96,7 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
     return in ? v : 0.f;
   };
   if (lane == 0) {
-    sm.node[0] = static_cast<uint32_t>(root_tok[req]);
+    sm.node[0] = static_cast<uint32_t>(root);
     sm.node[1] = 0xFFFFFFFFu;  // parent -1
     sm.node[2] = 0;
     sm.node[3] = 0;
@@ -207,6 +180,15 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   }
   __syncwarp();
 
+  return n;
+}
+
+// Flattened tree and ancestor mask of request req from sm.node[0..n], one warp.
+__device__ void write_tree(const WarpSmem& sm, int n, int B, int req, int lane,
+                           int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
+                           int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
+                           int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
+  const int W = (B + 1 + 31) / 32;
   // ---- flattened tree (coalesced, -1 past the last node) ----
   const size_t nb_out = (size_t)req * (B + 1);
   for (int i = lane; i <= B; i += 32) {
@@ -241,31 +223,363 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   }
 }
 
+__device__ __forceinline__ WarpSmem carve_warp_smem(unsigned char* base, int D, int K, int B) {
+  WarpSmem sm;
+  size_t off = 0;
+  sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
+  sm.slot = reinterpret_cast<uint4*>(base + off); off += align_up(sizeof(uint4) * (B + 1), 16);
+  sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
+  sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
+  sm.stage = reinterpret_cast<uint32_t*>(base + off);
+  return sm;
+}
+
+// One request per warp; NSL = key registers per lane, 32 * NSL >= B + 1 slots.
 template <int NSL>
-void launch_build_t(const TreeBuildLaunch& a, size_t smem, cudaStream_t st) {
+__global__ void __launch_bounds__(kBuildWarps * 32)
+ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
+                    const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
+                    int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
+                    int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
+                    int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int req = blockIdx.x * kBuildWarps + wib;
+  pdl_wait();
+  pdl_trigger();
+  if (req >= n_req) return;
+  const WarpSmem sm = carve_warp_smem(smem_raw + build_warp_bytes(D, K, B) * wib, D, K, B);
+  const float* lp_r = lp_g + (size_t)req * D * K;
+  const int32_t* ids_r = ids_g + (size_t)req * D * K;
+  for (int i = lane; i < D * K; i += 32) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
+  __syncwarp();
+  const int n = seq_build<NSL>(sm, D, K, B, lane, root_tok[req]);
+  write_tree(sm, n, B, req, lane, n_nodes_out, tok_out, parent_out, depth_out, rank_out,
+             mask_out);
+}
+
+// ---------------------------------------------------------------------------
+// Parallel construction for distinct scores.  When every depth's list is
+// non-increasing and <= 0, a candidate never outscores its parent or its
+// previous sibling, so the heap pops nodes in globally descending score order
+// and the tree is the B best prefixes.  When no two of those scores are equal
+// (and the B-th is strictly above every prefix left out) the creation-order
+// rule never applies and the pop order is the descending score order.  One
+// CTA finds that set depth by depth: the candidates of depth d are the children
+// of the depth d-1 nodes still kept, a child below the current B-th best score
+// is pruned, and a radix select over the order-preserving score bits keeps the
+// best B.  Any equality met on the way (or an input outside the conditions)
+// hands the request to the exact one-pop-at-a-time path.
+// ---------------------------------------------------------------------------
+constexpr int kFastThreads = 256;
+constexpr int kFastMaxB = 512;
+constexpr int kFastMaxCand = 4096;   // B * K
+
+struct FastSmem {
+  uint32_t* pkey[2];   // kept nodes: order-preserving score bits   [B]
+  int* ppar[2];        //             parent (kept index, -1 root)  [B]
+  int* pdr[2];         //             depth << 8 | rank             [B]
+  uint32_t* ckey;      // candidates of one depth                   [B*K]
+  int* cpar;
+  int* cdr;
+  int* newpos;         // old kept index -> new, later kept index -> node number [B]
+  int* front;          // kept indices of the last depth            [B]
+  uint32_t* skey;      // final sort                                [pow2 >= B]
+  int* sidx;
+  int* hist;           // [256]
+  int* misc;           // [8]
+};
+
+__host__ __device__ inline int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+__host__ __device__ inline size_t fast_scratch_bytes(int K, int B) {
+  const size_t BK = (size_t)B * K, N2 = pow2_at_least(B > 0 ? B : 1);
+  return align_up(sizeof(int) * (6 * (size_t)B + 3 * BK + 2 * (size_t)B + 2 * N2 + 256 + 8), 16);
+}
+
+__device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int K, int B) {
+  FastSmem f;
+  int* q = reinterpret_cast<int*>(base);
+  const int BK = B * K, N2 = pow2_at_least(B > 0 ? B : 1);
+  for (int b = 0; b < 2; ++b) {
+    f.pkey[b] = reinterpret_cast<uint32_t*>(q); q += B;
+    f.ppar[b] = q; q += B;
+    f.pdr[b] = q; q += B;
+  }
+  f.ckey = reinterpret_cast<uint32_t*>(q); q += BK;
+  f.cpar = q; q += BK;
+  f.cdr = q; q += BK;
+  f.newpos = q; q += B;
+  f.front = q; q += B;
+  f.skey = reinterpret_cast<uint32_t*>(q); q += N2;
+  f.sidx = q; q += N2;
+  f.hist = q; q += 256;
+  f.misc = q;
+  return f;
+}
+
+// Returns n (sm.node[0..n] filled) or -1 when the exact sequential path must
+// decide.  Every thread of the CTA calls it; all branches are CTA-uniform.
+__device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, int B, int32_t root) {
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int* misc = f.misc;   // [0] count, [1] fallback, [2] kept, [3] frontier, [4..6] select, [7] min
+  if (tid == 0) misc[1] = 0;
+  __syncthreads();
+  for (int i = tid; i < D * K; i += T) {
+    const float v = sm.lp[i];
+    bool bad = !(v <= 0.f);
+    if (i % K != 0) bad = bad || !(sm.lp[i - 1] >= v);
+    if (bad) misc[1] = 1;
+  }
+  __syncthreads();
+  if (misc[1]) return -1;
+
+  int cur = 0, n_p = 0, n_front = 1;
+  bool full = false;
+  uint32_t tau = 0;
+  if (tid == 0) f.front[0] = -1;
+  for (int d = 1; d <= D; ++d) {
+    if (tid == 0) misc[0] = 0;
+    __syncthreads();
+    // candidates: children of the depth d-1 nodes still kept
+    const uint32_t* pk = f.pkey[cur];
+    const int pairs = n_front * K;
+    for (int q = tid; q < pairs; q += T) {
+      const int fi = f.front[q / K];
+      const int r = q - (q / K) * K;
+      const float ps = fi < 0 ? 0.f : from_ordered_bits(pk[fi]);
+      const uint32_t key = ordered_bits(__fadd_rn(ps, sm.lp[(d - 1) * K + r]));
+      if (full && key <= tau) {
+        if (key == tau) misc[1] = 1;
+        continue;
+      }
+      const int slot = atomicAdd(&misc[0], 1);
+      f.ckey[slot] = key;
+      f.cpar[slot] = fi;
+      f.cdr[slot] = (d << 8) | (r + 1);
+    }
+    __syncthreads();
+    if (misc[1]) return -1;
+    const int n_c = misc[0];
+    if (n_c == 0) break;
+    const int total = n_p + n_c;
+    if (total <= B) {
+      // everything fits: append, the new depth becomes the frontier
+      for (int i = tid; i < n_c; i += T) {
+        f.pkey[cur][n_p + i] = f.ckey[i];
+        f.ppar[cur][n_p + i] = f.cpar[i];
+        f.pdr[cur][n_p + i] = f.cdr[i];
+        f.front[i] = n_p + i;
+      }
+      if (tid == 0) misc[7] = -1;   // 0xFFFFFFFF
+      __syncthreads();
+      n_p = total;
+      n_front = n_c;
+      if (n_p == B) {
+        for (int i = tid; i < n_p; i += T)
+          atomicMin(reinterpret_cast<unsigned int*>(&misc[7]), f.pkey[cur][i]);
+        __syncthreads();
+        full = true;
+        tau = static_cast<uint32_t>(misc[7]);
+      }
+      continue;
+    }
+    // radix select of the B-th largest key over kept + candidates
+    uint32_t prefix = 0, pmask = 0;
+    int need = B;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = tid; i < 256; i += T) f.hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < total; i += T) {
+        const uint32_t key = i < n_p ? f.pkey[cur][i] : f.ckey[i - n_p];
+        if ((key & pmask) == prefix) atomicAdd(&f.hist[(key >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { c[j] = f.hist[255 - 8 * lane - j]; sum += c[j]; }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        int run = incl - sum;   // keys in higher bins than this lane's
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < need && run + c[j] >= need) {
+            misc[4] = 255 - 8 * lane - j;
+            misc[5] = run;
+            misc[6] = c[j];
+          }
+          run += c[j];
+        }
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(misc[4]) << shift;
+      pmask |= 0xFFu << shift;
+      need -= misc[5];
+    }
+    if (misc[6] > 1) return -1;   // equal scores at (or above) the cut: creation order decides
+    const uint32_t cut = prefix;
+    // compaction into the other buffer; accepted candidates form the next frontier
+    const int nxt = cur ^ 1;
+    if (tid == 0) { misc[2] = 0; misc[3] = 0; }
+    __syncthreads();
+    for (int i = tid; i < total; i += T) {
+      const bool old = i < n_p;
+      const uint32_t key = old ? f.pkey[cur][i] : f.ckey[i - n_p];
+      int slot = -1;
+      if (key >= cut) {
+        slot = atomicAdd(&misc[2], 1);
+        f.pkey[nxt][slot] = key;
+        f.ppar[nxt][slot] = old ? f.ppar[cur][i] : f.cpar[i - n_p];
+        f.pdr[nxt][slot] = old ? f.pdr[cur][i] : f.cdr[i - n_p];
+        if (!old) f.front[atomicAdd(&misc[3], 1)] = slot;
+      }
+      if (old) f.newpos[i] = slot;
+    }
+    __syncthreads();
+    n_p = misc[2];
+    n_front = misc[3];
+    // parents to their new places (a kept node's parent is kept)
+    for (int i = tid; i < n_p; i += T) {
+      const int par = f.ppar[nxt][i];
+      f.ppar[nxt][i] = par < 0 ? -1 : f.newpos[par];
+    }
+    __syncthreads();
+    cur = nxt;
+    full = true;
+    tau = cut;
+    if (n_front == 0) break;
+  }
+
+  // pop order = descending score
+  const int N2 = pow2_at_least(n_p > 0 ? n_p : 1);
+  for (int i = tid; i < N2; i += T) {
+    f.skey[i] = i < n_p ? f.pkey[cur][i] : 0u;
+    f.sidx[i] = i;
+  }
+  __syncthreads();
+  for (int k = 2; k <= N2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < N2; i += T) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint32_t a = f.skey[i], b = f.skey[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? a < b : a > b) {
+            f.skey[i] = b; f.skey[ixj] = a;
+            const int t = f.sidx[i]; f.sidx[i] = f.sidx[ixj]; f.sidx[ixj] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (tid == 0) misc[1] = 0;
+  __syncthreads();
+  for (int i = tid; i + 1 < n_p; i += T)
+    if (f.skey[i] == f.skey[i + 1]) misc[1] = 1;
+  for (int i = tid; i < n_p; i += T) f.newpos[f.sidx[i]] = i + 1;   // kept index -> node number
+  __syncthreads();
+  if (misc[1]) return -1;
+  for (int i = tid; i < n_p; i += T) {
+    const int idx = f.sidx[i];
+    const int dr = f.pdr[cur][idx];
+    const int dd = dr >> 8, rr = dr & 255;
+    const int par = f.ppar[cur][idx];
+    *reinterpret_cast<uint4*>(sm.node + 4 * (i + 1)) =
+        make_uint4(static_cast<uint32_t>(sm.ids[(dd - 1) * K + (rr - 1)]),
+                   static_cast<uint32_t>(par < 0 ? 0 : f.newpos[par]), static_cast<uint32_t>(dd),
+                   static_cast<uint32_t>(rr));
+  }
+  if (tid == 0) {
+    sm.node[0] = static_cast<uint32_t>(root);
+    sm.node[1] = 0xFFFFFFFFu;
+    sm.node[2] = 0;
+    sm.node[3] = 0;
+  }
+  __syncthreads();
+  return n_p;
+}
+
+// One request per CTA: the parallel construction, else warp 0 runs the exact
+// sequential one; warp 0 writes the tree.
+template <int NSL>
+__global__ void __launch_bounds__(kFastThreads)
+ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
+                         const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
+                         int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
+                         int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
+                         int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int req = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
+  if (req >= n_req) return;
+  const WarpSmem sm = carve_warp_smem(smem_raw, D, K, B);
+  const FastSmem fs = carve_fast_smem(smem_raw + build_warp_bytes(D, K, B), K, B);
+  const float* lp_r = lp_g + (size_t)req * D * K;
+  const int32_t* ids_r = ids_g + (size_t)req * D * K;
+  for (int i = threadIdx.x; i < D * K; i += blockDim.x) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
+  __syncthreads();
+  const int32_t root = root_tok[req];
+  int n = fast_build(sm, fs, D, K, B, root);
+  if (warp != 0) return;
+  if (n < 0) n = seq_build<NSL>(sm, D, K, B, lane, root);
+  write_tree(sm, n, B, req, lane, n_nodes_out, tok_out, parent_out, depth_out, rank_out,
+             mask_out);
+}
+
+template <int NSL>
+void launch_build_t(const TreeBuildLaunch& a, cudaStream_t st) {
+  const bool fast = a.B >= 1 && a.B <= kFastMaxB && (long long)a.B * a.K <= kFastMaxCand;
+  TraceScope ts("ddtree_build", st);
+  if (fast) {
+    static bool attr_fast = false;  // per instantiation, per process
+    if (!attr_fast) {
+      cudaFuncSetAttribute(ddtree_build_fast_kernel<NSL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      attr_fast = true;
+    }
+    const size_t smem = build_warp_bytes(a.D, a.K, a.B) + fast_scratch_bytes(a.K, a.B);
+    launch_k(ddtree_build_fast_kernel<NSL>, dim3(a.n_req), dim3(kFastThreads), smem, st, a.n_req,
+             a.D, a.K, a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
+             a.depth, a.rank, a.mask);
+    return;
+  }
   static bool attr_set = false;  // per instantiation, per process
   if (!attr_set) {
     cudaFuncSetAttribute(ddtree_build_kernel<NSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          200 * 1024);
     attr_set = true;
   }
+  const size_t smem = build_warp_bytes(a.D, a.K, a.B) * kBuildWarps;
   dim3 grid(ceil_div(a.n_req, kBuildWarps));
-  TraceScope ts("ddtree_build", st);
   launch_k(ddtree_build_kernel<NSL>, grid, dim3(kBuildWarps * 32), smem, st, a.n_req, a.D, a.K,
            a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank,
            a.mask);
 }
 
 void launch_build(const TreeBuildLaunch& a, cudaStream_t st) {
-  const size_t smem = build_warp_bytes(a.D, a.K, a.B) * kBuildWarps;
   const int slots = a.B + 1;
-  if (slots <= 32) launch_build_t<1>(a, smem, st);
-  else if (slots <= 64) launch_build_t<2>(a, smem, st);
-  else if (slots <= 96) launch_build_t<3>(a, smem, st);
-  else if (slots <= 160) launch_build_t<5>(a, smem, st);
-  else if (slots <= 288) launch_build_t<9>(a, smem, st);
-  else if (slots <= 544) launch_build_t<17>(a, smem, st);
-  else launch_build_t<33>(a, smem, st);
+  if (slots <= 32) launch_build_t<1>(a, st);
+  else if (slots <= 64) launch_build_t<2>(a, st);
+  else if (slots <= 96) launch_build_t<3>(a, st);
+  else if (slots <= 160) launch_build_t<5>(a, st);
+  else if (slots <= 288) launch_build_t<9>(a, st);
+  else if (slots <= 544) launch_build_t<17>(a, st);
+  else launch_build_t<33>(a, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -111,6 +111,10 @@ def _check_tree(gpu, ref_list, B):
     (4, 1, 8, 16, 0.0),        # D = 1: a fan
     (2, 5, 3, 0, 0.0),         # B = 0: root only
     (7, 16, 8, 31, 1.0),       # every row coarsely quantised: many exact ties
+    (1, 15, 8, 256, 0.0),      # 8B workload, no ties: the parallel construction
+    (4, 15, 8, 512, 0.0),      # its largest budget
+    (3, 15, 8, 300, 0.0),      # a budget that is not a power of two
+    (6, 15, 8, 256, 0.05),     # a few tied rows: some requests fall back
 ])
 def test_tree_build_bit_exact(n_req, D, K, B, ties):
     lp, ids = synth.random_topk_table(n_req, D, K, 50000, seed=B + D + n_req,
@@ -119,6 +123,23 @@ def test_tree_build_bit_exact(n_req, D, K, B, ties):
     gpu, _ = _gpu_tree(lp, ids, roots, B)
     refs = [odt.build_tree(lp[r], ids[r], int(roots[r]), B) for r in range(n_req)]
     _check_tree(gpu, refs, B)
+
+
+@pytest.mark.parametrize("kind", ["unsorted", "positive", "zero"])
+def test_tree_build_inputs_outside_the_sorted_case(kind):
+    # the parallel construction assumes non-increasing, non-positive rows and
+    # distinct scores; anything else must still match Algorithm 1 exactly
+    lp, ids = synth.random_topk_table(3, 15, 8, 50000, seed=17, tie_fraction=0.0)
+    if kind == "unsorted":
+        lp[:, 4, [2, 5]] = lp[:, 4, [5, 2]]
+    elif kind == "positive":
+        lp[:, 2, 0] = 0.25
+    else:
+        lp[:, 6, 0] = 0.0
+    roots = np.arange(3, dtype=np.int32)
+    gpu, _ = _gpu_tree(lp, ids, roots, 256)
+    refs = [odt.build_tree(lp[r], ids[r], int(roots[r]), 256) for r in range(3)]
+    _check_tree(gpu, refs, 256)
 
 
 def test_exact_tie_order_on_gpu():
