@@ -89,6 +89,25 @@ def test_heap_returns_top_b_of_all_prefixes(ties):
     assert np.all(ps[1:] <= ps[:-1])
 
 
+def test_distinct_scores_pop_in_descending_order_of_all_prefixes():
+    # The premise of the GPU's parallel construction: with non-increasing,
+    # non-positive rows and pairwise distinct prefix scores, Algorithm 1 pops
+    # exactly the B best prefixes, one after another in descending score order.
+    D, K, B = 6, 3, 40
+    lp, ids = _table(5, D, K, ties=False)
+    prefixes = _all_prefixes(D, K)
+
+    def f32score(rho):
+        s = np.float32(0.0)
+        for i, r in enumerate(rho):
+            s = np.float32(s + lp[i, r - 1])
+        return s
+    scored = sorted(((float(f32score(p)), tuple(p)) for p in prefixes), reverse=True)
+    assert len({sc for sc, _ in scored}) == len(scored)   # the table has no ties
+    tree = odt.build_tree(lp, ids, root_tok=1, B=B)
+    assert [tuple(t) for t in _node_tuples(tree)] == [p for _, p in scored[:B]]
+
+
 def test_enumerates_every_prefix_exactly_once():
     D, K = 3, 3
     lp, ids = _table(5, D, K, ties=True)
