@@ -18,12 +18,14 @@
 //
 // Chains.  One launch runs up to kMaxPhases dependent GEMMs ("phases", e.g.
 // W_o -> W_gate|up -> W_down -> next layer's W_qkv), each GEMM's activations
-// being an earlier phase's output.  Weights depend on nothing, so the weight
-// stream runs through all phases without a break; only the activation tiles
-// of phase k wait, on a grid-wide counter that every CTA bumps (release) once
-// its epilogue work for phase k-1 is done.  The ring holds the weight tiles
-// already fetched meanwhile, so the hand-over between phases costs no stream
-// time as long as it is shorter than the ring's worth of streaming.
+// being an earlier phase's output.  The activation tiles of phase k wait on a
+// grid-wide counter that every CTA bumps (release) once its epilogue work for
+// phase k-1 is done; the weight tiles of phase k (which depend on nothing) only
+// wait for the CTA's own epilogue of phase k-1, so a CTA's weight stream starts
+// as soon as it has finished its part of the previous phase, without the
+// launch, TMEM allocation and pipeline fill of a new kernel.  (Streaming them
+// even earlier was measured to lose: the extra traffic slows the epilogues
+// that everyone waits for.)
 //
 // Roles (7 warps): warp 0 lane 0 loads weight tiles into a multi-stage shared
 // memory ring (evict-first in L2); warp 6 lane 0 loads the matching activation
@@ -300,7 +302,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   uint64_t* acce = accf + 2;           // [2] accumulator a has been drained
   uint64_t* drain = acce + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [0] abort, [1] last
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [0] abort, [2] progress
   float* buf = reinterpret_cast<float*>(smem + SL.buf_off);
   float* s_scale = reinterpret_cast<float*>(smem + SL.scale_off);
   float* s_red = reinterpret_cast<float*>(smem + SL.red_off);
@@ -326,6 +328,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     ptx::mbar_init(drain, 1);
     flags[0] = 0;
     flags[1] = 0;
+    flags[2] = 0;   // phases whose epilogue this CTA has finished
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -373,6 +376,20 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           // the tiles about to be read by TMA (async proxy) were written with
           // ordinary stores by other CTAs
           asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        if (wprod && k > 0) {
+          // Phase k's weights wait for this CTA's own epilogue of phase k-1:
+          // streaming them earlier competes with that epilogue's loads and
+          // stores, delays the phase hand-over and costs more than it saves.
+          const uint64_t t0 = global_ns();
+          while (flags[2] < k) {
+            if (flags[0] || global_ns() - t0 > kTimeoutNs) break;
+          }
+          if (flags[2] < k) {
+            if (!flags[0]) record_status(p.status, DFLASH_ERR_TIMEOUT);
+            flags[0] = 1;
+            break;
+          }
         }
         const CUtensorMap* map = wprod ? &maps.w[k] : &maps.x[k];
         uint8_t* dst0 = wprod ? sA : sB;
@@ -662,7 +679,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
       // this CTA's share of phase k is written: publish it
       ptx::named_bar_sync(1, kEpiThreads);
-      if (etid == 0) red_release_add(&p.sync[k], 1);
+      if (etid == 0) {
+        red_release_add(&p.sync[k], 1);
+        flags[2] = k + 1;   // the weight stream of phase k+1 may start
+      }
     }
   }
 
