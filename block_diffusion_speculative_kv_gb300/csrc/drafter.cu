@@ -386,6 +386,9 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     el.L = L;
     el.tk_part = fused_topk ? reinterpret_cast<float*>(c.ws + W.tkpart) : nullptr;
     el.tk_K = K;
+    // K <= 8: the LM-head chain also merges the records (no separate kernel)
+    el.tk_ids = fused_topk && K <= 8 ? topk_ids : nullptr;
+    el.tk_logp = fused_topk && K <= 8 ? topk_logp : nullptr;
     return Step{&model->tm_lm, model->w.lm_head, xn, d.d, d.vocab, d.d, el};
   };
   {
@@ -467,6 +470,7 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     if (st) return st;
   }
   // log-softmax + top-K
+  if (fused_topk && K <= 8) return DFLASH_OK;   // merged inside the LM-head chain
   if (fused_topk) {
     launch_topk_merge(reinterpret_cast<const float*>(c.ws + W.tkpart), num_sms(), n_req * D, K,
                       topk_ids, topk_logp, c.st);

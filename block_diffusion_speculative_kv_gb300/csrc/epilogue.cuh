@@ -79,6 +79,10 @@ struct EpiParams {
   // fused top-K of the logits rows: per-CTA records [grid][n_req*(L-1)][kTkStride]
   float* tk_part;
   int tk_K;
+  // when set (K <= 8, LOGITS the chain's last phase) the last CTA to publish its
+  // records merges them into ids / log-probabilities [n_req*(L-1)][K]
+  int32_t* tk_ids;
+  float* tk_logp;
 };
 
 // Record of a fused top-K: max, sum of exp(x - max), K values (desc), K ids.
@@ -135,17 +139,79 @@ __device__ __forceinline__ int row_request(const int* row_off, int n_req, int ro
   return lo;
 }
 
+// The global inputs of one chunk's epilogue that do not depend on the
+// accumulator (RESID: residual rows and gain; QKV: RoPE rotation; KV: RoPE
+// rotation and cache slot).  Loading them ahead of the accumulator lets the
+// loads overlap the MMAs.
+struct EpiPre {
+  float a[kChunk];   // RESID: x; QKV / KV: cos
+  float b[kChunk];   // QKV / KV: sin
+  int s[kChunk];     // KV: (request * n_kv) * cap + position, or -1 outside the slab
+  float g;           // RESID: gain of the column
+};
+
+template <typename T>
+__device__ __forceinline__ void epi_preload(const EpiParams& e, int col0, int crow0, int nrows,
+                                            int f, EpiPre& pre) {
+  const int col = col0 + f;
+  const bool cvalid = col < e.N_feat;
+  switch (e.kind) {
+    case EPI_RESID: {
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r)
+        pre.a[r] = (r < nrows && cvalid) ? e.x[(size_t)(crow0 + r) * e.N_feat + col] : 0.f;
+      pre.g = cvalid ? to_f32<T>(static_cast<const T*>(e.gain)[col]) : 0.f;
+      break;
+    }
+    case EPI_QKV: {
+      const bool rot = col < e.rope_cols;
+      const int half = e.head_dim >> 1;
+      const int i = col % e.head_dim;
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const float2 cs = (rot && r < nrows) ? e.rope[(size_t)(crow0 + r) * half + (i % half)]
+                                             : make_float2(1.f, 0.f);
+        pre.a[r] = cs.x;
+        pre.b[r] = cs.y;
+      }
+      break;
+    }
+    case EPI_KV: {
+      if (!cvalid) break;
+      const int kvd = e.n_kv * e.head_dim;
+      const int kind = (col / kvd) & 1;
+      const int i = (col % kvd) % e.head_dim;
+      const int half = e.head_dim >> 1;
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const int row = crow0 + (r < nrows ? r : 0);
+        const int req = row_request(e.row_off, e.n_req, row);
+        const int pos = e.pos0[req] + (row - e.row_off[req]);
+        const float2 cs =
+            (kind == 0) ? e.rope[(size_t)row * half + (i % half)] : make_float2(1.f, 0.f);
+        pre.a[r] = cs.x;
+        pre.b[r] = cs.y;
+        pre.s[r] = (r >= nrows || pos < 0 || pos >= e.cap) ? -1 : (req * e.n_kv) * e.cap + pos;
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
 // Apply the epilogue to one chunk: rows [crow0, crow0 + nrows) (nrows <= 16)
 // of the tile whose first column is col0.  buf[r * kBufLd + c] holds acc.  `f`
 // is this thread's tile column; all 128 threads of the group call this
 // together (warp-uniform control flow, shuffles inside).  s_scale is indexed by
 // row - srow0; s_red[warp][row - srow0] accumulates RESID sums of squares.
-// The rows are unrolled so every global load of the chunk is in flight at once.
+// pre: epi_preload of the same chunk.
 template <typename T>
 __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float* buf, int col0,
                                                 int crow0, int nrows, int f,
                                                 const float* s_scale, int srow0,
-                                                float* s_red, int s_red_ld, int ewarp) {
+                                                float* s_red, int s_red_ld, int ewarp,
+                                                const EpiPre& pre) {
   const int col = col0 + f;
   const bool cvalid = col < e.N_feat;
   const int lane = f & 31;
@@ -172,11 +238,6 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
       const int half = e.head_dim >> 1;
       const int i = col % e.head_dim;
       const int pf = (i < half) ? f + half : f - half;
-      float2 cs[kChunk];
-#pragma unroll
-      for (int r = 0; r < kChunk; ++r)
-        cs[r] = (rot && r < nrows) ? e.rope[(size_t)(crow0 + r) * half + (i % half)]
-                                   : make_float2(1.f, 0.f);
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) {
         if (r < nrows && cvalid) {
@@ -184,7 +245,7 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
           float v = a[r] * s;
           if (rot) {
             const float pv = buf[r * kBufLd + pf] * s;
-            v = (i < half) ? (v * cs[r].x - pv * cs[r].y) : (v * cs[r].x + pv * cs[r].y);
+            v = (i < half) ? (v * pre.a[r] - pv * pre.b[r]) : (v * pre.a[r] + pv * pre.b[r]);
           }
           static_cast<T*>(e.out)[(size_t)(crow0 + r) * e.ldo + col] = from_f32<T>(v);
         }
@@ -194,9 +255,8 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
     case EPI_RESID: {
       float xv[kChunk];
 #pragma unroll
-      for (int r = 0; r < kChunk; ++r)
-        xv[r] = (r < nrows && cvalid) ? e.x[(size_t)(crow0 + r) * e.N_feat + col] : 0.f;
-      const float g = cvalid ? to_f32<T>(static_cast<const T*>(e.gain)[col]) : 0.f;
+      for (int r = 0; r < kChunk; ++r) xv[r] = pre.a[r];
+      const float g = pre.g;
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) {
         if (r < nrows && cvalid) {
@@ -243,25 +303,16 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
       const int half = e.head_dim >> 1;
       const int pf = (i < half) ? f + half : f - half;
       T* dst = static_cast<T*>(kind == 0 ? e.cache_k[layer] : e.cache_v[layer]);
-      int req[kChunk], pos[kChunk];
-      float2 cs[kChunk];
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) {
-        const int row = crow0 + (r < nrows ? r : 0);
-        req[r] = row_request(e.row_off, e.n_req, row);
-        pos[r] = e.pos0[req[r]] + (row - e.row_off[req[r]]);
-        cs[r] = (kind == 0) ? e.rope[(size_t)row * half + (i % half)] : make_float2(1.f, 0.f);
-      }
-#pragma unroll
-      for (int r = 0; r < kChunk; ++r) {
-        if (r >= nrows || pos[r] < 0 || pos[r] >= e.cap) continue;  // outside the slab
+        if (pre.s[r] < 0) continue;  // outside the slab (or past nrows)
         float v = a[r];
         if (kind == 0) {
           const float pv = buf[r * kBufLd + pf];
-          v = (i < half) ? (v * cs[r].x - pv * cs[r].y) : (v * cs[r].x + pv * cs[r].y);
+          v = (i < half) ? (v * pre.a[r] - pv * pre.b[r]) : (v * pre.a[r] + pv * pre.b[r]);
         }
-        dst[(((size_t)req[r] * e.n_kv + head) * e.cap + pos[r]) * e.head_dim + i] =
-            from_f32<T>(v);
+        // ((req * n_kv + head) * cap + pos) * head_dim + i
+        dst[((size_t)pre.s[r] + (size_t)head * e.cap) * e.head_dim + i] = from_f32<T>(v);
       }
       break;
     }

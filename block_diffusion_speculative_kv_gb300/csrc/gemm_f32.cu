@@ -64,8 +64,10 @@ gemm_f32_kernel(const float* __restrict__ X, long long ldx, const float* __restr
   epi_row_scales(e, row0, nrows, s_scale, threadIdx.x, 128);
   for (int i = threadIdx.x; i < 4 * kChunk; i += 128) s_red[i] = 0.f;
   __syncthreads();
+  EpiPre pre;
+  epi_preload<float>(e, col0, row0, nrows, f, pre);
   epi_apply_chunk<float>(e, buf, col0, row0, nrows, f, s_scale, row0, s_red, kChunk,
-                         threadIdx.x >> 5);
+                         threadIdx.x >> 5, pre);
   if (e.kind == EPI_RESID) {
     __syncthreads();
     epi_resid_flush(e, ftile, row0, nrows, s_red, kChunk, 4, threadIdx.x, 128);

@@ -286,6 +286,109 @@ __device__ __forceinline__ void tk_update_rows(const EpiParams& E, float* tk, in
     }
 }
 
+// Merge of two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  s = (M == -CUDART_INF_F) ? 0.f
+      : (m == -CUDART_INF_F ? 0.f : s * exp2f((m - M) * 1.4426950408889634f)) +
+            (m2 == -CUDART_INF_F ? 0.f : s2 * exp2f((m2 - M) * 1.4426950408889634f));
+  m = M;
+}
+
+// a := the 8 best of a and b, both sorted by (value desc, id asc).  The better
+// of a[q] and b[7-q] at every q is the top half of the union as a bitonic
+// sequence; three half-cleaner stages sort it.
+__device__ __forceinline__ void tk_merge8(float (&a)[8], int (&ai)[8], const float (&b)[8],
+                                          const int (&bi)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (tk_better(b[7 - q], bi[7 - q], a[q], ai[q])) { a[q] = b[7 - q]; ai[q] = bi[7 - q]; }
+#pragma unroll
+  for (int j = 4; j > 0; j >>= 1) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if ((q & j) == 0 && tk_better(a[q + j], ai[q + j], a[q], ai[q])) {
+        const float tv = a[q];
+        const int ti = ai[q];
+        a[q] = a[q + j];
+        ai[q] = ai[q + j];
+        a[q + j] = tv;
+        ai[q + j] = ti;
+      }
+    }
+  }
+}
+
+// Butterfly over lane groups: after the offsets lo..hi (powers of two, xor),
+// every lane of a group holds the group's merged list and (max, sum).
+__device__ __forceinline__ void tk_lane_merge(float (&tv)[8], int (&ti)[8], float& m, float& s,
+                                              int off_lo, int off_hi) {
+  for (int off = off_lo; off <= off_hi; off <<= 1) {
+    float ov[8];
+    int oi[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      ov[q] = __shfl_xor_sync(0xffffffffu, tv[q], off);
+      oi[q] = __shfl_xor_sync(0xffffffffu, ti[q], off);
+    }
+    lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off));
+    tk_merge8(tv, ti, ov, oi);
+  }
+}
+
+// Final top-K of one logits row from the per-CTA records (K <= 8), by the 128
+// epilogue threads of one CTA: each thread folds records etid, etid + 128, ...;
+// a butterfly merges each warp; the four warps' lists (32 entries) are sorted
+// across one warp.  scratch: 4 * 18 floats of shared memory.
+__device__ __forceinline__ void tk_row_merge(const EpiParams& E, int n_rec, int n_out, int orow,
+                                             int etid, int ew, int lane, float* scratch) {
+  const int K = E.tk_K;
+  float m = -CUDART_INF_F, sm = 0.f;
+  float tv[8];
+  int ti[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) { tv[q] = -CUDART_INF_F; ti[q] = 0x7fffffff; }
+  for (int r = etid; r < n_rec; r += kEpiThreads) {
+    const float* rec = E.tk_part + ((size_t)r * n_out + orow) * kTkStride;
+    float v[8];
+    int id[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[q] = q < K ? __ldcg(rec + 2 + q) : -CUDART_INF_F;
+      id[q] = q < K ? __float_as_int(__ldcg(rec + 2 + kTkMax + q)) : 0x7fffffff;
+    }
+    lse_merge(m, sm, __ldcg(rec), __ldcg(rec + 1));
+    tk_merge8(tv, ti, v, id);
+  }
+  tk_lane_merge(tv, ti, m, sm, 1, 16);
+  if (lane == 0) {
+    float* o = scratch + ew * 18;
+    o[0] = m;
+    o[1] = sm;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      o[2 + q] = tv[q];
+      o[10 + q] = __int_as_float(ti[q]);
+    }
+  }
+  ptx::named_bar_sync(1, kEpiThreads);
+  if (ew == 0) {
+    const float* o = scratch + (lane >> 3) * 18;
+    float v = o[2 + (lane & 7)];
+    int id = __float_as_int(o[10 + (lane & 7)]);
+    warp_sort_desc(v, id, lane);
+    float M = -CUDART_INF_F, S = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) lse_merge(M, S, scratch[w * 18], scratch[w * 18 + 1]);
+    const float lse = M + logf(S);
+    if (lane < K) {
+      E.tk_ids[(size_t)orow * K + lane] = id;
+      E.tk_logp[(size_t)orow * K + lane] = v - lse;
+    }
+  }
+  ptx::named_bar_sync(1, kEpiThreads);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
@@ -544,6 +647,50 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // accumulator read straight from TMEM.
         const bool single = nslots == 1;
         const bool reducer = !single && c == c_first;
+        // One 16-row chunk per tile: what the epilogue reads besides the
+        // accumulator is loaded while the MMAs run -- the chunk's EpiPre and,
+        // for a split tile, the sum of the other CTAs' partials (their K
+        // blocks open their unit ranges, so they are posted early).  The
+        // partial slots are read as float4, 16 values per thread.
+        const bool early = p.n_tile == kChunk;
+        EpiPre pre;
+        float4 psum[4];
+        if (early && (single || reducer)) epi_preload<T>(E, ftile * kTileN, row0, nrows, f, pre);
+        if (early && reducer) {
+          bool got = true;
+          if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
+          if (ptx::named_bar_or(1, kEpiThreads, !got)) {
+            record_status(p.status, DFLASH_ERR_TIMEOUT);
+            flags[0] = 1;
+            stop = true;
+            break;
+          }
+          const float4* slots4 = reinterpret_cast<const float4*>(
+              p.part + (size_t)c_first * P.max_slots * kChunk * kTileN);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) psum[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          // slots 1.. in order, five slots' loads in flight together
+          for (int s0 = 1; s0 < nslots; s0 += 5) {
+            float4 v[5][4];
+#pragma unroll
+            for (int sq = 0; sq < 5; ++sq)
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                v[sq][q] = s0 + sq < nslots
+                               ? __ldcg(slots4 + (size_t)(s0 + sq) * (kChunk * kTileN / 4) +
+                                        etid + 128 * q)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int sq = 0; sq < 5; ++sq)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                psum[q].x += v[sq][q].x;
+                psum[q].y += v[sq][q].y;
+                psum[q].z += v[sq][q].z;
+                psum[q].w += v[sq][q].w;
+              }
+          }
+        }
 
         const bool ok = ptx::mbar_wait_bounded(&accf[acc], acc_phase, kTimeoutNs, flags);
         if (!ok) {
@@ -573,7 +720,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         } else {
           if (!scales_once) epi_row_scales(E, row0, nrows, s_scale, etid, kEpiThreads);
           for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
-          if (reducer) {
+          if (reducer && !early) {
             bool got = true;
             if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
             if (ptx::named_bar_or(1, kEpiThreads, !got)) {
@@ -590,7 +737,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             __syncwarp();
             ptx::tmem_ld_32x16(tacc + static_cast<uint32_t>(c0), sum);
             // slots 1.. in order; four slots' loads (16 rows each) in flight together
-            for (int s0 = 1; s0 < nslots; s0 += 4) {
+            for (int s0 = 1; !early && s0 < nslots; s0 += 4) {
               float v[4][kChunk];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
@@ -607,8 +754,24 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = sum[j];
             ptx::named_bar_sync(1, kEpiThreads);
+            if (early && reducer) {
+              // float4 q of this thread: row (etid + 128 q) / 32, columns 4 * (etid % 32) ..
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float4* d = reinterpret_cast<float4*>(buf + ((etid >> 5) + 4 * q) * kBufLd +
+                                                      4 * (etid & 31));
+                float4 w = *d;
+                w.x += psum[q].x;
+                w.y += psum[q].y;
+                w.z += psum[q].z;
+                w.w += psum[q].w;
+                *d = w;
+              }
+              ptx::named_bar_sync(1, kEpiThreads);
+            }
+            if (!early) epi_preload<T>(E, ftile * kTileN, row0 + c0, nr, f, pre);
             epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
-                               p.n_tile, ew);
+                               p.n_tile, ew, pre);
             if (fused_tk) {
               if (E.tk_K <= 8)
                 tk_update_rows(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, ftile * kTileN,
@@ -636,7 +799,36 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         ptx::named_bar_sync(1, kEpiThreads);
         const int K = E.tk_K;
         const int n_out = E.M_rows / E.L * (E.L - 1);
-        for (int row = ew; row < min(p.n_tile, E.M_rows); row += 4) {
+        const int n_rows = min(p.n_tile, E.M_rows);
+        // K <= 8: eight rows per warp pass, lane = 4 * row slot + warp state
+        for (int base = ew; K <= 8 && base < n_rows; base += 32) {
+          const int row = base + 4 * (lane >> 2);
+          const bool live = row < n_rows && row % E.L != 0;
+          const float* st = tk + ((lane & 3) * p.n_tile + (live ? row : 0)) * tk_stride;
+          float m = live ? st[0] : -CUDART_INF_F;
+          float sm = live ? st[1] : 0.f;
+          float tv[8];
+          int ti[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            tv[q] = live && q < K ? st[2 + q] : -CUDART_INF_F;
+            ti[q] = live && q < K ? __float_as_int(st[2 + p.tk_kpad + q]) : 0x7fffffff;
+          }
+          tk_lane_merge(tv, ti, m, sm, 1, 2);
+          if (live && (lane & 3) == 0) {
+            const int orow = row / E.L * (E.L - 1) + row % E.L - 1;
+            float* rec = E.tk_part + ((size_t)c * n_out + orow) * kTkStride;
+            rec[0] = m;
+            rec[1] = sm;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q < K) {
+                rec[2 + q] = tv[q];
+                rec[2 + kTkMax + q] = __int_as_float(ti[q]);
+              }
+          }
+        }
+        for (int row = ew; K > 8 && row < n_rows; row += 4) {
           if (row % E.L == 0) continue;
           const int orow = row / E.L * (E.L - 1) + row % E.L - 1;
           float* rec = E.tk_part + ((size_t)c * n_out + orow) * kTkStride;
@@ -674,6 +866,39 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           if (lane == 0) {
             rec[0] = m;
             rec[1] = sm;
+          }
+        }
+        if (E.tk_ids != nullptr) {
+          // Final merge: the last n_merge CTAs to publish their records wait
+          // for the rest, then each merges rows slot, slot + n_merge, ...
+          int* arrive = p.sync + kMaxPhases + 1;
+          int* merged = p.sync + kMaxPhases + 2;
+          const int n_merge = min(n_out, G);
+          ptx::named_bar_sync(1, kEpiThreads);
+          if (etid == 0) {
+            __threadfence();
+            flags[1] = atomicAdd(arrive, 1);
+          }
+          ptx::named_bar_sync(1, kEpiThreads);
+          const int slot = flags[1] - (G - n_merge);
+          if (slot >= 0) {
+            bool ok = true;
+            if (etid == 0) {
+              ok = wait_counter(arrive, G, flags);
+              __threadfence();
+            }
+            if (ptx::named_bar_or(1, kEpiThreads, !ok)) {
+              record_status(p.status, DFLASH_ERR_TIMEOUT);
+              flags[0] = 1;
+            } else {
+              for (int orow = slot; orow < n_out; orow += n_merge)
+                tk_row_merge(E, G, n_out, orow, etid, ew, lane, tk);
+              // the last merger resets both counters for the next launch
+              if (etid == 0 && atomicAdd(merged, 1) == n_merge - 1) {
+                *arrive = 0;
+                *merged = 0;
+              }
+            }
           }
         }
       }
@@ -802,8 +1027,12 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
   p.status = status;
   int smem = 0;
   for (int k = 0; k < n_phases; ++k)
-    if (ph[k].epi.kind == EPI_LOGITS && ph[k].epi.tk_part != nullptr)
+    if (ph[k].epi.kind == EPI_LOGITS && ph[k].epi.tk_part != nullptr) {
       p.tk_kpad = (ph[k].epi.tk_K + 7) / 8 * 8;
+      if (ph[k].epi.tk_ids != nullptr && (k != n_phases - 1 || ph[k].epi.tk_K > 8))
+        return set_error(DFLASH_ERR_INVALID_ARG,
+                         "in-chain top-K merge: LM head must be the last phase, K <= 8");
+    }
   for (int k = 0; k < n_phases; ++k) {
     const TcPlan pl = tc_plan(M_rows, ph[k].N, ph[k].K, G, p.tk_kpad);
     p.n_tile = pl.n_tile;
@@ -832,6 +1061,6 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
   return check_launch("gemm_tc");
 }
 
-int gemm_counter_ints() { return kMaxPhases * num_sms() + kMaxPhases + 1; }
+int gemm_counter_ints() { return kMaxPhases * num_sms() + kMaxPhases + 3; }
 
 }  // namespace dfl
