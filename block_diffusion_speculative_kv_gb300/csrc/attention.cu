@@ -375,9 +375,13 @@ attn_split_kernel(const AttnParams p) {
 }
 
 // Merge the partials of one (request, KV head) with log-sum-exp rescaling: a
-// warp per query row (4 rows per CTA), lanes over the head dimension.  The
-// chunk maxima are gathered 32 at a time, then the rescaled partial outputs
-// are accumulated with several chunks' loads in flight.
+// warp per query row (4 rows per CTA), lanes over the head dimension.  Up to
+// kAllParts chunks: every partial (max, sum and output slice) is loaded at
+// once and the maximum taken from the loaded values, one round trip in all.
+// More chunks: the maxima are gathered first, then the rescaled partials are
+// accumulated with U chunks' loads in flight.
+constexpr int kAllParts = 24;
+
 template <int HD>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const AttnParams p) {
@@ -390,47 +394,77 @@ attn_combine_kernel(const AttnParams p) {
   if (r >= QR) return;
   const int nparts = p.n_chunks;
   const size_t base = ((size_t)req * p.n_kv + g) * nparts * QR;
-  float M = -CUDART_INF_F;
-  for (int c0 = 0; c0 < nparts; c0 += 32) {
-    const int c = c0 + lane;
-    if (c < nparts) {
-      const size_t row = base + (size_t)c * QR + r;
-      if (p.part_ml[row * 2 + 1] > 0.f) M = fmaxf(M, p.part_ml[row * 2]);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   constexpr int DPL = HD / 32;
+  static_assert(DPL == 4 || DPL == 2, "head_dim 128 or 64");
   float acc[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
   float Lsum = 0.f;
-  constexpr int U = 8;   // chunk partials in flight per lane (16 B each)
-  static_assert(DPL == 4 || DPL == 2, "head_dim 128 or 64");
-  for (int c0 = 0; c0 < nparts; c0 += U) {
-    float w[U], l[U], v[U][DPL];
+  auto load_o = [&](size_t row, bool live, float (&v)[DPL]) {
+    const float* src = p.part_o + row * HD + lane * DPL;
+    if constexpr (DPL == 4) {
+      const float4 t = live ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = live ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+      v[0] = t.x; v[1] = t.y;
+    }
+  };
+  if (nparts <= kAllParts) {
+    float m[kAllParts], l[kAllParts], v[kAllParts][DPL];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u;
-      const size_t row = base + (size_t)(c < nparts ? c : 0) * QR + r;
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + row * 2);
-      l[u] = (c < nparts) ? ml.y : 0.f;
-      w[u] = (l[u] > 0.f) ? exp2f(ml.x - M) : 0.f;
-      const float* src = p.part_o + row * HD + lane * DPL;
-      if constexpr (DPL == 4) {
-        const float4 t = (l[u] > 0.f) ? *reinterpret_cast<const float4*>(src)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-      } else {
-        const float2 t = (l[u] > 0.f) ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
-        v[u][0] = t.x; v[u][1] = t.y;
+    for (int u = 0; u < kAllParts; ++u) {
+      const bool in = u < nparts;
+      const size_t row = base + (size_t)(in ? u : 0) * QR + r;
+      const float2 ml = in ? *reinterpret_cast<const float2*>(p.part_ml + row * 2)
+                           : make_float2(-CUDART_INF_F, 0.f);
+      m[u] = ml.x;
+      l[u] = ml.y;
+      // (an empty chunk writes no output slice: loaded here, never used)
+      load_o(row, in, v[u]);
+    }
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int u = 0; u < kAllParts; ++u)
+      if (l[u] > 0.f) M = fmaxf(M, m[u]);
+#pragma unroll
+    for (int u = 0; u < kAllParts; ++u) {
+      if (l[u] > 0.f) {
+        const float w = exp2f(m[u] - M);
+        Lsum += w * l[u];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] += w * v[u][i];
+      }
+    }
+  } else {
+    float M = -CUDART_INF_F;
+    for (int c0 = 0; c0 < nparts; c0 += 32) {
+      const int c = c0 + lane;
+      if (c < nparts) {
+        const size_t row = base + (size_t)c * QR + r;
+        if (p.part_ml[row * 2 + 1] > 0.f) M = fmaxf(M, p.part_ml[row * 2]);
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      Lsum += w[u] * l[u];
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    constexpr int U = 8;   // chunk partials in flight per lane (16 B each)
+    for (int c0 = 0; c0 < nparts; c0 += U) {
+      float w[U], l[U], v[U][DPL];
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[i] += w[u] * v[u][i];
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u;
+        const size_t row = base + (size_t)(c < nparts ? c : 0) * QR + r;
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + row * 2);
+        l[u] = (c < nparts) ? ml.y : 0.f;
+        w[u] = (l[u] > 0.f) ? exp2f(ml.x - M) : 0.f;
+        load_o(row, l[u] > 0.f, v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        Lsum += w[u] * l[u];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] += w[u] * v[u][i];
+      }
     }
   }
   const float inv = 1.f / Lsum;

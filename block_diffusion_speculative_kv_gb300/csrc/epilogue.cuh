@@ -89,7 +89,15 @@ struct EpiParams {
 constexpr int kTkMax = 32;
 constexpr int kTkStride = 2 + 2 * kTkMax;
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
+// An approximate reciprocal (rcp.approx, within about one ulp) instead of an
+// IEEE division: the epilogue's rows are short dependent chains on one warp
+// per scheduler, and the division's long sequence dominated them.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float silu_f(float g) { return g * rcp_approx(1.f + __expf(-g)); }
 
 // Row scales of the rows [row0, row0 + n) into s_scale (s = 1 without ssq).
 // A row's partial sums are split over tpr threads of one warp (tpr a power of
@@ -195,6 +203,48 @@ __device__ __forceinline__ void epi_preload(const EpiParams& e, int col0, int cr
       }
       break;
     }
+    default:
+      break;
+  }
+}
+
+// L2 prefetch of the global inputs of a chunk's epilogue (what epi_preload
+// reads), issued long before the chunk's accumulator exists.
+__device__ __forceinline__ void prefetch_l2(const void* p);
+template <typename T>
+__device__ __forceinline__ void epi_prefetch_inputs(const EpiParams& e, int col0, int crow0,
+                                                    int nrows, int f) {
+  const int col = col0 + f;
+  if (col >= e.N_feat) return;
+  if (e.kind == EPI_RESID) {
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r)
+      if (r < nrows) prefetch_l2(e.x + (size_t)(crow0 + r) * e.N_feat + col);
+  }
+}
+
+// Touch the first destination row of a chunk ahead of its stores.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+template <typename T>
+__device__ __forceinline__ void epi_touch_out(const EpiParams& e, int col0, int crow0, int f) {
+  const int col = min(col0 + f, e.N_feat - 1);
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_QKV:
+      prefetch_l2(static_cast<const T*>(e.out) + (size_t)crow0 * e.ldo + col);
+      break;
+    case EPI_SWIGLU:
+      prefetch_l2(static_cast<const T*>(e.out) + (size_t)crow0 * e.ldo + (col >> 1));
+      break;
+    case EPI_RESID:
+      prefetch_l2(static_cast<const T*>(e.xn) + (size_t)crow0 * e.N_feat + col);
+      prefetch_l2(e.ssq_out);
+      break;
+    case EPI_LOGITS:
+      if (e.logits) prefetch_l2(e.logits + col);
+      break;
     default:
       break;
   }
@@ -330,6 +380,81 @@ __device__ __forceinline__ void epi_apply_chunk(const EpiParams& e, const float*
     }
     default:
       break;
+  }
+}
+
+// RESID over one 16-row chunk with four consecutive columns per thread: warp
+// w takes rows w, w + 4, w + 8, w + 12 and lane l columns 4l .. 4l + 3, so the
+// residual rows are read and written as float4 and each row's sum of squares
+// needs one warp reduction (instead of one per row and column thread).
+// Needs N_feat % 4 == 0.  pre.a[4i + j]: x of row w + 4i, column 4l + j;
+// pre.b[j]: gain of column 4l + j.
+template <typename T>
+__device__ __forceinline__ void epi_preload_resid4(const EpiParams& e, int col0, int crow0,
+                                                   int nrows, int ew, int lane, EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  const bool cv = col < e.N_feat;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    const float4 v = (r < nrows && cv)
+                         ? *reinterpret_cast<const float4*>(e.x + (size_t)(crow0 + r) * e.N_feat + col)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    pre.a[4 * i + 0] = v.x;
+    pre.a[4 * i + 1] = v.y;
+    pre.a[4 * i + 2] = v.z;
+    pre.a[4 * i + 3] = v.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    pre.b[j] = cv ? to_f32<T>(static_cast<const T*>(e.gain)[col + j]) : 0.f;
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_apply_resid4(const EpiParams& e, const float* buf, int col0,
+                                                 int crow0, int nrows, int ew, int lane,
+                                                 int srow0, float* s_red, int s_red_ld,
+                                                 const EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  const bool cv = col < e.N_feat;
+  float ss[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    const float4 a = *reinterpret_cast<const float4*>(buf + r * kBufLd + 4 * lane);
+    const float x0 = pre.a[4 * i + 0] + a.x, x1 = pre.a[4 * i + 1] + a.y;
+    const float x2 = pre.a[4 * i + 2] + a.z, x3 = pre.a[4 * i + 3] + a.w;
+    const bool live = r < nrows && cv;
+    if (live) {
+      const size_t idx = (size_t)(crow0 + r) * e.N_feat + col;
+      *reinterpret_cast<float4*>(e.x + idx) = make_float4(x0, x1, x2, x3);
+      T* xn = static_cast<T*>(e.xn) + idx;
+      if constexpr (sizeof(T) == 2) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x0 * pre.b[0], x1 * pre.b[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(x2 * pre.b[2], x3 * pre.b[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(xn) = pk;
+      } else {
+        *reinterpret_cast<float4*>(xn) =
+            make_float4(x0 * pre.b[0], x1 * pre.b[1], x2 * pre.b[2], x3 * pre.b[3]);
+      }
+    }
+    ss[i] = live ? (x0 * x0 + x1 * x1) + (x2 * x2 + x3 * x3) : 0.f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], off);
+  }
+  if (lane < 4) {
+    float v = ss[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+      if (lane == i) v = ss[i];
+    const int r = ew + 4 * lane;
+    if (r < nrows) s_red[ew * s_red_ld + (crow0 + r - srow0)] += v;
   }
 }
 

@@ -121,10 +121,13 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
                : "memory");
 }
 // Wait until *p >= target (bounded; false on expiry or abort).
+// The polling thread backs off between reads: a hot loop takes issue slots
+// from the epilogue warp that shares its scheduler.
 __device__ __forceinline__ bool wait_counter(const int* p, int target, const volatile int* abort) {
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = global_ns();
   while (true) {
+    __nanosleep(32);
     if (ld_acquire(p) >= target) return true;
     if (abort && *abort) return false;
     if (global_ns() - t0 > kTimeoutNs) return false;
@@ -450,6 +453,25 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const uint32_t tmem_base = *tmem_slot;
   // Weights are never written by a kernel: the weight stream starts before the
   // previous kernel completes; everything else waits for it.
+  // L2 prefetch of the residual rows the first phase's epilogue will read (a
+  // hint only, so it may precede the wait below; in a layer's chain those rows
+  // were written two kernels back and are long out of L2).
+  if (warp >= 2 && warp <= 5 && p.ph[0].epi.kind == EPI_RESID && p.n_tile == kChunk) {
+    const TcPhase& P0 = p.ph[0];
+    const int G0 = P0.grid;
+    if (c < G0) {
+      const long long ub = (long long)c * P0.total_units / G0;
+      const long long ue = (long long)(c + 1) * P0.total_units / G0;
+      for (long long t = ub / P0.kblocks; t * P0.kblocks < ue; ++t) {
+        const int ftile = static_cast<int>(t / P0.n_rtiles);
+        const int row0 = static_cast<int>(t - (long long)ftile * P0.n_rtiles) * p.n_tile;
+        // only the CTA that applies the epilogue of tile t (its first units)
+        if (cta_of_unit(t * P0.kblocks, P0.total_units, G0) == c)
+          epi_prefetch_inputs<T>(P0.epi, ftile * kTileN, row0,
+                                 min(p.n_tile, P0.epi.M_rows - row0), (warp & 3) * 32 + lane);
+      }
+    }
+  }
   if (!(warp == 0 && lane == 0)) pdl_wait();
   pdl_trigger();
 
@@ -487,6 +509,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const uint64_t t0 = global_ns();
           while (flags[2] < k) {
             if (flags[0] || global_ns() - t0 > kTimeoutNs) break;
+            __nanosleep(32);   // (the epilogue warp on this scheduler is busy)
           }
           if (flags[2] < k) {
             if (!flags[0]) record_status(p.status, DFLASH_ERR_TIMEOUT);
@@ -653,9 +676,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // blocks open their unit ranges, so they are posted early).  The
         // partial slots are read as float4, 16 values per thread.
         const bool early = p.n_tile == kChunk;
+        const bool resid4 = early && E.kind == EPI_RESID && (E.N_feat & 3) == 0;
         EpiPre pre;
         float4 psum[4];
-        if (early && (single || reducer)) epi_preload<T>(E, ftile * kTileN, row0, nrows, f, pre);
+        if (early && (single || reducer)) {
+          if (resid4) epi_preload_resid4<T>(E, ftile * kTileN, row0, nrows, ew, lane, pre);
+          else epi_preload<T>(E, ftile * kTileN, row0, nrows, f, pre);
+          epi_touch_out<T>(E, ftile * kTileN, row0, f);
+        }
         if (early && reducer) {
           bool got = true;
           if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
@@ -770,8 +798,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               ptx::named_bar_sync(1, kEpiThreads);
             }
             if (!early) epi_preload<T>(E, ftile * kTileN, row0 + c0, nr, f, pre);
-            epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
-                               p.n_tile, ew, pre);
+            if (resid4)
+              epi_apply_resid4<T>(E, buf, ftile * kTileN, row0, nr, ew, lane, row0, s_red,
+                                  p.n_tile, pre);
+            else
+              epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
+                                 p.n_tile, ew, pre);
             if (fused_tk) {
               if (E.tk_K <= 8)
                 tk_update_rows(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, ftile * kTileN,
