@@ -458,6 +458,74 @@ __device__ __forceinline__ void epi_apply_resid4(const EpiParams& e, const float
   }
 }
 
+// QKV over one 16-row chunk, same mapping as epi_apply_resid4 (warp w: rows
+// w + 4i; lane l: columns 4l .. 4l + 3, which lie in one half of a head, so
+// their RoPE partners are four consecutive columns too).  Needs head_dim % 8
+// == 0 and N_feat % 4 == 0.  pre.a / pre.b[4i + j]: cos / sin of row w + 4i,
+// column 4l + j.
+__device__ __forceinline__ void epi_preload_qkv4(const EpiParams& e, int col0, int crow0,
+                                                 int nrows, int ew, int lane, EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  const bool rot = col < e.rope_cols;
+  const int half = e.head_dim >> 1;
+  const int ih = (col % e.head_dim) % half;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    float4 c01 = make_float4(1.f, 0.f, 1.f, 0.f), c23 = c01;
+    if (rot && r < nrows) {
+      const float4* src = reinterpret_cast<const float4*>(e.rope + (size_t)(crow0 + r) * half + ih);
+      c01 = src[0];
+      c23 = src[1];
+    }
+    pre.a[4 * i + 0] = c01.x; pre.b[4 * i + 0] = c01.y;
+    pre.a[4 * i + 1] = c01.z; pre.b[4 * i + 1] = c01.w;
+    pre.a[4 * i + 2] = c23.x; pre.b[4 * i + 2] = c23.y;
+    pre.a[4 * i + 3] = c23.z; pre.b[4 * i + 3] = c23.w;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_apply_qkv4(const EpiParams& e, const float* buf, int col0,
+                                               int crow0, int nrows, int ew, int lane,
+                                               const float* s_scale, int srow0,
+                                               const EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  if (col >= e.N_feat) return;
+  const bool rot = col < e.rope_cols;
+  const int half = e.head_dim >> 1;
+  const bool lo = (col % e.head_dim) < half;
+  const int pc = 4 * lane + (lo ? half : -half);   // partner columns in the tile
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    if (r >= nrows) continue;
+    const float sc = s_scale[crow0 + r - srow0];
+    const float4 a = *reinterpret_cast<const float4*>(buf + r * kBufLd + 4 * lane);
+    float v[4] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc};
+    if (rot) {
+      const float4 q = *reinterpret_cast<const float4*>(buf + r * kBufLd + pc);
+      const float pv[4] = {q.x * sc, q.y * sc, q.z * sc, q.w * sc};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float c = pre.a[4 * i + j], sn = pre.b[4 * i + j];
+        v[j] = lo ? (v[j] * c - pv[j] * sn) : (v[j] * c + pv[j] * sn);
+      }
+    }
+    T* dst = static_cast<T*>(e.out) + (size_t)(crow0 + r) * e.ldo + col;
+    if constexpr (sizeof(T) == 2) {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&p0);
+      pk.y = *reinterpret_cast<uint32_t*>(&p1);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+}
+
 // After all chunks of a RESID tile: fold the per-warp sums of squares.
 __device__ __forceinline__ void epi_resid_flush(const EpiParams& e, int ftile, int row0, int n,
                                                 const float* s_red, int s_red_ld, int nwarps,

@@ -673,14 +673,18 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // One 16-row chunk per tile: what the epilogue reads besides the
         // accumulator is loaded while the MMAs run -- the chunk's EpiPre and,
         // for a split tile, the sum of the other CTAs' partials (their K
-        // blocks open their unit ranges, so they are posted early).  The
-        // partial slots are read as float4, 16 values per thread.
+        // blocks open their unit ranges, so they are posted early).  A partial
+        // slot is then stored column-major, [128 columns][16 rows]: thread f
+        // writes and reads its column's 16 values as four float4.
         const bool early = p.n_tile == kChunk;
         const bool resid4 = early && E.kind == EPI_RESID && (E.N_feat & 3) == 0;
+        const bool qkv4 = early && E.kind == EPI_QKV && (E.N_feat & 3) == 0 &&
+                          (E.head_dim & 7) == 0 && (E.ldo & 3) == 0;
         EpiPre pre;
         float4 psum[4];
         if (early && (single || reducer)) {
           if (resid4) epi_preload_resid4<T>(E, ftile * kTileN, row0, nrows, ew, lane, pre);
+          else if (qkv4) epi_preload_qkv4(E, ftile * kTileN, row0, nrows, ew, lane, pre);
           else epi_preload<T>(E, ftile * kTileN, row0, nrows, f, pre);
           epi_touch_out<T>(E, ftile * kTileN, row0, f);
         }
@@ -706,7 +710,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               for (int q = 0; q < 4; ++q)
                 v[sq][q] = s0 + sq < nslots
                                ? __ldcg(slots4 + (size_t)(s0 + sq) * (kChunk * kTileN / 4) +
-                                        etid + 128 * q)
+                                        f * 4 + q)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int sq = 0; sq < 5; ++sq)
@@ -738,8 +742,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             float v[16];
             __syncwarp();
             ptx::tmem_ld_32x16(tacc + static_cast<uint32_t>(c0), v);
+            if (early) {
+              float4* d4 = reinterpret_cast<float4*>(my_part) + f * 4;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kTileN + f] = v[j];
+              for (int q = 0; q < 4; ++q)
+                d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kTileN + f] = v[j];
+            }
           }
           ptx::tc_fence_before();
           ptx::mbar_arrive(&acce[acc]);
@@ -779,28 +790,24 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 #pragma unroll
                 for (int j = 0; j < kChunk; ++j) sum[j] += v[q][j];
             }
+            if (early && reducer) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                sum[4 * q] += psum[q].x;
+                sum[4 * q + 1] += psum[q].y;
+                sum[4 * q + 2] += psum[q].z;
+                sum[4 * q + 3] += psum[q].w;
+              }
+            }
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) buf[j * kBufLd + f] = sum[j];
             ptx::named_bar_sync(1, kEpiThreads);
-            if (early && reducer) {
-              // float4 q of this thread: row (etid + 128 q) / 32, columns 4 * (etid % 32) ..
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float4* d = reinterpret_cast<float4*>(buf + ((etid >> 5) + 4 * q) * kBufLd +
-                                                      4 * (etid & 31));
-                float4 w = *d;
-                w.x += psum[q].x;
-                w.y += psum[q].y;
-                w.z += psum[q].z;
-                w.w += psum[q].w;
-                *d = w;
-              }
-              ptx::named_bar_sync(1, kEpiThreads);
-            }
             if (!early) epi_preload<T>(E, ftile * kTileN, row0 + c0, nr, f, pre);
             if (resid4)
               epi_apply_resid4<T>(E, buf, ftile * kTileN, row0, nr, ew, lane, row0, s_red,
                                   p.n_tile, pre);
+            else if (qkv4)
+              epi_apply_qkv4<T>(E, buf, ftile * kTileN, row0, nr, ew, lane, s_scale, row0, pre);
             else
               epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                  p.n_tile, ew, pre);
