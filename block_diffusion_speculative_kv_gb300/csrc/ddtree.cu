@@ -223,6 +223,46 @@ __device__ void write_tree(const WarpSmem& sm, int n, int B, int req, int lane,
   }
 }
 
+// The same output written by every warp of the CTA: the flat arrays by thread,
+// the mask 32 rows per warp at a time (stage: a [32][W] region per warp).
+__device__ void write_tree_cta(const WarpSmem& sm, uint32_t* stage_all, int n, int B, int req,
+                               int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
+                               int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
+                               int32_t* __restrict__ rank_out, uint32_t* __restrict__ mask_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int W = (B + 1 + 31) / 32;
+  const size_t nb_out = (size_t)req * (B + 1);
+  for (int i = tid; i <= B; i += blockDim.x) {
+    const bool live = i <= n;
+    const uint4 rec = live ? *reinterpret_cast<const uint4*>(sm.node + 4 * i) : make_uint4(0, 0, 0, 0);
+    tok_out[nb_out + i] = live ? static_cast<int32_t>(rec.x) : -1;
+    parent_out[nb_out + i] = live ? static_cast<int32_t>(rec.y) : -1;
+    depth_out[nb_out + i] = live ? static_cast<int32_t>(rec.z) : -1;
+    rank_out[nb_out + i] = live ? static_cast<int32_t>(rec.w) : -1;
+  }
+  if (tid == 0) n_nodes_out[req] = n;
+  uint32_t* stage = stage_all + (size_t)warp * 32 * W;
+  uint32_t* mrow = mask_out + nb_out * W;
+  for (int i0 = warp * 32; i0 <= B; i0 += 32 * nw) {
+    for (int t = lane; t < 32 * W; t += 32) stage[t] = 0u;
+    __syncwarp();
+    const int i = i0 + lane;
+    if (i <= n) {
+      uint32_t* st = stage + lane * W;
+      int j = i;
+      while (true) {
+        st[j >> 5] |= 1u << (j & 31);
+        if (j == 0) break;
+        j = static_cast<int>(sm.node[4 * j + 1]);
+      }
+    }
+    __syncwarp();
+    const int rows = min(32, B + 1 - i0);
+    for (int t = lane; t < rows * W; t += 32) mrow[(size_t)i0 * W + t] = stage[t];
+    __syncwarp();
+  }
+}
+
 __device__ __forceinline__ WarpSmem carve_warp_smem(unsigned char* base, int D, int K, int B) {
   WarpSmem sm;
   size_t off = 0;
@@ -289,6 +329,7 @@ struct FastSmem {
   int* sidx;
   int* hist;           // [256]
   int* misc;           // [8]
+  uint32_t* stage;     // mask staging, [kFastThreads / 32][32][W]
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -299,7 +340,9 @@ __host__ __device__ inline int pow2_at_least(int x) {
 
 __host__ __device__ inline size_t fast_scratch_bytes(int K, int B) {
   const size_t BK = (size_t)B * K, N2 = pow2_at_least(B > 0 ? B : 1);
-  return align_up(sizeof(int) * (6 * (size_t)B + 3 * BK + 2 * (size_t)B + 2 * N2 + 256 + 8), 16);
+  const size_t W = (B + 1 + 31) / 32;
+  return align_up(sizeof(int) * (6 * (size_t)B + 3 * BK + 2 * (size_t)B + 2 * N2 + 256 + 8), 16) +
+         sizeof(uint32_t) * (kFastThreads / 32) * 32 * W;
 }
 
 __device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int K, int B) {
@@ -320,6 +363,10 @@ __device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int K, 
   f.sidx = q; q += N2;
   f.hist = q; q += 256;
   f.misc = q;
+  f.stage = reinterpret_cast<uint32_t*>(
+      base + align_up(sizeof(int) * (6 * (size_t)B + 3 * (size_t)BK + 2 * (size_t)B + 2 * (size_t)N2 +
+                                     256 + 8),
+                      16));
   return f;
 }
 
@@ -462,34 +509,21 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
     if (n_front == 0) break;
   }
 
-  // pop order = descending score
-  const int N2 = pow2_at_least(n_p > 0 ? n_p : 1);
-  for (int i = tid; i < N2; i += T) {
-    f.skey[i] = i < n_p ? f.pkey[cur][i] : 0u;
-    f.sidx[i] = i;
-  }
-  __syncthreads();
-  for (int k = 2; k <= N2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < N2; i += T) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint32_t a = f.skey[i], b = f.skey[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? a < b : a > b) {
-            f.skey[i] = b; f.skey[ixj] = a;
-            const int t = f.sidx[i]; f.sidx[i] = f.sidx[ixj]; f.sidx[ixj] = t;
-          }
-        }
-      }
-      __syncthreads();
+  // pop order = descending score: a kept node's position is the number of
+  // kept keys above it (one pass, no sorting network); equal keys are left to
+  // the exact sequential construction
+  for (int i = tid; i < n_p; i += T) {
+    const uint32_t ki = f.pkey[cur][i];
+    int gt = 0, eq = 0;
+    for (int j = 0; j < n_p; ++j) {
+      const uint32_t kj = f.pkey[cur][j];
+      gt += kj > ki ? 1 : 0;
+      eq += kj == ki ? 1 : 0;
     }
+    if (eq > 1) misc[1] = 1;
+    f.sidx[gt < n_p ? gt : n_p - 1] = i;
+    f.newpos[i] = gt + 1;   // kept index -> node number
   }
-  if (tid == 0) misc[1] = 0;
-  __syncthreads();
-  for (int i = tid; i + 1 < n_p; i += T)
-    if (f.skey[i] == f.skey[i + 1]) misc[1] = 1;
-  for (int i = tid; i < n_p; i += T) f.newpos[f.sidx[i]] = i + 1;   // kept index -> node number
   __syncthreads();
   if (misc[1]) return -1;
   for (int i = tid; i < n_p; i += T) {
@@ -535,10 +569,17 @@ ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict
   __syncthreads();
   const int32_t root = root_tok[req];
   int n = fast_build(sm, fs, D, K, B, root);
-  if (warp != 0) return;
-  if (n < 0) n = seq_build<NSL>(sm, D, K, B, lane, root);
-  write_tree(sm, n, B, req, lane, n_nodes_out, tok_out, parent_out, depth_out, rank_out,
-             mask_out);
+  if (n < 0) {
+    // (uniform: every thread saw the same flag)
+    if (warp == 0) {
+      n = seq_build<NSL>(sm, D, K, B, lane, root);
+      if (lane == 0) fs.misc[0] = n;
+    }
+    __syncthreads();
+    n = fs.misc[0];
+  }
+  write_tree_cta(sm, fs.stage, n, B, req, n_nodes_out, tok_out, parent_out, depth_out, rank_out,
+                 mask_out);
 }
 
 template <int NSL>
