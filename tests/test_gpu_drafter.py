@@ -181,6 +181,11 @@ def test_draft_qwen3_4b_shape_fused_topk_widths(K):
     _draft_case(1, K=K)
 
 
+def test_draft_qwen3_4b_shape_anchor_isolated():
+    # the anchor row sees no other block position (tensor-core attention mask)
+    _draft_case(1, anchor_sees_block=False)
+
+
 def test_draft_qwen3_8b_shape_long_context():
     _draft_case(2)
 
