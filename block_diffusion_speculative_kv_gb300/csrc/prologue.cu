@@ -40,53 +40,72 @@ block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,
   const int row = blockIdx.x;
   const int req = row / L, j = row % L;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  pdl_wait();
-  pdl_trigger();
+  // Everything read here is an input of the call (or a weight): the previous
+  // kernel writes none of it, and every kernel before that one has completed
+  // once this one runs.  So the loads and the arithmetic come first and only
+  // the stores wait for the previous kernel (which may share these workspace
+  // regions).
   int tok = (j == 0) ? anchor[req] : mask_id;
-  if (tok < 0 || tok >= vocab) {
-    if (threadIdx.x == 0) record_status(status, DFLASH_ERR_INVALID_ARG);
-    tok = 0;
-  }
+  const bool bad_tok = tok < 0 || tok >= vocab;
+  if (bad_tok) tok = 0;
   // warp w takes the 128-column parts w, w+4, ...; lane l the 4 columns 4l..4l+3
   const int parts = (d + 127) / 128;
-  constexpr int kMaxParts = 64;  // d <= 8192
+  constexpr int kParts = 8;   // parts per warp held in registers (the first 4 * 8 * 128 columns)
   const T* erow = embed + (size_t)tok * d;
-  for (int p0 = warp; p0 < parts; p0 += 4 * 8) {
-    float v[8][4], g[8][4];
+  float v[kParts][4], g[kParts][4], sq[kParts];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int p = p0 + 4 * u;
+  for (int u = 0; u < kParts; ++u) {
+    const int p = warp + 4 * u;
+    sq[u] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = p * 128 + lane * 4 + e;
-        const bool ok = p < parts && c < d;
-        v[u][e] = ok ? to_f32<T>(erow[c]) : 0.f;
-        g[u][e] = ok ? to_f32<T>(gain[c]) : 0.f;
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int c = p * 128 + lane * 4 + e;
+      const bool ok = p < parts && c < d;
+      v[u][e] = ok ? to_f32<T>(erow[c]) : 0.f;
+      g[u][e] = ok ? to_f32<T>(gain[c]) : 0.f;
+      sq[u] += v[u][e] * v[u][e];
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int p = p0 + 4 * u;
-      float sq = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = p * 128 + lane * 4 + e;
-        if (p < parts && c < d) {
-          x[(size_t)row * d + c] = v[u][e];
-          xn[(size_t)row * d + c] = from_f32<T>(v[u][e] * g[u][e]);
-        }
-        sq += v[u][e] * v[u][e];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-      if (lane == 0 && p < parts) ssq[(size_t)p * R + row] = sq;
-    }
+    for (int off = 16; off > 0; off >>= 1) sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], off);
   }
-  (void)kMaxParts;
   const int half = head_dim / 2;
   const int pos = ctx_len[req] + j;
-  for (int i = threadIdx.x; i < half; i += blockDim.x)
-    rope[(size_t)row * half + i] = rope_cs(pos, i, fr);
+  const int i_rope = threadIdx.x;
+  const float2 cs = i_rope < half ? rope_cs(pos, i_rope, fr) : make_float2(1.f, 0.f);
+  pdl_wait();
+  pdl_trigger();
+  if (bad_tok && threadIdx.x == 0) record_status(status, DFLASH_ERR_INVALID_ARG);
+#pragma unroll
+  for (int u = 0; u < kParts; ++u) {
+    const int p = warp + 4 * u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = p * 128 + lane * 4 + e;
+      if (p < parts && c < d) {
+        x[(size_t)row * d + c] = v[u][e];
+        xn[(size_t)row * d + c] = from_f32<T>(v[u][e] * g[u][e]);
+      }
+    }
+    if (lane == 0 && p < parts) ssq[(size_t)p * R + row] = sq[u];
+  }
+  if (i_rope < half) rope[(size_t)row * half + i_rope] = cs;
+  // columns past the first 4 * kParts parts (d > 4096): loaded after the wait
+  for (int p = warp + 4 * kParts; p < parts; p += 4) {
+    float s2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = p * 128 + lane * 4 + e;
+      if (c < d) {
+        const float a = to_f32<T>(erow[c]);
+        x[(size_t)row * d + c] = a;
+        xn[(size_t)row * d + c] = from_f32<T>(a * to_f32<T>(gain[c]));
+        s2 += a * a;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+    if (lane == 0) ssq[(size_t)p * R + row] = s2;
+  }
 }
 
 __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* __restrict__ pos0,
@@ -94,18 +113,23 @@ __global__ void inject_rope_kernel(const int* __restrict__ row_off, const int* _
                                    float2* __restrict__ rope) {
   const int half = head_dim / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  // (inputs only: computed before the wait, stored after it)
+  const bool live = idx < (long long)n_rows * half;
+  float2 cs = make_float2(1.f, 0.f);
+  if (live) {
+    const int row = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+    int lo = 0, hi = n_req - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (row_off[mid] <= row) lo = mid;
+      else hi = mid - 1;
+    }
+    const int pos = pos0[lo] + (row - row_off[lo]);
+    cs = rope_cs(pos, i, fr);
+  }
   pdl_wait();
   pdl_trigger();
-  if (idx >= (long long)n_rows * half) return;
-  const int row = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
-  int lo = 0, hi = n_req - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (row_off[mid] <= row) lo = mid;
-    else hi = mid - 1;
-  }
-  const int pos = pos0[lo] + (row - row_off[lo]);
-  rope[idx] = rope_cs(pos, i, fr);
+  if (live) rope[idx] = cs;
 }
 
 }  // namespace
