@@ -4,8 +4,9 @@
 One step is one drafter cycle of the Qwen3-8B-shaped batch-1 workload
 (5 layers, hidden 4096, 32/8 heads of 128, FFN 12288, vocabulary 151936,
 8192 injected context positions, block L = 16, top-K 8, DDTree budget 256):
-  dflash_inject_kv    the 16 newest context positions (W_proj and U_K/U_V)
-  dflash_draft_block  5 layers + LM head + log-softmax + top-K
+  dflash_draft_cycle  dflash_inject_kv (the 16 newest context positions: W_proj
+                      and U_K/U_V) then dflash_draft_block (5 layers + LM head +
+                      log-softmax + top-K), one call
   ddtree_build        Algorithm 1 + ancestor mask
 The acceptance walk is timed separately (accept_us).  Inputs are seeded
 synthetic data of those shapes (no trained weights or datasets exist here).
@@ -226,8 +227,10 @@ class Cycle:
         self.target = None
 
     def run(self):
-        self.dr.inject_kv(self.feats, self.row_off, self.pos0)
-        self.dr.draft_block(self.anchor, self.ctx_len, self.max_ctx, self.ids, self.lp)
+        # inject + draft as one C-ABI call (the injection's GEMMs share a
+        # launch with the first QKV projection), then the tree
+        self.dr.draft_cycle(self.feats, self.row_off, self.pos0, self.anchor, self.ctx_len,
+                            self.max_ctx, self.ids, self.lp)
         self.bd.ddtree_build(self.lp, self.ids, self.anchor, self.wl.B, *self.tree)
 
     def make_targets(self):

@@ -68,6 +68,8 @@ _SIGS = {
     "dflash_inject_kv": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_draft_block": (_i, [_vp, C.POINTER(Cache), _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
+    "dflash_draft_cycle": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i,
+                                _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_topk_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_logits_topk": (_i, [_i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "ddtree_build": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),

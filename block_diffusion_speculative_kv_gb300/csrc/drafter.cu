@@ -251,9 +251,10 @@ size_t dflash_workspace_bytes(const dflash_model* model, int n_req, int max_inje
   return ws_layout(*model, n_req, max_inject_rows, L, K).total;
 }
 
-dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* cache, int n_req,
-                               int n_rows, const int32_t* row_off, const int32_t* pos0,
-                               const void* feats, void* ws, size_t ws_bytes, void* stream) {
+// Validation of the injection's arguments (the workspace is checked by the caller).
+static dflash_status check_inject(const dflash_model* model, const dflash_cache* cache, int n_req,
+                           int n_rows, const int32_t* row_off, const int32_t* pos0,
+                           const void* feats) {
   if (!model || !cache) return set_error(DFLASH_ERR_INVALID_ARG, "null model or cache");
   if (n_req < 1 || n_req > cache->n_req)
     return set_error(DFLASH_ERR_INVALID_ARG, "n_req must be in [1, cache->n_req]");
@@ -267,27 +268,26 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
   if (cache->cap < 1) return set_error(DFLASH_ERR_INVALID_ARG, "cache cap must be >= 1");
   if (model->bf16 && !aligned16(feats))
     return set_error(DFLASH_ERR_INVALID_ARG, "feats must be 16-byte aligned");
-  // the workspace must have been sized for at least n_rows injected rows
-  const WsLayout L = ws_layout(*model, n_req, n_rows, 2, 1);
-  const size_t need = L.rope_inj + sizeof(float2) * (size_t)n_rows * (d.head_dim / 2);
-  if (!ws || ws_bytes < need)
-    return set_error(DFLASH_ERR_WORKSPACE, "inject workspace needs %zu bytes, got %zu", need,
-                     ws_bytes);
-  CallCtx c{model, static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream),
-            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + L.counters)};
-  float2* rope = reinterpret_cast<float2*>(c.ws + L.rope_inj);
+  return DFLASH_OK;
+}
+
+// Steps a1 + a2 as two GEMM steps (f = feats . W_proj^T; [K|V] of every layer
+// = f . U^T, K rotated, scattered into the cache), after the RoPE table of the
+// injected positions is launched.
+static dflash_status inject_steps(const dflash_model* model, const dflash_cache* cache, int n_req,
+                           int n_rows, const int32_t* row_off, const int32_t* pos0,
+                           const void* feats, const CallCtx& c, Step (&out)[2]) {
+  const dflash_dims& d = model->dims;
+  float2* rope = reinterpret_cast<float2*>(c.ws + c.L.rope_inj);
   launch_inject_rope(row_off, pos0, n_req, n_rows, d.head_dim, model->freqs, rope, c.st);
   dflash_status st = check_launch("inject rope");
   if (st) return st;
-
-  // a1: f = feats . W_proj^T
-  void* f = c.ws + L.f;
+  void* f = c.ws + c.L.f;
   EpiParams e1 = epi_base(*model, n_rows, d.d);
   e1.kind = EPI_STORE;
   e1.ssq_in = nullptr;
   e1.out = f;
   e1.ldo = d.d;
-  // a2: [K|V] of every layer = f . U^T, K rotated, scattered into the cache
   EpiParams e2 = epi_base(*model, n_rows, d.n_layers * 2 * d.n_kv * d.head_dim);
   e2.kind = EPI_KV;
   e2.ssq_in = nullptr;
@@ -301,17 +301,36 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
   e2.n_req = n_req;
   e2.row_off = row_off;
   e2.pos0 = pos0;
-  const Step chain[2] = {
-      {&model->tm_proj, model->w.w_proj, feats, (long long)d.n_feat * d.d_feat, d.d,
-       d.n_feat * d.d_feat, e1},
-      {&model->tm_ukv, model->w.u_kv, f, d.d, d.n_layers * 2 * d.n_kv * d.head_dim, d.d, e2}};
+  out[0] = Step{&model->tm_proj, model->w.w_proj, feats, (long long)d.n_feat * d.d_feat, d.d,
+                d.n_feat * d.d_feat, e1};
+  out[1] = Step{&model->tm_ukv, model->w.u_kv, f, d.d, d.n_layers * 2 * d.n_kv * d.head_dim,
+                d.d, e2};
+  return DFLASH_OK;
+}
+
+dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* cache, int n_req,
+                               int n_rows, const int32_t* row_off, const int32_t* pos0,
+                               const void* feats, void* ws, size_t ws_bytes, void* stream) {
+  dflash_status st = check_inject(model, cache, n_req, n_rows, row_off, pos0, feats);
+  if (st || n_rows == 0) return st;
+  const dflash_dims& d = model->dims;
+  // the workspace must have been sized for at least n_rows injected rows
+  const WsLayout L = ws_layout(*model, n_req, n_rows, 2, 1);
+  const size_t need = L.rope_inj + sizeof(float2) * (size_t)n_rows * (d.head_dim / 2);
+  if (!ws || ws_bytes < need)
+    return set_error(DFLASH_ERR_WORKSPACE, "inject workspace needs %zu bytes, got %zu", need,
+                     ws_bytes);
+  CallCtx c{model, static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream),
+            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + L.counters)};
+  Step chain[2];
+  st = inject_steps(model, cache, n_req, n_rows, row_off, pos0, feats, c, chain);
+  if (st) return st;
   return run_chain(c, chain, 2, n_rows);
 }
 
-dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache, int n_req,
-                                 const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
-                                 int L, int K, int32_t* topk_ids, float* topk_logp,
-                                 float* logits, void* ws, size_t ws_bytes, void* stream) {
+static dflash_status check_draft(const dflash_model* model, const dflash_cache* cache, int n_req,
+                          const int32_t* anchor, const int32_t* ctx_len, int max_ctx, int L,
+                          int K, int32_t* topk_ids, float* topk_logp) {
   if (!model || !cache) return set_error(DFLASH_ERR_INVALID_ARG, "null model or cache");
   const dflash_dims& d = model->dims;
   if (n_req < 1 || n_req > cache->n_req)
@@ -325,12 +344,17 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     return set_error(DFLASH_ERR_INVALID_ARG, "null anchor/ctx_len/topk output");
   for (int l = 0; l < d.n_layers; ++l)
     if (!cache->k[l] || !cache->v[l]) return set_error(DFLASH_ERR_INVALID_ARG, "null cache layer %d", l);
-  const WsLayout W = ws_layout(*model, n_req, 0, L, K);
-  if (!ws || ws_bytes < W.f)
-    return set_error(DFLASH_ERR_WORKSPACE, "draft workspace needs %zu bytes, got %zu", W.f,
-                     ws_bytes);
-  CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
-            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
+  return DFLASH_OK;
+}
+
+// Steps a3 - a6.  `pre`: GEMM steps over the same n_req * L activation rows
+// that run in the first GEMM launch, ahead of layer 0's QKV projection.
+static dflash_status draft_impl(const dflash_model* model, const dflash_cache* cache, int n_req,
+                         const int32_t* anchor, const int32_t* ctx_len, int max_ctx, int L, int K,
+                         int32_t* topk_ids, float* topk_logp, float* logits, const CallCtx& c,
+                         const Step* pre, int n_pre) {
+  const dflash_dims& d = model->dims;
+  const WsLayout& W = c.L;
   const int R = n_req * L;
   const int D = L - 1;
   const int hd = d.head_dim;
@@ -392,8 +416,10 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
     return Step{&model->tm_lm, model->w.lm_head, xn, d.d, d.vocab, d.d, el};
   };
   {
-    const Step first = qkv_step(0);
-    st = run_chain(c, &first, 1, R);
+    Step first[kMaxPhases];
+    for (int i = 0; i < n_pre; ++i) first[i] = pre[i];
+    first[n_pre] = qkv_step(0);
+    st = run_chain(c, first, n_pre + 1, R);
     if (st) return st;
   }
   for (int l = 0; l < d.n_layers; ++l) {
@@ -490,6 +516,56 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
   tk.logp = topk_logp;
   launch_topk(tk, c.st);
   return check_launch("top-K");
+}
+
+dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache, int n_req,
+                                 const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
+                                 int L, int K, int32_t* topk_ids, float* topk_logp,
+                                 float* logits, void* ws, size_t ws_bytes, void* stream) {
+  dflash_status st = check_draft(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids,
+                                 topk_logp);
+  if (st) return st;
+  const WsLayout W = ws_layout(*model, n_req, 0, L, K);
+  if (!ws || ws_bytes < W.f)
+    return set_error(DFLASH_ERR_WORKSPACE, "draft workspace needs %zu bytes, got %zu", W.f,
+                     ws_bytes);
+  CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
+            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
+  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
+                    logits, c, nullptr, 0);
+}
+
+dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* cache, int n_req,
+                                 int n_rows, const int32_t* row_off, const int32_t* pos0,
+                                 const void* feats, const int32_t* anchor,
+                                 const int32_t* ctx_len, int max_ctx, int L, int K,
+                                 int32_t* topk_ids, float* topk_logp, float* logits, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  dflash_status st = check_inject(model, cache, n_req, n_rows, row_off, pos0, feats);
+  if (st) return st;
+  st = check_draft(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp);
+  if (st) return st;
+  const WsLayout W = ws_layout(*model, n_req, n_rows, L, K);
+  if (!ws || ws_bytes < W.total)
+    return set_error(DFLASH_ERR_WORKSPACE, "cycle workspace needs %zu bytes, got %zu", W.total,
+                     ws_bytes);
+  CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
+            static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
+  if (n_rows == 0)
+    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
+                      logits, c, nullptr, 0);
+  Step inj[2];
+  st = inject_steps(model, cache, n_req, n_rows, row_off, pos0, feats, c, inj);
+  if (st) return st;
+  // One GEMM launch for the injection and layer 0's QKV when they share the
+  // activation row count (a chain runs over one row count).
+  if (model->bf16 && n_rows == n_req * L)
+    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
+                      logits, c, inj, 2);
+  st = run_chain(c, inj, 2, n_rows);
+  if (st) return st;
+  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
+                    logits, c, nullptr, 0);
 }
 
 size_t dflash_linear_workspace_bytes(int M, int N, int K) {

@@ -203,6 +203,21 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
                                  float* topk_logp, float* logits,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* Steps a1 - a6 in one call: dflash_inject_kv(n_rows, row_off, pos0, feats)
+ * followed by dflash_draft_block(anchor, ctx_len, max_ctx, L, K, ...), with the
+ * same arguments, meanings and results as the two calls in sequence (the new
+ * context entries are visible to the block pass).  When the injected row count
+ * equals n_req * L (bf16 models), the injection's two GEMMs and the first
+ * layer's QKV projection run in one GEMM launch.  The workspace must be sized
+ * by dflash_workspace_bytes(model, n_req, >= n_rows, L, >= K).  n_rows may be
+ * 0 (the block pass alone). */
+dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* cache,
+                                 int n_req, int n_rows, const int32_t* row_off,
+                                 const int32_t* pos0, const void* feats,
+                                 const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
+                                 int L, int K, int32_t* topk_ids, float* topk_logp,
+                                 float* logits, void* ws, size_t ws_bytes, void* stream);
+
 /* Step a6 on its own: log-softmax + top-K over given logits rows (DDTree page,
  * 3.4.2 and Lemma 1 in 3.4.4: only the top-K tokens per depth are needed).
  *   logits  [rows][ld] of dtype (DFLASH_F32 or DFLASH_BF16), vocab <= ld

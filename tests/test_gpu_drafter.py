@@ -196,3 +196,51 @@ def test_draft_batched_ragged_sampled():
     ctx = synth.context_lengths(wl)
     pick = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 7})
     _draft_case(3, sample_reqs=pick)
+
+
+# ---------------------------------------------------------------------------
+# inject + draft as one call
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wid,rows_per_req", [
+    (1, None),      # n_rows == n_req * L: the injection shares the first GEMM launch
+    (1, [5]),       # other row counts: the two steps run one after the other
+    (0, None),      # fp32 model
+])
+def test_draft_cycle_equals_inject_then_draft(wid, rows_per_req):
+    wl = WORKLOADS[wid]
+    s = wl.shape
+    n_req = wl.n_req
+    if rows_per_req is None:
+        rows_per_req = [wl.L] * n_req
+    w = synth.drafter_weights(s, wl.seed, device=DEV)
+    ctx = synth.context_lengths(wl)
+    max_ctx = int(ctx.max())
+    n_rows = sum(rows_per_req)
+    dr = Drafter(s, w, n_req=n_req, cap=wl.cap, max_inject_rows=n_rows, L=wl.L, K=wl.K)
+    ks, vs = synth.cache_prefix(s, n_req, wl.cap, wl.seed, device=DEV)
+    feats = synth.features(n_rows, s, wl.seed, stream=7, device=DEV)
+    row_off = np.concatenate([[0], np.cumsum(rows_per_req)])
+    pos0 = ctx - np.asarray(rows_per_req)          # the newest positions of each context
+    anchors = _i32(synth.anchors(n_req, s.vocab, s.mask_id, wl.seed))
+    D = wl.L - 1
+    outs = []
+    for fused in (False, True):
+        for l in range(s.n_layers):
+            dr.cache_k[l].copy_(ks[l])
+            dr.cache_v[l].copy_(vs[l])
+        ids = torch.empty(n_req, D, wl.K, dtype=torch.int32, device=DEV)
+        lp = torch.empty(n_req, D, wl.K, dtype=torch.float32, device=DEV)
+        if fused:
+            dr.draft_cycle(feats, _i32(row_off), _i32(pos0), anchors, _i32(ctx), max_ctx, ids, lp)
+        else:
+            dr.inject_kv(feats, _i32(row_off), _i32(pos0))
+            dr.draft_block(anchors, _i32(ctx), max_ctx, ids, lp)
+        torch.cuda.synchronize()
+        assert dr.read_status() == 0
+        outs.append((ids, lp, [c.clone() for c in dr.cache_k], [c.clone() for c in dr.cache_v]))
+    (i0, l0, k0, v0), (i1, l1, k1, v1) = outs
+    assert torch.equal(i0, i1)
+    assert torch.equal(l0, l1)
+    for a, b in zip(k0 + v0, k1 + v1):
+        assert torch.equal(a, b)
