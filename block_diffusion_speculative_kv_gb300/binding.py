@@ -70,6 +70,12 @@ _SIGS = {
                                 _vp, _sz, _vp]),
     "dflash_draft_cycle": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i,
                                 _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dflash_tree_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "dflash_tree_attention": (_i, [_i, _i, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, C.c_longlong,
+                                   _vp, _vp, C.c_longlong, _vp, _vp, _vp, C.c_longlong, _vp,
+                                   _sz, _vp]),
+    "dflash_tree_rope": (_i, [_i, _i, _i, _i, C.c_float, _vp, _vp, _vp, C.c_longlong, _i,
+                              _vp]),
     "dflash_topk_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_logits_topk": (_i, [_i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "ddtree_build": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -235,3 +241,38 @@ def tree_buffers(n_req: int, B: int, device="cuda"):
     return (torch.empty(n_req, **i32), torch.empty(n_req, B + 1, **i32),
             torch.empty(n_req, B + 1, **i32), torch.empty(n_req, B + 1, **i32),
             torch.empty(n_req, B + 1, **i32), torch.empty(n_req, B + 1, W, **i32))
+
+
+# ---------------------------------------------------------------------------
+# Verification-side tree attention (DDTree page, 3.4.5)
+# ---------------------------------------------------------------------------
+
+def tree_attention_workspace_bytes(n_req: int, n_q: int, n_kv: int, head_dim: int, B: int,
+                                   max_ctx: int) -> int:
+    return int(lib().dflash_tree_attention_workspace_bytes(n_req, n_q, n_kv, head_dim, B,
+                                                           max_ctx))
+
+
+def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cache_k: torch.Tensor,
+                   cache_v: torch.Tensor, ctx_len: torch.Tensor, max_ctx: int,
+                   mask: torch.Tensor, n_nodes: torch.Tensor, out: torch.Tensor,
+                   ws: torch.Tensor, stream=None):
+    """q [n_req, B+1, n_q*hd], k/v [n_req, B+1, n_kv*hd], cache [n_req, n_kv, cap, hd]
+    (bf16), mask [n_req, B+1, W] (int32 view of the uint32 words), out like q."""
+    n_req, B1, qw = q.shape
+    _, n_kv, cap, hd = cache_k.shape
+    n_q = qw // hd
+    _check(lib().dflash_tree_attention(
+        n_req, n_q, n_kv, hd, B1 - 1, _ptr(ctx_len), max_ctx, cap, _ptr(cache_k),
+        _ptr(cache_v), _ptr(q), q.stride(1), _ptr(k), _ptr(v), k.stride(1), _ptr(mask),
+        _ptr(n_nodes), _ptr(out), out.stride(1), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def tree_rope(x: torch.Tensor, n_heads: int, head_dim: int, theta: float, ctx_len: torch.Tensor,
+              depth: torch.Tensor, stream=None):
+    """Rotate heads 0..n_heads-1 of x [n_req, B+1, ld] in place at ctx_len + depth."""
+    n_req, B1, ld = x.shape
+    _check(lib().dflash_tree_rope(n_req, B1 - 1, n_heads, head_dim, theta, _ptr(ctx_len),
+                                  _ptr(depth), _ptr(x), x.stride(1), _dtype_code(x),
+                                  _stream(stream)))

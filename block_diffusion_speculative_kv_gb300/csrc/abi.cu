@@ -68,10 +68,6 @@ void trace(const char* kernel, int phase, cudaStream_t st) {
 
 using namespace dfl;
 
-#define DFL_REQUIRE(cond, ...)                                   \
-  do {                                                           \
-    if (!(cond)) return set_error(DFLASH_ERR_INVALID_ARG, __VA_ARGS__); \
-  } while (0)
 
 extern "C" {
 

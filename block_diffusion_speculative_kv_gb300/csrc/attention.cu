@@ -21,6 +21,7 @@
 // in turn with an online softmax (used for fp32 models).
 #include "attention.h"
 #include "common.cuh"
+#include "mma_sync.cuh"
 
 #include <math_constants.h>
 
@@ -28,56 +29,10 @@ namespace dfl {
 
 namespace {
 
+using namespace mmas;
+
 constexpr int kKeyTile = 64;
 constexpr int kStages = 6;   // K/V tiles in flight per CTA (~192 KB at head_dim 128)
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Byte offset of 16-byte chunk `ch` of row `row` in a [rows][HD] bf16 tile.
-template <int HD>
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-  return static_cast<uint32_t>(row * (HD * 2) + ((ch ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 template <int HD>
 __global__ void __launch_bounds__(256, 1)
@@ -467,9 +422,18 @@ attn_combine_kernel(const AttnParams p) {
       }
     }
   }
-  const float inv = 1.f / Lsum;
+  // (a row that saw no key at all, a tree node past the last one, gets zeros)
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   const int h = g * p.G + r / p.L, j = r % p.L;
-  __nv_bfloat16* dst = p.out + ((size_t)req * p.L + j) * p.out_ld + (size_t)h * HD + lane * DPL;
+  // blockIdx.z: a request, or with query tiles (tree attention) a (request,
+  // tile) pair whose rows are nodes tile * L + j of out_rows per request
+  size_t orow = (size_t)req * p.L + j;
+  if (p.n_qt > 0) {
+    const int node = (req % p.n_qt) * p.L + j;
+    if (node >= p.out_rows) return;
+    orow = (size_t)(req / p.n_qt) * p.out_rows + node;
+  }
+  __nv_bfloat16* dst = p.out + orow * p.out_ld + (size_t)h * HD + lane * DPL;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) dst[i] = __float2bfloat16_rn(acc[i] * inv);
 }
@@ -530,6 +494,12 @@ attn_f32_kernel(const AttnParamsF32 p) {
 }
 
 }  // namespace
+
+void launch_attn_combine(const AttnParams& p, int head_dim, dim3 cgrid, cudaStream_t st) {
+  TraceScope ts("attn_combine", st);
+  if (head_dim == 128) launch_k(attn_combine_kernel<128>, cgrid, dim3(128), 0, st, p);
+  else launch_k(attn_combine_kernel<64>, cgrid, dim3(128), 0, st, p);
+}
 
 int attn_chunk(int max_ctx, int n_kv, int n_req) {
   // One CTA per SM holds a deep ring: when a wave covers every (request, KV

@@ -27,6 +27,10 @@ struct AttnParams {
   float* part_ml;  // [n_req][n_kv][n_chunks][G*L][2]
   __nv_bfloat16* out;
   long long out_ld;
+  // tree attention only (0 otherwise): query tiles per request, and the
+  // output's rows per request (B + 1)
+  int n_qt;
+  int out_rows;
 };
 
 struct AttnParamsF32 {
@@ -45,6 +49,8 @@ struct AttnParamsF32 {
 int attn_chunk(int max_ctx, int n_kv, int n_req);
 size_t attn_smem_bytes(int G, int L, int HD);
 dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStream_t st);
+// the merge of the split partials alone (grid: row blocks of 4, KV heads, blockIdx.z units)
+void launch_attn_combine(const AttnParams& p, int head_dim, dim3 cgrid, cudaStream_t st);
 dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStream_t st);
 
 }  // namespace dfl

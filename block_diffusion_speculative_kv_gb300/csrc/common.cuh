@@ -110,3 +110,10 @@ struct TraceScope {
 };
 
 }  // namespace dfl
+
+// Argument check of a C-ABI entry point: on failure, record the message and
+// return DFLASH_ERR_INVALID_ARG.
+#define DFL_REQUIRE(cond, ...)                                            \
+  do {                                                                    \
+    if (!(cond)) return dfl::set_error(DFLASH_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)

@@ -62,6 +62,17 @@ struct RopeFreqs {
   double f[64];
 };
 RopeFreqs rope_freqs(float theta, int head_dim);
+// (cos, sin) of pos * f[i]: the angle is formed and reduced modulo 2*pi in
+// double (three FP64 operations), its sine and cosine taken in fp32.
+__device__ __forceinline__ float2 rope_cs(int pos, int i, const RopeFreqs& fr) {
+  const double two_pi = 6.283185307179586476925;
+  const double a = static_cast<double>(pos) * fr.f[i];
+  const double k = rint(a * (1.0 / two_pi));
+  const float r = static_cast<float>(fma(-k, two_pi, a));
+  float s, c;
+  sincosf(r, &s, &c);
+  return make_float2(c, s);
+}
 
 struct BlockPrologueLaunch {
   bool bf16;

@@ -19,16 +19,6 @@ namespace dfl {
 
 namespace {
 
-__device__ __forceinline__ float2 rope_cs(int pos, int i, const RopeFreqs& fr) {
-  const double two_pi = 6.283185307179586476925;
-  const double a = static_cast<double>(pos) * fr.f[i];
-  const double k = rint(a * (1.0 / two_pi));
-  const float r = static_cast<float>(fma(-k, two_pi, a));
-  float s, c;
-  sincosf(r, &s, &c);
-  return make_float2(c, s);
-}
-
 template <typename T>
 __global__ void __launch_bounds__(128)
 block_prologue_kernel(const T* __restrict__ embed, const T* __restrict__ gain,

@@ -16,6 +16,9 @@
  *                       the flattened tree, depth position ids and the ancestor
  *                       attention mask (DDTree page, sections 3.4.4-3.4.5);
  *   ddtree_accept       the verifier walk against the target's token choices
+ *   dflash_tree_attention / dflash_tree_rope
+ *                       the verification pass's attention over the flattened
+ *                       tree (ancestor mask, depth position ids)
  *                       (DDTree page, section 3.4.5).
  *
  * Conventions shared by every call
@@ -283,6 +286,43 @@ dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes,
                             const int32_t* tok, const int32_t* parent,
                             const int32_t* target_tok, int32_t* accept_len,
                             int32_t* accepted, int32_t* bonus, void* stream);
+
+/* Verification-side tree attention (DDTree page, 3.4.5): one target-model
+ * attention layer over the flattened draft tree.  Per request r, tree node i
+ * (0 <= i <= n_nodes[r]; node 0 is the root) attends, head h reading KV head
+ * h / (n_q / n_kv), to
+ *   - the request's context: cache slots t < ctx_len[r] of cache_k / cache_v
+ *     ([n_req][n_kv][cap][head_dim] bf16, as the drafter's cache), and
+ *   - the tree nodes j whose bit j is set in mask row i (its ancestors and
+ *     itself; the mask ddtree_build writes, [n_req][B+1][ceil((B+1)/32)]),
+ * with softmax(q . key / sqrt(head_dim)) weights.
+ *   q    bf16 [n_req][B+1][q_ld]: query heads at columns h * head_dim,
+ *        already rotated at position ctx_len + depth (dflash_tree_rope)
+ *   k, v bf16 [n_req][B+1][kv_ld]: the nodes' own keys (rotated) and values,
+ *        KV head g at column g * head_dim
+ *   out  bf16 [n_req][B+1][out_ld]: rows of nodes past n_nodes[r] are zero
+ * Requires head_dim == 128, n_q a multiple of n_kv with at most 4 query heads
+ * per KV head, 0 <= B <= 1024, 0 <= ctx_len[r] <= max_ctx <= cap, strides that
+ * are multiples of 8 elements.  Device pointers; ws of
+ * dflash_tree_attention_workspace_bytes(...) bytes (no initialisation needed);
+ * all of it is written on the given stream. */
+size_t dflash_tree_attention_workspace_bytes(int n_req, int n_q, int n_kv, int head_dim, int B,
+                                             int max_ctx);
+dflash_status dflash_tree_attention(int n_req, int n_q, int n_kv, int head_dim, int B,
+                                    const int32_t* ctx_len, int max_ctx, int cap,
+                                    const void* cache_k, const void* cache_v, const void* q,
+                                    long long q_ld, const void* k, const void* v, long long kv_ld,
+                                    const uint32_t* mask, const int32_t* n_nodes, void* out,
+                                    long long out_ld, void* ws, size_t ws_bytes, void* stream);
+
+/* Depth position ids of the flattened tree (DDTree page, 3.4.5): rotates heads
+ * 0 .. n_heads-1 of x[r][i] (rows of ld elements, dtype DFLASH_BF16 or
+ * DFLASH_F32, in place) at position ctx_len[r] + depth[r][i] with the
+ * rotate-half RoPE of base theta; rows with depth < 0 (past the last node) are
+ * left alone.  depth is ddtree_build's [n_req][B+1] output. */
+dflash_status dflash_tree_rope(int n_req, int B, int n_heads, int head_dim, float theta,
+                               const int32_t* ctx_len, const int32_t* depth, void* x,
+                               long long ld, int dtype, void* stream);
 
 /* The dense contraction every step above is built on, exposed on its own:
  * Y[M][N] = X[M][K] . W[N][K]^T with bf16 X and W and fp32 Y, on the tcgen05
