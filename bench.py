@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
-                                       "topk_b1", "tree_stress", "tree_b1"],
+                                       "topk_b1", "tree_stress", "tree_b1", "tree_attention"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -420,6 +420,40 @@ def run_case(args):
         def fn():
             bd.logits_topk(logits, wl.K, ids, lp, ws)
         nbytes = logits.numel() * 2
+    elif args.case == "tree_attention":
+        # one Qwen3-8B-shaped target layer of the verification pass: 32/8 heads
+        # of 128, 8192 context slots, the 257-node tree of the batch-1 workload
+        wl = WORKLOADS[2]
+        n_q, n_kv, hd, B, T = 32, 8, 128, wl.B, 8192
+        lp, idt = synth.random_topk_table(1, wl.D, wl.K, 151936, wl.seed)
+        bufs = bd.tree_buffers(1, B, "cuda")
+        bd.ddtree_build(torch.from_numpy(lp).cuda(), torch.from_numpy(idt).cuda(),
+                        torch.zeros(1, dtype=torch.int32, device="cuda"), B, *bufs)
+        n_nodes, mask = bufs[0], bufs[5]
+        copies = 5                                    # 5 x 33.5 MB of cache > L2
+        cks = [(torch.randn(1, n_kv, T, hd, generator=g, device="cuda") * 0.35).to(torch.bfloat16)
+               for _ in range(copies)]
+        cvs = [torch.randn(1, n_kv, T, hd, generator=g, device="cuda").to(torch.bfloat16)
+               for _ in range(copies)]
+        q = (torch.randn(1, B + 1, n_q * hd, generator=g, device="cuda") * 0.35).to(torch.bfloat16)
+        k = (torch.randn(1, B + 1, n_kv * hd, generator=g, device="cuda") * 0.35).to(torch.bfloat16)
+        v = torch.randn(1, B + 1, n_kv * hd, generator=g, device="cuda").to(torch.bfloat16)
+        out = torch.empty_like(q)
+        ctx = torch.full((1,), T, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(bd.tree_attention_workspace_bytes(1, n_q, n_kv, hd, B, T),
+                         dtype=torch.uint8, device="cuda")
+        fn_i = [0]
+
+        def fn():
+            c = fn_i[0] % copies
+            bd.tree_attention(q, k, v, cks[c], cvs[c], ctx, T, mask, n_nodes, out, ws)
+            fn_i[0] += 1
+        torch.cuda.synchronize()
+        nn = int(n_nodes.item())
+        d_cpu = bufs[3].cpu().numpy()[0]
+        anc = int(sum(int(d_cpu[i]) + 1 for i in range(nn + 1)))   # |ancestors incl. self|
+        flops = 4.0 * hd * n_q * ((nn + 1) * T + anc)
+        nbytes = 2 * 2 * n_kv * T * hd + 3 * 2 * (B + 1) * n_q * hd
     else:
         wl = WORKLOADS[4] if args.case == "tree_stress" else WORKLOADS[2]
         lp, idt = synth.random_topk_table(wl.n_req, wl.D, wl.K, 151936, wl.seed)
@@ -436,6 +470,9 @@ def run_case(args):
            "clocks": clocks}
     if nbytes:
         out["gbs"] = round(nbytes / (us * 1e-6) / 1e9, 1)
+    if args.case == "tree_attention":
+        out["tflops"] = round(flops / (us * 1e-6) / 1e12, 1)
+        out["nodes"] = nn + 1
     print(json.dumps(out))
 
 
