@@ -14,7 +14,9 @@ Readings (the page names no sampler):
   the generator seeded with `seed` is mix(seed + k * 0x9E3779B97F4A7C15), with
   mix(z) = z ^ z >> 30, * 0xBF58476D1CE4E5B9, ^ >> 27, * 0x94D049BB133111EB,
   ^ >> 31 (all mod 2^64); element v of row r takes k = (r << 32 | v) + 1 and
-  U = (top 24 bits + 0.5) / 2^24;
+  U = (top 23 bits + 0.5) / 2^23, exact in float32 and strictly inside (0, 1)
+  (with 24 bits the largest value rounds to 1 in float32 and G becomes
+  infinite);
 * the decision is taken in float32: s_v = f32(l_v) * f32(1 / T) + G_v with G
   evaluated in float32, ties to the smaller token id; T = 0 is the argmax;
 * the chain tree of a drafted block: node 0 the anchor, node d the token of
@@ -50,8 +52,8 @@ def uniforms(seed: int, row: int, vocab: int) -> np.ndarray:
     """U_v for v < vocab of one row, float32 in (0, 1)."""
     k = (np.uint64(row) << np.uint64(32)) | np.arange(vocab, dtype=np.uint64)
     x = splitmix64_np(seed, k + np.uint64(1))
-    top = (x >> np.uint64(40)).astype(np.float64)
-    return ((top + 0.5) * 2.0 ** -24).astype(np.float32)
+    top = (x >> np.uint64(41)).astype(np.float64)
+    return ((top + 0.5) * 2.0 ** -23).astype(np.float32)
 
 
 def gumbel(u: np.ndarray) -> np.ndarray:

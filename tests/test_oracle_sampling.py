@@ -22,6 +22,11 @@ def test_splitmix64_published_outputs():
 def test_uniforms_open_interval_and_moments():
     u = osm.uniforms(7, 3, 200000)
     assert u.dtype == np.float32 and u.min() > 0 and u.max() < 1
+    # every value is an odd multiple of 2^-24, exactly representable
+    assert np.all(np.mod(u.astype(np.float64) * 2.0 ** 24, 2.0) == 1.0)
+    # the extreme codes stay inside (0, 1) with a finite Gumbel value
+    ends = np.array([(0 + 0.5) * 2.0 ** -23, (2 ** 23 - 1 + 0.5) * 2.0 ** -23], dtype=np.float32)
+    assert ends[1] < 1 and np.all(np.isfinite(osm.gumbel(ends)))
     assert abs(float(u.mean()) - 0.5) < 3e-3
     assert abs(float(u.var()) - 1 / 12) < 2e-3
 
