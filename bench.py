@@ -57,7 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
-                                       "topk_b1", "tree_stress", "tree_b1", "tree_attention"],
+                                       "topk_b1", "tree_stress", "tree_b1", "tree_attention",
+                                       "chain_sweep"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -384,8 +385,51 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def run_chain_sweep(args):
+    """Vanilla DFlash (a chain of the per-position argmax at T = 0, or of one
+    Gumbel-max sample per position at T = 1, drafted inside the LM-head top-K
+    pass) against DDTree (top-8 per position, budget B) at block sizes L = 4,
+    8, 16, on the Qwen3-8B-shaped batch-1 drafter with 8192 context slots.
+    One line per (drafter, L, T): microseconds per draft cycle (inject + draft
+    + tree)."""
+    cyc = Cycle(2)
+    bd = cyc.bd
+    wl = cyc.wl
+    i32 = dict(dtype=torch.int32, device="cuda")
+    rows = []
+    for L in (4, 8, 16):
+        D = L - 1
+        feats = cyc.feats[:L].contiguous()
+        row_off = torch.tensor([0, L], **i32)
+        pos0 = torch.as_tensor(cyc.ctx - L, **i32)
+        for drafter, T in (("chain", 0.0), ("chain", 1.0), ("ddtree", 0.0)):
+            K = 1 if drafter == "chain" else wl.K
+            B = D if drafter == "chain" else wl.B
+            ids = torch.empty(1, D, K, **i32)
+            lq = torch.empty(1, D, K, dtype=torch.float32, device="cuda")
+            tree = bd.tree_buffers(1, B, "cuda")
+            smp = (T, 12345, 0) if T > 0 else None
+
+            def fn():
+                cyc.dr.draft_cycle(feats, row_off, pos0, cyc.anchor, cyc.ctx_len, cyc.max_ctx,
+                                   ids, lq, L=L, K=K, sampling=smp)
+                if drafter == "chain":
+                    bd.chain_tree(ids, cyc.anchor, B, *tree)
+                else:
+                    bd.ddtree_build(lq, ids, cyc.anchor, B, *tree)
+            ms, clocks = timed_region(fn, args.steps, max(args.warmup, 3), 1)
+            assert cyc.dr.read_status() == 0
+            rows.append({"drafter": drafter, "L": L, "T": T, "K": K, "B": B,
+                         "us_per_cycle": round(ms * 1e3 / args.steps, 1),
+                         "sm_mhz": clocks.get("sm_mhz") if isinstance(clocks, dict) else None})
+    print(json.dumps({"case": "chain_sweep", "workload": wl.name, "steps": args.steps,
+                      "rows": rows}))
+
+
 def run_case(args):
     """One kernel on its own, launched back to back (inputs larger than L2)."""
+    if args.case == "chain_sweep":
+        return run_chain_sweep(args)
     from block_diffusion_speculative_kv_gb300 import binding as bd
     from block_diffusion_speculative_kv_gb300 import synth
     from block_diffusion_speculative_kv_gb300.configs import WORKLOADS

@@ -54,6 +54,19 @@ class Cache(C.Structure):
                 ("n_req", C.c_int), ("cap", C.c_int)]
 
 
+class Sampling(C.Structure):
+    """Temperature sampling of a top-K pass (temperature 0: plain top-K)."""
+    _fields_ = [("temperature", C.c_float), ("seed", C.c_uint64), ("row_offset", C.c_int64)]
+
+
+def sampling_arg(sampling):
+    """None, or (temperature, seed[, row_offset]) -> a Sampling pointer argument."""
+    if sampling is None:
+        return None
+    t, seed, *rest = sampling
+    return C.byref(Sampling(float(t), int(seed) & (2 ** 64 - 1), int(rest[0]) if rest else 0))
+
+
 _lib = None
 
 _vp, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
@@ -66,10 +79,10 @@ _SIGS = {
     "dflash_workspace_init": (_i, [_vp, _sz, _vp]),
     "dflash_read_status": (_i, [_vp, C.POINTER(_i), _vp]),
     "dflash_inject_kv": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "dflash_draft_block": (_i, [_vp, C.POINTER(Cache), _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp,
-                                _vp, _sz, _vp]),
+    "dflash_draft_block": (_i, [_vp, C.POINTER(Cache), _i, _vp, _vp, _i, _i, _i,
+                                C.POINTER(Sampling), _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_draft_cycle": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i,
-                                _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+                                _i, C.POINTER(Sampling), _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_tree_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "dflash_tree_attention": (_i, [_i, _i, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, C.c_longlong,
                                    _vp, _vp, C.c_longlong, _vp, _vp, _vp, C.c_longlong, _vp,
@@ -78,6 +91,9 @@ _SIGS = {
                               _vp]),
     "dflash_topk_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_logits_topk": (_i, [_i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "dflash_logits_sample": (_i, [_i, _i, _i, _i, _vp, C.POINTER(Sampling), _i, _vp, _vp, _vp,
+                                  _sz, _vp]),
+    "dflash_chain_tree": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ddtree_build": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ddtree_accept": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dflash_linear_workspace_bytes": (_sz, [_i, _i, _i]),
@@ -188,6 +204,17 @@ def logits_topk(logits: torch.Tensor, K: int, ids: torch.Tensor, logp: torch.Ten
                                     ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def logits_sample(logits: torch.Tensor, sampling, K: int, ids: torch.Tensor,
+                  logq: torch.Tensor, ws: torch.Tensor, vocab: Optional[int] = None, stream=None):
+    """Gumbel-max draw of K tokens per row at sampling = (temperature, seed[,
+    row_offset]); ids[:, 0] is a sample from softmax(logits / temperature)."""
+    rows, ld = logits.shape
+    vocab = ld if vocab is None else vocab
+    _check(lib().dflash_logits_sample(rows, vocab, ld, _dtype_code(logits), _ptr(logits),
+                                      sampling_arg(sampling), K, _ptr(ids), _ptr(logq), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def logits_topk_noalloc(logits: torch.Tensor, K: int, ids: torch.Tensor, logp: torch.Tensor,
                         vocab: Optional[int] = None, stream=None):
     """Step a6 without a workspace, for callers that cannot allocate device
@@ -224,6 +251,15 @@ def ddtree_build(topk_logp: torch.Tensor, topk_ids: torch.Tensor, root_tok: torc
     _check(lib().ddtree_build(n_req, D, K, B, _ptr(topk_logp), _ptr(topk_ids), _ptr(root_tok),
                               _ptr(n_nodes), _ptr(tok), _ptr(parent), _ptr(depth), _ptr(rank),
                               _ptr(mask), _stream(stream)))
+
+
+def chain_tree(topk_ids: torch.Tensor, root_tok: torch.Tensor, B: int, n_nodes, tok, parent,
+               depth, rank, mask, stream=None):
+    """The vanilla DFlash chain of topk_ids[:, :, 0] in ddtree_build's layout."""
+    n_req, D, K = topk_ids.shape
+    _check(lib().dflash_chain_tree(n_req, D, K, B, _ptr(topk_ids), _ptr(root_tok), _ptr(n_nodes),
+                                   _ptr(tok), _ptr(parent), _ptr(depth), _ptr(rank), _ptr(mask),
+                                   _stream(stream)))
 
 
 def ddtree_accept(D: int, B: int, n_nodes, tok, parent, target_tok, accept_len, accepted, bonus,

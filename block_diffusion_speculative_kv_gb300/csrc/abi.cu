@@ -64,6 +64,19 @@ void trace(const char* kernel, int phase, cudaStream_t st) {
   if (fn) fn(g_trace_user.load(std::memory_order_relaxed), kernel, phase, st);
 }
 
+dflash_status parse_sampling(const dflash_sampling* s, SampleSpec* out) {
+  *out = SampleSpec{};
+  if (s == nullptr || s->temperature == 0.f) return DFLASH_OK;
+  const float T = s->temperature;
+  if (!(T >= 1e-6f && T <= 1e6f))
+    return set_error(DFLASH_ERR_INVALID_ARG, "sampling temperature must be 0 or in [1e-6, 1e6]");
+  out->inv_t = static_cast<float>(1.0 / static_cast<double>(T));
+  out->t = T;
+  out->seed = s->seed;
+  out->row0 = static_cast<long long>(s->row_offset);
+  return DFLASH_OK;
+}
+
 }  // namespace dfl
 
 using namespace dfl;
@@ -107,13 +120,16 @@ size_t dflash_topk_workspace_bytes(int rows, int vocab, int K) {
          topk_part_bytes(rows, 32);
 }
 
-dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
-                                 int K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
-                                 void* stream) {
+static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, const void* logits,
+                                      const dflash_sampling* sampling, int K, int32_t* ids,
+                                      float* logp, void* ws, size_t ws_bytes, void* stream) {
   DFL_REQUIRE(rows >= 0, "rows must be >= 0");
   DFL_REQUIRE(vocab >= 1 && ld >= vocab, "need 1 <= vocab <= ld");
   DFL_REQUIRE(K >= 1 && K <= 32 && K <= vocab, "need 1 <= K <= min(32, vocab)");
   DFL_REQUIRE(dtype == DFLASH_F32 || dtype == DFLASH_BF16, "dtype must be F32 or BF16");
+  SampleSpec smp;
+  const dflash_status ps = parse_sampling(sampling, &smp);
+  if (ps) return ps;
   if (rows == 0) return DFLASH_OK;
   DFL_REQUIRE(logits && ids && logp, "null logits/ids/logp");
   const size_t need = dflash_topk_workspace_bytes(rows, vocab, K);
@@ -128,8 +144,23 @@ dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const v
   a.part = reinterpret_cast<float*>(w + ws_header_bytes() +
                                     align_up(sizeof(int) * (size_t)rows, 256));
   a.ids = ids; a.logp = logp;
+  a.inv_t = smp.inv_t; a.t = smp.t; a.seed = smp.seed; a.row0 = smp.row0;
   launch_topk(a, static_cast<cudaStream_t>(stream));
   return check_launch("logits_topk");
+}
+
+dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
+                                 int K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return logits_topk_impl(rows, vocab, ld, dtype, logits, nullptr, K, ids, logp, ws, ws_bytes,
+                          stream);
+}
+
+dflash_status dflash_logits_sample(int rows, int vocab, int ld, int dtype, const void* logits,
+                                   const dflash_sampling* sampling, int K, int32_t* ids,
+                                   float* logq, void* ws, size_t ws_bytes, void* stream) {
+  return logits_topk_impl(rows, vocab, ld, dtype, logits, sampling, K, ids, logq, ws, ws_bytes,
+                          stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -151,6 +182,23 @@ dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_log
                     depth, rank, mask};
   launch_tree_build(a, static_cast<cudaStream_t>(stream));
   return check_launch("ddtree_build");
+}
+
+dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* topk_ids,
+                                const int32_t* root_tok, int32_t* n_nodes, int32_t* tok,
+                                int32_t* parent, int32_t* depth, int32_t* rank, uint32_t* mask,
+                                void* stream) {
+  DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
+  DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
+  DFL_REQUIRE(K >= 1 && K <= 32, "need 1 <= K <= 32");
+  DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
+  if (n_req == 0) return DFLASH_OK;
+  DFL_REQUIRE(topk_ids && root_tok && n_nodes && tok && parent && depth && rank && mask,
+              "null pointer argument");
+  TreeBuildLaunch a{n_req, D, K, B, nullptr, topk_ids, root_tok, n_nodes, tok, parent,
+                    depth, rank, mask};
+  launch_chain_tree(a, static_cast<cudaStream_t>(stream));
+  return check_launch("chain_tree");
 }
 
 dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes, const int32_t* tok,

@@ -675,6 +675,48 @@ void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st) {
   launch_build(a, st);
 }
 
+// The vanilla DFlash chain in the tree layout: one CTA per request writes the
+// node arrays and the lower-triangular mask (row i: bits 0..i) of all B + 1
+// rows; rows past node n are -1 / zero.
+__global__ void chain_tree_kernel(int D, int K, int B, const int32_t* __restrict__ topk_ids,
+                                  const int32_t* __restrict__ root_tok,
+                                  int32_t* __restrict__ n_nodes, int32_t* __restrict__ tok,
+                                  int32_t* __restrict__ parent, int32_t* __restrict__ depth,
+                                  int32_t* __restrict__ rank, uint32_t* __restrict__ mask) {
+  const int req = blockIdx.x;
+  const int W1 = B + 1;
+  const int words = (W1 + 31) / 32;
+  const int n = min(D, B);
+  pdl_wait();
+  pdl_trigger();
+  const size_t nb = (size_t)req * W1;
+  for (int i = threadIdx.x; i < W1; i += blockDim.x) {
+    const bool live = i <= n;
+    tok[nb + i] = !live ? -1 : i == 0 ? root_tok[req] : topk_ids[((size_t)req * D + i - 1) * K];
+    parent[nb + i] = live ? i - 1 : -1;
+    depth[nb + i] = live ? i : -1;
+    rank[nb + i] = !live ? -1 : i == 0 ? 0 : 1;
+  }
+  uint32_t* mrow = mask + nb * words;
+  for (int e = threadIdx.x; e < W1 * words; e += blockDim.x) {
+    const int i = e / words, lo = (e % words) * 32;
+    uint32_t bits = 0u;
+    if (i <= n && i >= lo) {
+      const int top = min(i - lo, 31);   // bits 0..top of this word
+      bits = top == 31 ? 0xffffffffu : (2u << top) - 1u;
+    }
+    mrow[e] = bits;
+  }
+  if (threadIdx.x == 0) n_nodes[req] = n;
+}
+
+void launch_chain_tree(const TreeBuildLaunch& a, cudaStream_t st) {
+  if (a.n_req <= 0) return;
+  TraceScope ts("chain_tree", st);
+  launch_k(chain_tree_kernel, dim3(a.n_req), dim3(256), 0, st, a.D, a.K, a.B, a.topk_ids,
+           a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank, a.mask);
+}
+
 void launch_tree_accept(const TreeAcceptLaunch& a, cudaStream_t st) {
   if (a.n_req <= 0) return;
   const int warps = 4;

@@ -351,8 +351,8 @@ static dflash_status check_draft(const dflash_model* model, const dflash_cache* 
 // that run in the first GEMM launch, ahead of layer 0's QKV projection.
 static dflash_status draft_impl(const dflash_model* model, const dflash_cache* cache, int n_req,
                          const int32_t* anchor, const int32_t* ctx_len, int max_ctx, int L, int K,
-                         int32_t* topk_ids, float* topk_logp, float* logits, const CallCtx& c,
-                         const Step* pre, int n_pre) {
+                         const SampleSpec& smp, int32_t* topk_ids, float* topk_logp,
+                         float* logits, const CallCtx& c, const Step* pre, int n_pre) {
   const dflash_dims& d = model->dims;
   const WsLayout& W = c.L;
   const int R = n_req * L;
@@ -400,8 +400,9 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   };
   // With one 16-row tile the log-softmax / top-K rides in the LM head's
   // epilogue (per-CTA records, merged by a small kernel); the logits are then
-  // stored only if the caller asked for them.
-  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16;
+  // stored only if the caller asked for them.  Sampling rides there for K <= 8.
+  const bool sampling = smp.inv_t > 0.f;
+  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16 && !(sampling && K > 8);
   auto lm_step = [&]() {
     EpiParams el = epi_base(*model, R, d.vocab);
     el.kind = EPI_LOGITS;
@@ -413,6 +414,12 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
     // K <= 8: the LM-head chain also merges the records (no separate kernel)
     el.tk_ids = fused_topk && K <= 8 ? topk_ids : nullptr;
     el.tk_logp = fused_topk && K <= 8 ? topk_logp : nullptr;
+    if (fused_topk) {
+      el.tk_inv_t = smp.inv_t;
+      el.tk_t = smp.t;
+      el.tk_seed = smp.seed;
+      el.tk_row0 = smp.row0;
+    }
     return Step{&model->tm_lm, model->w.lm_head, xn, d.d, d.vocab, d.d, el};
   };
   {
@@ -514,16 +521,24 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   tk.counters = c.counters;
   tk.ids = topk_ids;
   tk.logp = topk_logp;
+  tk.inv_t = smp.inv_t;
+  tk.t = smp.t;
+  tk.seed = smp.seed;
+  tk.row0 = smp.row0;
   launch_topk(tk, c.st);
   return check_launch("top-K");
 }
 
 dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache, int n_req,
                                  const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
-                                 int L, int K, int32_t* topk_ids, float* topk_logp,
-                                 float* logits, void* ws, size_t ws_bytes, void* stream) {
+                                 int L, int K, const dflash_sampling* sampling,
+                                 int32_t* topk_ids, float* topk_logp, float* logits, void* ws,
+                                 size_t ws_bytes, void* stream) {
   dflash_status st = check_draft(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids,
                                  topk_logp);
+  if (st) return st;
+  SampleSpec smp;
+  st = parse_sampling(sampling, &smp);
   if (st) return st;
   const WsLayout W = ws_layout(*model, n_req, 0, L, K);
   if (!ws || ws_bytes < W.f)
@@ -531,19 +546,23 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
                      ws_bytes);
   CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
             static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
-  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
-                    logits, c, nullptr, 0);
+  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, smp, topk_ids,
+                    topk_logp, logits, c, nullptr, 0);
 }
 
 dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* cache, int n_req,
                                  int n_rows, const int32_t* row_off, const int32_t* pos0,
                                  const void* feats, const int32_t* anchor,
                                  const int32_t* ctx_len, int max_ctx, int L, int K,
-                                 int32_t* topk_ids, float* topk_logp, float* logits, void* ws,
-                                 size_t ws_bytes, void* stream) {
+                                 const dflash_sampling* sampling, int32_t* topk_ids,
+                                 float* topk_logp, float* logits, void* ws, size_t ws_bytes,
+                                 void* stream) {
   dflash_status st = check_inject(model, cache, n_req, n_rows, row_off, pos0, feats);
   if (st) return st;
   st = check_draft(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp);
+  if (st) return st;
+  SampleSpec smp;
+  st = parse_sampling(sampling, &smp);
   if (st) return st;
   const WsLayout W = ws_layout(*model, n_req, n_rows, L, K);
   if (!ws || ws_bytes < W.total)
@@ -552,20 +571,20 @@ dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* 
   CallCtx c{model, static_cast<char*>(ws), W, static_cast<cudaStream_t>(stream),
             static_cast<int*>(ws), reinterpret_cast<int*>(static_cast<char*>(ws) + W.counters)};
   if (n_rows == 0)
-    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
-                      logits, c, nullptr, 0);
+    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, smp, topk_ids,
+                      topk_logp, logits, c, nullptr, 0);
   Step inj[2];
   st = inject_steps(model, cache, n_req, n_rows, row_off, pos0, feats, c, inj);
   if (st) return st;
   // One GEMM launch for the injection and layer 0's QKV when they share the
   // activation row count (a chain runs over one row count).
   if (model->bf16 && n_rows == n_req * L)
-    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
-                      logits, c, inj, 2);
+    return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, smp, topk_ids,
+                      topk_logp, logits, c, inj, 2);
   st = run_chain(c, inj, 2, n_rows);
   if (st) return st;
-  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, topk_ids, topk_logp,
-                    logits, c, nullptr, 0);
+  return draft_impl(model, cache, n_req, anchor, ctx_len, max_ctx, L, K, smp, topk_ids,
+                    topk_logp, logits, c, nullptr, 0);
 }
 
 size_t dflash_linear_workspace_bytes(int M, int N, int K) {

@@ -83,6 +83,12 @@ struct EpiParams {
   // records merges them into ids / log-probabilities [n_req*(L-1)][K]
   int32_t* tk_ids;
   float* tk_logp;
+  // temperature sampling (tk_inv_t > 0, K <= 8): the lists rank the Gumbel
+  // scores l * tk_inv_t + G of counter row tk_row0 + output row, and the merge
+  // writes log q of each drawn token (see sampling.cuh)
+  float tk_inv_t, tk_t;
+  uint64_t tk_seed;
+  long long tk_row0;
 };
 
 // Record of a fused top-K: max, sum of exp(x - max), K values (desc), K ids.

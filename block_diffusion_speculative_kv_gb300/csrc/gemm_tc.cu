@@ -47,6 +47,7 @@
 #include "epilogue.cuh"
 #include "gemm.h"
 #include "ptx.cuh"
+#include "sampling.cuh"
 
 namespace dfl {
 
@@ -231,6 +232,7 @@ __device__ __forceinline__ void tk_update(const EpiParams& E, float* tk, int kpa
 // The same fold for K <= 8 with one lane per tile row: lane j walks the warp's
 // 32 columns of chunk row j in column order with its state in registers (one
 // exp per value, a register insert only when the value beats the K-th kept).
+// With sampling the list ranks Gumbel scores while (max, sum) covers logits.
 __device__ __forceinline__ void tk_update_rows(const EpiParams& E, float* tk, int kpad, int n_tile,
                                                const float* buf, const float* s_scale, int c0,
                                                int nr, int col0, int ew, int lane) {
@@ -254,17 +256,20 @@ __device__ __forceinline__ void tk_update_rows(const EpiParams& E, float* tk, in
   const float sc = s_scale[row];
   const float* src = buf + lane * kBufLd + ew * 32;
   const int ncol = min(32, E.N_feat - (col0 + ew * 32));
+  const bool smp = E.tk_inv_t > 0.f;
+  const long long grow = E.tk_row0 + (row / E.L * (E.L - 1) + row % E.L - 1);
   for (int q = 0; q < ncol; ++q) {
-    const float v = src[q] * sc;
-    if (v > m) {
-      sum = (m == -CUDART_INF_F ? 0.f : sum * exp2f((m - v) * 1.4426950408889634f)) + 1.f;
-      m = v;
+    const float l = src[q] * sc;
+    if (l > m) {
+      sum = (m == -CUDART_INF_F ? 0.f : sum * exp2f((m - l) * 1.4426950408889634f)) + 1.f;
+      m = l;
     } else {
-      sum += exp2f((v - m) * 1.4426950408889634f);
+      sum += exp2f((l - m) * 1.4426950408889634f);
     }
+    const int id = col0 + ew * 32 + q;
+    const float v = smp ? gumbel_score(l, E.tk_inv_t, E.tk_seed, grow, id) : l;
     if (v > thr) {
       // sorted insert (value desc; an equal value stays ahead: it came first)
-      const int id = col0 + ew * 32 + q;
 #pragma unroll
       for (int j = KM - 1; j >= 0; --j) {
         if (j < K) {
@@ -386,7 +391,9 @@ __device__ __forceinline__ void tk_row_merge(const EpiParams& E, int n_rec, int 
     const float lse = M + logf(S);
     if (lane < K) {
       E.tk_ids[(size_t)orow * K + lane] = id;
-      E.tk_logp[(size_t)orow * K + lane] = v - lse;
+      E.tk_logp[(size_t)orow * K + lane] =
+          E.tk_inv_t > 0.f ? sampled_logq(v, E.tk_t, E.tk_seed, E.tk_row0 + orow, id, lse)
+                           : v - lse;
     }
   }
   ptx::named_bar_sync(1, kEpiThreads);
@@ -1071,6 +1078,8 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
       if (ph[k].epi.tk_ids != nullptr && (k != n_phases - 1 || ph[k].epi.tk_K > 8))
         return set_error(DFLASH_ERR_INVALID_ARG,
                          "in-chain top-K merge: LM head must be the last phase, K <= 8");
+      if (ph[k].epi.tk_inv_t > 0.f && ph[k].epi.tk_ids == nullptr)
+        return set_error(DFLASH_ERR_INVALID_ARG, "fused sampling needs the in-chain merge");
     }
   for (int k = 0; k < n_phases; ++k) {
     const TcPlan pl = tc_plan(M_rows, ph[k].N, ph[k].K, G, p.tk_kpad);

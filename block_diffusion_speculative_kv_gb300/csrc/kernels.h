@@ -5,9 +5,20 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include "dflash.h"
+
 namespace dfl {
 
 // ---- log-softmax + top-K (topk.cu) ----
+// Temperature sampling of a top-K pass (inv_t == 0: plain top-K).
+struct SampleSpec {
+  float inv_t = 0.f, t = 0.f;
+  uint64_t seed = 0;
+  long long row0 = 0;
+};
+// Validates a dflash_sampling (NULL or temperature 0: plain top-K).
+dflash_status parse_sampling(const dflash_sampling* s, SampleSpec* out);
+
 struct TopkLaunch {
   const void* logits;
   int rows, vocab;
@@ -19,6 +30,11 @@ struct TopkLaunch {
   int* counters;  // [rows], zero on entry, left zero on exit
   int32_t* ids;
   float* logp;
+  // temperature sampling (inv_t > 0): rank Gumbel scores of counter rows
+  // row0 + r under seed; inv_t = 1/T, t = T.  Zero-initialised: plain top-K.
+  float inv_t, t;
+  uint64_t seed;
+  long long row0;
 };
 int topk_splits(int rows, int vocab);
 size_t topk_part_bytes(int rows, int splits);
@@ -43,6 +59,8 @@ struct TreeBuildLaunch {
 };
 size_t tree_build_smem_bytes(int D, int K, int B);
 void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st);
+// The chain of topk_ids[.][.][0] in the same layout (topk_logp unused).
+void launch_chain_tree(const TreeBuildLaunch& a, cudaStream_t st);
 
 struct TreeAcceptLaunch {
   int n_req, D, B;

@@ -12,9 +12,16 @@
 // split the CTA finishes the row; otherwise it writes a partial record and the
 // last CTA to arrive for the row (an atomic arrival counter, no waiting)
 // merges the partial records in split order and writes the result.
+//
+// With temperature sampling (DFlash page, 3.4.4) the lists rank Gumbel scores
+// l / T + G instead of logits, so the first entry is a sample from
+// softmax(l / T) and the K entries a draw without replacement; the running
+// (max, sum of exp) pair still covers the logits, and the log-probability
+// written for an entry is its logit (recovered from the score) minus lse.
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 #include <math_constants.h>
 
@@ -91,11 +98,24 @@ __device__ __forceinline__ void load_vec(const T* p, float (&x)[N]) {
   }
 }
 
-template <typename T, int KMAX, bool VECTOR>
+struct TopkSample {
+  float inv_t, t;      // 1/T and T (inv_t == 0: plain top-K)
+  uint64_t seed;
+  long long row0;      // counter row of logits row 0
+};
+
+template <bool SAMPLE>
+__device__ __forceinline__ float out_logp(float v, int id, int row, float lse,
+                                          const TopkSample& smp) {
+  if constexpr (SAMPLE) return sampled_logq(v, smp.t, smp.seed, smp.row0 + row, id, lse);
+  else return v - lse;
+}
+
+template <typename T, int KMAX, bool VECTOR, bool SAMPLE>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int K,
             int splits, int chunk, TopkPart part, int* __restrict__ counters,
-            int32_t* __restrict__ ids_out, float* __restrict__ logp_out) {
+            int32_t* __restrict__ ids_out, float* __restrict__ logp_out, TopkSample smp) {
   constexpr int VN = VECTOR ? Vec<T>::N : 1;
   __shared__ float s_v[KMAX];
   __shared__ int s_i[KMAX];
@@ -123,7 +143,8 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
   // at or above it, so anything strictly below cannot be in the row's top-K;
   // it is refreshed after every step of the warp-uniform main loop.
   float wthr = -CUDART_INF_F;
-  auto consume = [&](const float* x, int n, int id0) {
+  // x: logits (for the log-sum-exp), y: the values ranked (logits or scores)
+  auto consume = [&](const float* x, const float* y, int n, int id0) {
     float vmax = x[0];
 #pragma unroll
     for (int e = 1; e < VN; ++e) if (e < n) vmax = fmaxf(vmax, x[e]);
@@ -137,7 +158,18 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
     }
 #pragma unroll
     for (int e = 0; e < VN; ++e)
-      if (e < n && x[e] > thr && x[e] >= wthr) list_insert<KMAX>(tv, ti, K, x[e], id0 + e, thr);
+      if (e < n && y[e] > thr && y[e] >= wthr) list_insert<KMAX>(tv, ti, K, y[e], id0 + e, thr);
+  };
+  auto rank_values = [&](const float* x, float* y, int n, int id0) {
+#pragma unroll
+    for (int e = 0; e < VN; ++e) {
+      if constexpr (SAMPLE)
+        y[e] = (e < n && x[e] != -CUDART_INF_F)
+                   ? gumbel_score(x[e], smp.inv_t, smp.seed, smp.row0 + row, id0 + e)
+                   : -CUDART_INF_F;
+      else
+        y[e] = x[e];
+    }
   };
 
   if (v1 > v0) {
@@ -161,6 +193,9 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
           for (int e = 0; e < VN; ++e) x[u][e] = -CUDART_INF_F;
         }
       }
+      float y[U][VN];
+#pragma unroll
+      for (int u = 0; u < U; ++u) rank_values(x[u], y[u], VN, v0 + (kb + u * 32 + lane) * VN);
       if (first) {
         // seed: the K-th largest of the lanes' maxima over this first step is
         // met or beaten by K distinct values, so it bounds the row's K-th value
@@ -168,7 +203,7 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int e = 0; e < VN; ++e) lm = fmaxf(lm, x[u][e]);
+          for (int e = 0; e < VN; ++e) lm = fmaxf(lm, y[u][e]);
         float seed = -CUDART_INF_F;
         for (int r = 0; r < K; ++r) {
           const uint32_t mb = __reduce_max_sync(0xffffffffu, ordered_bits(lm));
@@ -181,7 +216,7 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
       }
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) consume(x[u], VN, v0 + (kb + u * 32 + lane) * VN);
+        if (ok[u]) consume(x[u], y[u], VN, v0 + (kb + u * 32 + lane) * VN);
       wthr = fmaxf(wthr, from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(thr))));
     }
     const int tail0 = v0 + nvec * VN;
@@ -190,7 +225,9 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
       x[0] = to_f32<T>(rp[tail0 + tid]);
 #pragma unroll
       for (int e = 1; e < VN; ++e) x[e] = -CUDART_INF_F;
-      consume(x, 1, tail0 + tid);
+      float y[VN];
+      rank_values(x, y, 1, tail0 + tid);
+      consume(x, y, 1, tail0 + tid);
     }
   }
 
@@ -236,7 +273,7 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
       const float lse = cm + logf(cs);
       for (int r = lane; r < K; r += 32) {
         ids_out[(long long)row * K + r] = s_i[r];
-        logp_out[(long long)row * K + r] = s_v[r] - lse;
+        logp_out[(long long)row * K + r] = out_logp<SAMPLE>(s_v[r], s_i[r], row, lse, smp);
       }
     }
     return;
@@ -280,14 +317,14 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
       if (own && p < K && bv == v && bi == i) ++p;
       if (lane == 0) {
         ids_out[(long long)row * K + r] = bi;
-        logp_out[(long long)row * K + r] = bv - lse;
+        logp_out[(long long)row * K + r] = out_logp<SAMPLE>(bv, bi, row, lse, smp);
       }
     }
   }
   if (lane == 0) counters[row] = 0;
 }
 
-template <typename T, int KMAX>
+template <typename T, int KMAX, bool SAMPLE>
 void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
   const int VN = Vec<T>::N;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(a.logits) % 16) == 0) &&
@@ -295,16 +332,17 @@ void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
   int chunk = ceil_div(a.vocab, a.splits);
   chunk = ceil_div(chunk, 8) * 8;
   TopkPart part{a.part, 2 + 2 * KMAX};
+  TopkSample smp{a.inv_t, a.t, a.seed, a.row0};
   dim3 grid(a.rows * a.splits);
-  TraceScope ts("lse_topk", st);
+  TraceScope ts(SAMPLE ? "lse_sample" : "lse_topk", st);
   if (vec_ok) {
-    launch_k(topk_kernel<T, KMAX, true>, grid, dim3(kTopkThreads), 0, st,
+    launch_k(topk_kernel<T, KMAX, true, SAMPLE>, grid, dim3(kTopkThreads), 0, st,
              static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
-             a.counters, a.ids, a.logp);
+             a.counters, a.ids, a.logp, smp);
   } else {
-    launch_k(topk_kernel<T, KMAX, false>, grid, dim3(kTopkThreads), 0, st,
+    launch_k(topk_kernel<T, KMAX, false, SAMPLE>, grid, dim3(kTopkThreads), 0, st,
              static_cast<const T*>(a.logits), a.rows, a.vocab, a.ld, a.K, a.splits, chunk, part,
-             a.counters, a.ids, a.logp);
+             a.counters, a.ids, a.logp, smp);
   }
   (void)VN;
 }
@@ -412,12 +450,23 @@ size_t topk_part_bytes(int rows, int splits) {
 void launch_topk(const TopkLaunch& a, cudaStream_t st) {
   if (a.rows <= 0) return;
   const bool k8 = a.K <= 8;
+  const bool smp = a.inv_t > 0.f;
   if (a.dtype == DFLASH_BF16) {
-    if (k8) launch_topk_t<__nv_bfloat16, 8>(a, st);
-    else launch_topk_t<__nv_bfloat16, 32>(a, st);
+    if (smp) {
+      if (k8) launch_topk_t<__nv_bfloat16, 8, true>(a, st);
+      else launch_topk_t<__nv_bfloat16, 32, true>(a, st);
+    } else {
+      if (k8) launch_topk_t<__nv_bfloat16, 8, false>(a, st);
+      else launch_topk_t<__nv_bfloat16, 32, false>(a, st);
+    }
   } else {
-    if (k8) launch_topk_t<float, 8>(a, st);
-    else launch_topk_t<float, 32>(a, st);
+    if (smp) {
+      if (k8) launch_topk_t<float, 8, true>(a, st);
+      else launch_topk_t<float, 32, true>(a, st);
+    } else {
+      if (k8) launch_topk_t<float, 8, false>(a, st);
+      else launch_topk_t<float, 32, false>(a, st);
+    }
   }
 }
 

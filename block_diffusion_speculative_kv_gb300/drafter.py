@@ -102,20 +102,23 @@ class Drafter:
     def draft_block(self, anchor: torch.Tensor, ctx_len: torch.Tensor, max_ctx: int,
                     topk_ids: torch.Tensor, topk_logp: torch.Tensor,
                     logits: Optional[torch.Tensor] = None, n_req: Optional[int] = None,
-                    L: Optional[int] = None, K: Optional[int] = None, stream=None):
+                    L: Optional[int] = None, K: Optional[int] = None, sampling=None,
+                    stream=None):
+        """sampling: None (top-K by logit) or (temperature, seed[, row_offset])."""
         n_req = self.n_req if n_req is None else n_req
         L = self.L if L is None else L
         K = self.K if K is None else K
         bd._check(bd.lib().dflash_draft_block(
             self.handle, C.byref(self.cache_struct), n_req, bd._ptr(anchor), bd._ptr(ctx_len),
-            max_ctx, L, K, bd._ptr(topk_ids), bd._ptr(topk_logp), bd._ptr(logits),
-            bd._ptr(self.ws), self.ws.numel(), bd._stream(stream)))
+            max_ctx, L, K, bd.sampling_arg(sampling), bd._ptr(topk_ids), bd._ptr(topk_logp),
+            bd._ptr(logits), bd._ptr(self.ws), self.ws.numel(), bd._stream(stream)))
 
     def draft_cycle(self, feats: torch.Tensor, row_off: torch.Tensor, pos0: torch.Tensor,
                     anchor: torch.Tensor, ctx_len: torch.Tensor, max_ctx: int,
                     topk_ids: torch.Tensor, topk_logp: torch.Tensor,
                     logits: Optional[torch.Tensor] = None, n_req: Optional[int] = None,
-                    L: Optional[int] = None, K: Optional[int] = None, stream=None):
+                    L: Optional[int] = None, K: Optional[int] = None, sampling=None,
+                    stream=None):
         """inject_kv followed by draft_block, as one call (same results)."""
         n_req = self.n_req if n_req is None else n_req
         L = self.L if L is None else L
@@ -123,8 +126,8 @@ class Drafter:
         bd._check(bd.lib().dflash_draft_cycle(
             self.handle, C.byref(self.cache_struct), n_req, feats.shape[0], bd._ptr(row_off),
             bd._ptr(pos0), bd._ptr(feats), bd._ptr(anchor), bd._ptr(ctx_len), max_ctx, L, K,
-            bd._ptr(topk_ids), bd._ptr(topk_logp), bd._ptr(logits), bd._ptr(self.ws),
-            self.ws.numel(), bd._stream(stream)))
+            bd.sampling_arg(sampling), bd._ptr(topk_ids), bd._ptr(topk_logp), bd._ptr(logits),
+            bd._ptr(self.ws), self.ws.numel(), bd._stream(stream)))
 
     def read_status(self) -> int:
         return bd.read_status(self.ws)

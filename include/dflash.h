@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 1
+#define DFLASH_ABI_VERSION 2
 #define DFLASH_MAX_LAYERS 16
 
 typedef enum {
@@ -66,6 +66,26 @@ typedef enum {
 } dflash_status;
 
 typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+
+/* Temperature of the drafted tokens (DFlash page, 3.4.4: argmax at temperature
+ * 0, a sample from softmax(logits) at temperature 1).  A top-K pass given a
+ * dflash_sampling with temperature T > 0 ranks, instead of the logits l_v, the
+ * Gumbel scores s_v = l_v * f32(1/T) + G_v (an fp32 multiply then an fp32
+ * add), G_v = -log(-log U_v) in fp32, and keeps the K best (score desc, token
+ * id asc): entry 0 is a sample from softmax(l / T), the K entries a draw
+ * without replacement.  U_v: the SplitMix64 generator (Steele, Lea, Flood,
+ * 2014) seeded with `seed`; element v of counter row c takes output number
+ * (c << 32 | v) + 1 and U = (its top 23 bits + 1/2) / 2^23.  Output row r of a
+ * call uses counter row row_offset + r.  The log-probabilities written are
+ * log q(token) = logit - logsumexp(row), the logit recovered from the score as
+ * (s - G) * T (exact to the fp32 rounding of s).  A NULL pointer or T == 0
+ * selects the plain top-K (ranked by logit).  Requires T == 0 or
+ * 1e-6 <= T <= 1e6. */
+typedef struct dflash_sampling {
+  float temperature;
+  uint64_t seed;
+  int64_t row_offset;
+} dflash_sampling;
 
 /* Drafter shape and the readings the pages leave open.
  * - Pre-norm RMSNorm: x / sqrt(mean(x^2) + rms_eps) * gain, before attention,
@@ -188,7 +208,8 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
 
 /* Steps a3 - a6: one drafter pass over the block [anchor, mask x (L-1)] of each
  * request, then per-position log-softmax and top-K (DFlash page, 3.4.4; DDTree
- * page, 3.4.2: q_i = softmax(l_i)).
+ * page, 3.4.2: q_i = softmax(l_i)), or, with `sampling` at T > 0, the Gumbel
+ * draw of dflash_sampling (output row r = request * (L-1) + position - 1).
  *   anchor    int32 [n_req] (device) the bonus token of each request
  *   ctx_len   int32 [n_req] (device) context entries of each request in the
  *             cache, 0 <= ctx_len[r] <= max_ctx <= cache->cap
@@ -202,8 +223,8 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
  */
 dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* cache,
                                  int n_req, const int32_t* anchor, const int32_t* ctx_len,
-                                 int max_ctx, int L, int K, int32_t* topk_ids,
-                                 float* topk_logp, float* logits,
+                                 int max_ctx, int L, int K, const dflash_sampling* sampling,
+                                 int32_t* topk_ids, float* topk_logp, float* logits,
                                  void* ws, size_t ws_bytes, void* stream);
 
 /* Steps a1 - a6 in one call: dflash_inject_kv(n_rows, row_off, pos0, feats)
@@ -218,8 +239,9 @@ dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* 
                                  int n_req, int n_rows, const int32_t* row_off,
                                  const int32_t* pos0, const void* feats,
                                  const int32_t* anchor, const int32_t* ctx_len, int max_ctx,
-                                 int L, int K, int32_t* topk_ids, float* topk_logp,
-                                 float* logits, void* ws, size_t ws_bytes, void* stream);
+                                 int L, int K, const dflash_sampling* sampling,
+                                 int32_t* topk_ids, float* topk_logp, float* logits, void* ws,
+                                 size_t ws_bytes, void* stream);
 
 /* Step a6 on its own: log-softmax + top-K over given logits rows (DDTree page,
  * 3.4.2 and Lemma 1 in 3.4.4: only the top-K tokens per depth are needed).
@@ -232,6 +254,16 @@ size_t dflash_topk_workspace_bytes(int rows, int vocab, int K);
 dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
                                  int K, int32_t* ids, float* logp,
                                  void* ws, size_t ws_bytes, void* stream);
+
+/* Step a6 with temperature sampling (DFlash page, 3.4.4; see dflash_sampling):
+ * the same pass as dflash_logits_topk ranking Gumbel scores, so ids[r][0] is a
+ * sample from softmax(logits[r] / T) and ids[r][0..K) a draw without
+ * replacement; logq[r][k] = log q(ids[r][k]).  Same arguments, limits and
+ * workspace as dflash_logits_topk; sampling NULL or T == 0 is
+ * dflash_logits_topk. */
+dflash_status dflash_logits_sample(int rows, int vocab, int ld, int dtype, const void* logits,
+                                   const dflash_sampling* sampling, int K, int32_t* ids,
+                                   float* logq, void* ws, size_t ws_bytes, void* stream);
 
 /* Step a6 for callers that cannot provide a workspace.  The pages have no
  * counterpart: this variant exists for callers that cannot allocate device
@@ -274,6 +306,20 @@ dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_log
                            const int32_t* topk_ids, const int32_t* root_tok,
                            int32_t* n_nodes, int32_t* tok, int32_t* parent,
                            int32_t* depth, int32_t* rank, uint32_t* mask, void* stream);
+
+/* The vanilla DFlash draft as a tree (DFlash page, 3.4.1 and 3.4.4): the chain
+ * root -> drafted token of position 1 -> ... -> position D, in ddtree_build's
+ * output layout so that tree attention and ddtree_accept serve both drafters.
+ * Node d (1 <= d <= n = min(D, B)) holds topk_ids[r][d-1][0] (the argmax, or
+ * the sample of a dflash_sampling call), parent d-1, depth d, rank 1; mask row
+ * i has bits 0..i.  The walk over a chain accepts the longest prefix the
+ * target agrees with.  topk_ids int32 [n_req][D][K]; outputs as ddtree_build
+ * (entries past node n are -1, mask rows 0).  Requires 1 <= D <= 16,
+ * 1 <= K <= 32, 0 <= B <= 1024.  Needs no workspace. */
+dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* topk_ids,
+                                const int32_t* root_tok, int32_t* n_nodes, int32_t* tok,
+                                int32_t* parent, int32_t* depth, int32_t* rank, uint32_t* mask,
+                                void* stream);
 
 /* Step a8: greedy verifier walk (DDTree page, 3.4.5).  From the root, while the
  * current node has a child whose token equals target_tok[current], move to it.

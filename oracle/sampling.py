@@ -19,9 +19,13 @@ Readings (the page names no sampler):
   infinite);
 * the decision is taken in float32: s_v = f32(l_v) * f32(1 / T) + G_v with G
   evaluated in float32, ties to the smaller token id; T = 0 is the argmax;
+* the K best scores (score desc, id asc) are a draw of K tokens without
+  replacement (the Gumbel-top-k property), and the log-probability reported
+  for a drawn token is log softmax(l)[token];
 * the chain tree of a drafted block: node 0 the anchor, node d the token of
-  position d, each node the parent of the next, rank 0 (not a top-K rank),
-  the ancestor mask of a chain (row i: bits 0..i).
+  position d (rank 1: entry 0 of the position's list), each node the parent
+  of the next, the ancestor mask of a chain (row i: bits 0..i); a budget
+  B < D keeps the first B positions.
 """
 from __future__ import annotations
 
@@ -81,11 +85,23 @@ def sample_rows(logits, temperature: float, seed: int, row_offset: int = 0) -> n
     return out
 
 
+def gumbel_topk(logits_row, temperature: float, seed: int, row: int, K: int):
+    """The K best Gumbel scores of one row: ids (score desc, id asc) and the
+    log-probabilities log softmax(l) of those ids (float64)."""
+    l = np.asarray(logits_row, dtype=np.float32)
+    s = scores(l, temperature, seed, row)
+    order = np.lexsort((np.arange(s.shape[0]), -s.astype(np.float64)))[:K]
+    l64 = l.astype(np.float64)
+    m = l64.max()
+    lse = m + np.log(np.sum(np.exp(l64 - m)))
+    return order.astype(np.int32), l64[order] - lse
+
+
 def chain_tree(root_tok: int, tokens, B: int):
-    """Flattened chain tree of D = len(tokens) drafted tokens in buffers of
-    width B + 1 (B >= D): tok, parent, depth, rank, mask like the DDTree
-    oracle's build_tree output, n_nodes = D."""
-    D = len(tokens)
+    """Flattened chain tree of the drafted tokens in buffers of width B + 1:
+    tok, parent, depth, rank, mask like the DDTree oracle's build_tree output,
+    n_nodes = min(len(tokens), B)."""
+    D = min(len(tokens), B)
     width = B + 1
     tok = np.full(width, -1, dtype=np.int32)
     parent = np.full(width, -1, dtype=np.int32)
@@ -93,7 +109,7 @@ def chain_tree(root_tok: int, tokens, B: int):
     rank = np.full(width, -1, dtype=np.int32)
     tok[0], depth[0], rank[0] = root_tok, 0, 0
     for d in range(1, D + 1):
-        tok[d], parent[d], depth[d], rank[d] = tokens[d - 1], d - 1, d, 0
+        tok[d], parent[d], depth[d], rank[d] = tokens[d - 1], d - 1, d, 1
     words = (width + 31) // 32
     mask = np.zeros((width, words), dtype=np.uint32)
     for i in range(D + 1):

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(libpath):
 def test_binding_covers_every_declared_symbol(libpath):
     assert sorted(binding.exported_symbols()) == _declared()
     lib = binding.lib()
-    assert lib.dflash_abi_version() == 1
+    assert lib.dflash_abi_version() == 2
 
 
 def test_host_validation_needs_no_gpu(libpath):
@@ -54,3 +54,12 @@ def test_host_validation_needs_no_gpu(libpath):
     assert lib.dflash_topk_workspace_bytes(4, 100, 0) == 0
     # zero-sized requests are valid no-ops
     assert lib.ddtree_build(0, 8, 8, 64, *([None] * 9), None) == 0
+    assert lib.dflash_chain_tree(1, 0, 1, 64, *([None] * 8), None) == 1
+    assert lib.dflash_chain_tree(0, 4, 1, 64, *([None] * 8), None) == 0
+    # a negative or huge temperature is rejected on the host; 0 is the top-K
+    for t in (-1.0, 1e-9, 1e9, float("nan")):
+        s = ctypes.byref(binding.Sampling(t, 1, 0))
+        assert lib.dflash_logits_sample(0, 100, 100, 0, None, s, 1, None, None, None, 0,
+                                        None) == 1, t
+    s = ctypes.byref(binding.Sampling(0.0, 1, 0))
+    assert lib.dflash_logits_sample(0, 100, 100, 0, None, s, 1, None, None, None, 0, None) == 0

@@ -49,6 +49,30 @@ def test_gumbel_max_draws_follow_softmax():
     assert scipy.stats.chisquare(counts, p2 * n)[1] > 1e-4
 
 
+def test_gumbel_top2_is_a_draw_without_replacement():
+    # P(first = a, second = b) = p_a * p_b / (1 - p_a) over the 6 ordered pairs
+    logits = np.array([0.7, -0.3, 0.1], dtype=np.float32)
+    n = 12000
+    pairs = np.zeros((3, 3), dtype=np.int64)
+    for r in range(n):
+        ids, _ = osm.gumbel_topk(logits, 1.0, 17, r, 2)
+        pairs[ids[0], ids[1]] += 1
+    p = np.exp(logits.astype(np.float64))
+    p /= p.sum()
+    obs, exp = [], []
+    for a in range(3):
+        for b in range(3):
+            if a != b:
+                obs.append(pairs[a, b])
+                exp.append(n * p[a] * p[b] / (1 - p[a]))
+    assert np.trace(pairs) == 0
+    assert scipy.stats.chisquare(obs, exp)[1] > 1e-4
+    # entry 0 is the single-token sample, and the log-probabilities are exact
+    ids, lq = osm.gumbel_topk(logits, 1.0, 17, 5, 3)
+    assert ids[0] == osm.sample_rows(logits[None], 1.0, 17, row_offset=5)[0]
+    assert np.allclose(lq, np.log(p[ids]), atol=1e-12)
+
+
 def test_limits_and_ties():
     rng = np.random.default_rng(0)
     logits = rng.normal(size=(6, 50)).astype(np.float32) * 5
@@ -63,6 +87,11 @@ def test_chain_tree_mask_and_walk():
     t = osm.chain_tree(9, tokens, B=6)
     assert t["n_nodes"] == 4
     assert np.array_equal(t["mask"], odt.tree_mask(t["parent"], 4, 6))
+    assert list(t["rank"][:6]) == [0, 1, 1, 1, 1, -1]
+    # a budget below D keeps the first B positions
+    short = osm.chain_tree(9, tokens, B=2)
+    assert short["n_nodes"] == 2 and list(short["tok"]) == [9, 11, 12]
+    assert np.array_equal(short["mask"], odt.tree_mask(short["parent"], 2, 2))
     # the walk on a chain accepts the longest matching prefix (linear acceptance)
     for k in range(5):
         target = np.full(7, -1, dtype=np.int32)
