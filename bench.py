@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
                                        "topk_b1", "tree_stress", "tree_b1", "tree_attention",
-                                       "chain_sweep"],
+                                       "chain_sweep", "budget_sweep"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -426,10 +426,62 @@ def run_chain_sweep(args):
                       "rows": rows}))
 
 
+def run_budget_sweep(args):
+    """DDTree node budget B = 16 .. 1024 on the Qwen3-8B-shaped batch-1 drafter
+    (8192 context slots), with the workload's K = 8 and with Lemma 1's exact
+    K = B.  Per (B, K): microseconds per full cycle (inject + draft + top-K +
+    tree), for the top-K alone over the cycle's 15 rows of fp32 logits, and for
+    the tree build alone; the tree's node count and depth."""
+    cyc = Cycle(2)
+    bd, wl = cyc.bd, cyc.wl
+    L, D = wl.L, wl.L - 1
+    i32 = dict(dtype=torch.int32, device="cuda")
+    nbytes = int(bd.lib().dflash_workspace_bytes(cyc.dr.handle, 1, L, L, 1024))
+    cyc.dr.ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    logits = torch.empty(1, D, wl.shape.vocab, dtype=torch.float32, device="cuda")
+    cyc.dr.draft_cycle(cyc.feats, cyc.row_off, cyc.pos0, cyc.anchor, cyc.ctx_len, cyc.max_ctx,
+                       cyc.ids, cyc.lp, logits)
+    lg2 = logits.reshape(D, wl.shape.vocab)
+    rows = []
+    for B in (16, 32, 64, 128, 256, 512, 1024):
+        for K in sorted({wl.K, B}):
+            ids = torch.empty(1, D, K, **i32)
+            lq = torch.empty(1, D, K, dtype=torch.float32, device="cuda")
+            tree = bd.tree_buffers(1, B, "cuda")
+            tws = torch.zeros(bd.topk_workspace_bytes(D, wl.shape.vocab, K), dtype=torch.uint8,
+                              device="cuda")
+
+            def cycle_fn():
+                cyc.dr.draft_cycle(cyc.feats, cyc.row_off, cyc.pos0, cyc.anchor, cyc.ctx_len,
+                                   cyc.max_ctx, ids, lq, K=K)
+                bd.ddtree_build(lq, ids, cyc.anchor, B, *tree)
+
+            def topk_fn():
+                bd.logits_topk(lg2, K, ids.reshape(D, K), lq.reshape(D, K), tws)
+
+            def tree_fn():
+                bd.ddtree_build(lq, ids, cyc.anchor, B, *tree)
+            w = max(args.warmup, 3)
+            ms_c, clocks = timed_region(cycle_fn, args.steps, w, 1)
+            ms_k, _ = timed_region(topk_fn, args.steps, w, 1)
+            ms_t, _ = timed_region(tree_fn, args.steps, w, 1)
+            assert cyc.dr.read_status() == 0
+            rows.append({"B": B, "K": K, "us_cycle": round(ms_c * 1e3 / args.steps, 1),
+                         "us_topk": round(ms_k * 1e3 / args.steps, 2),
+                         "us_tree": round(ms_t * 1e3 / args.steps, 2),
+                         "n_nodes": int(tree[0].item()), "depth": int(tree[3].max().item()),
+                         "max_rank": int(tree[4].max().item()),
+                         "sm_mhz": clocks.get("sm_mhz") if isinstance(clocks, dict) else None})
+    print(json.dumps({"case": "budget_sweep", "workload": wl.name, "steps": args.steps,
+                      "rows": rows}))
+
+
 def run_case(args):
     """One kernel on its own, launched back to back (inputs larger than L2)."""
     if args.case == "chain_sweep":
         return run_chain_sweep(args)
+    if args.case == "budget_sweep":
+        return run_budget_sweep(args)
     from block_diffusion_speculative_kv_gb300 import binding as bd
     from block_diffusion_speculative_kv_gb300 import synth
     from block_diffusion_speculative_kv_gb300.configs import WORKLOADS

@@ -115,9 +115,9 @@ dflash_status dflash_read_status(void* ws, int* device_status, void* stream) {
 // Step a6 standalone: log-softmax + top-K over given logits.
 // ---------------------------------------------------------------------------
 size_t dflash_topk_workspace_bytes(int rows, int vocab, int K) {
-  if (rows < 0 || vocab <= 0 || K < 1 || K > 32) return 0;
-  return ws_header_bytes() + align_up(sizeof(int) * (size_t)rows, 256) +
-         topk_part_bytes(rows, 32);
+  if (rows < 0 || vocab <= 0 || K < 1 || K > 1024) return 0;
+  const size_t part = K > 32 ? topk_large_part_bytes(rows, vocab, K) : topk_part_bytes(rows, 32);
+  return ws_header_bytes() + align_up(sizeof(int) * (size_t)rows, 256) + part;
 }
 
 static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, const void* logits,
@@ -125,11 +125,16 @@ static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, co
                                       float* logp, void* ws, size_t ws_bytes, void* stream) {
   DFL_REQUIRE(rows >= 0, "rows must be >= 0");
   DFL_REQUIRE(vocab >= 1 && ld >= vocab, "need 1 <= vocab <= ld");
-  DFL_REQUIRE(K >= 1 && K <= 32 && K <= vocab, "need 1 <= K <= min(32, vocab)");
+  DFL_REQUIRE(K >= 1 && K <= 1024 && K <= vocab, "need 1 <= K <= min(1024, vocab)");
   DFL_REQUIRE(dtype == DFLASH_F32 || dtype == DFLASH_BF16, "dtype must be F32 or BF16");
   SampleSpec smp;
   const dflash_status ps = parse_sampling(sampling, &smp);
   if (ps) return ps;
+  if (smp.inv_t > 0.f && K > 32)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "sampling draws at most 32 tokens per row");
+  if (K > 32 && topk_large_merge_smem(vocab, K) > 200 * 1024)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "K = %d is too large for a vocabulary of %d", K,
+                     vocab);
   if (rows == 0) return DFLASH_OK;
   DFL_REQUIRE(logits && ids && logp, "null logits/ids/logp");
   const size_t need = dflash_topk_workspace_bytes(rows, vocab, K);
@@ -145,7 +150,12 @@ static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, co
                                     align_up(sizeof(int) * (size_t)rows, 256));
   a.ids = ids; a.logp = logp;
   a.inv_t = smp.inv_t; a.t = smp.t; a.seed = smp.seed; a.row0 = smp.row0;
-  launch_topk(a, static_cast<cudaStream_t>(stream));
+  if (K > 32) {
+    const dflash_status ls = launch_topk_large(a, a.part, static_cast<cudaStream_t>(stream));
+    if (ls) return ls;
+  } else {
+    launch_topk(a, static_cast<cudaStream_t>(stream));
+  }
   return check_launch("logits_topk");
 }
 
@@ -172,7 +182,7 @@ dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_log
                            uint32_t* mask, void* stream) {
   DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
   DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
-  DFL_REQUIRE(K >= 1 && K <= 32, "need 1 <= K <= 32");
+  DFL_REQUIRE(K >= 1 && K <= 1024, "need 1 <= K <= 1024");
   DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
   if (n_req == 0) return DFLASH_OK;
   DFL_REQUIRE(topk_logp && topk_ids && root_tok && n_nodes && tok && parent && depth && rank &&
@@ -190,7 +200,7 @@ dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* t
                                 void* stream) {
   DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
   DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
-  DFL_REQUIRE(K >= 1 && K <= 32, "need 1 <= K <= 32");
+  DFL_REQUIRE(K >= 1 && K <= 1024, "need 1 <= K <= 1024");
   DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
   if (n_req == 0) return DFLASH_OK;
   DFL_REQUIRE(topk_ids && root_tok && n_nodes && tok && parent && depth && rank && mask,

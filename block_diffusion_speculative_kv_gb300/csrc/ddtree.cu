@@ -35,6 +35,7 @@ namespace dfl {
 namespace {
 
 constexpr int kBuildWarps = 4;
+constexpr int kBuildSmemMax = 200 * 1024;
 constexpr uint32_t kSeqMax = (1u << 21) - 1;   // creation counter field
 
 __device__ __forceinline__ uint64_t make_key(float score, uint32_t seq, int reg, int lane) {
@@ -49,7 +50,7 @@ __device__ __forceinline__ uint32_t pack_info(int parent, int depth, int rank) {
 
 struct WarpSmem {
   float* lp;        // [D*K]
-  int* ids;         // [D*K]
+  const int32_t* ids;   // [D*K] the request's token ids, read from global memory
   uint32_t* node;   // [B+1][4]: tok, parent, depth, rank
   uint4* slot;      // [B+1]: info (parent | depth << 11 | rank << 16), parent score,
                     //        next sibling's score, log-prob of the first child
@@ -62,7 +63,6 @@ __host__ __device__ inline size_t build_warp_bytes(int D, int K, int B) {
   b += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
   b += align_up(sizeof(uint4) * (B + 1), 16);
   b += align_up(sizeof(float) * D * K, 16);
-  b += align_up(sizeof(int) * D * K, 16);
   b += align_up(sizeof(uint32_t) * 32 * W, 16);
   return b;
 }
@@ -141,7 +141,7 @@ __device__ int seq_build(const WarpSmem& sm, int D, int K, int B, int lane, int3
     const float wscore = from_ordered_bits(mhi);
     const int p = winfo & 0x7FF;
     const int d = (winfo >> 11) & 0x1F;
-    const int r = (winfo >> 16) & 0x3F;
+    const int r = (winfo >> 16) & 0xFFFF;
     ++n;
     const bool has_sib = r < K;
     const bool has_child = d < D;
@@ -165,8 +165,8 @@ __device__ int seq_build(const WarpSmem& sm, int D, int K, int B, int lane, int3
     const bool is_o = has_child && lane == co;
     if (lane == 0)
       *reinterpret_cast<uint4*>(sm.node + 4 * n) =
-          make_uint4(static_cast<uint32_t>(sm.ids[(d - 1) * K + (r - 1)]),
-                     static_cast<uint32_t>(p), static_cast<uint32_t>(d), static_cast<uint32_t>(r));
+          make_uint4(0u, static_cast<uint32_t>(p), static_cast<uint32_t>(d),
+                     static_cast<uint32_t>(r));
     if (is_w && has_sib) sm.slot[wi * 32 + w] = adv;
     if (is_o) sm.slot[cslot] = opn;
 #pragma unroll
@@ -179,7 +179,12 @@ __device__ int seq_build(const WarpSmem& sm, int D, int K, int B, int lane, int3
     brec = load_rec();
   }
   __syncwarp();
-
+  // the nodes' tokens, looked up once the pops are done (many loads in flight)
+  for (int i = lane + 1; i <= n; i += 32) {
+    const uint32_t* nd = sm.node + 4 * i;
+    sm.node[4 * i] = static_cast<uint32_t>(sm.ids[(nd[2] - 1) * K + (nd[3] - 1)]);
+  }
+  __syncwarp();
   return n;
 }
 
@@ -269,12 +274,13 @@ __device__ __forceinline__ WarpSmem carve_warp_smem(unsigned char* base, int D, 
   sm.node = reinterpret_cast<uint32_t*>(base + off); off += align_up(sizeof(uint32_t) * 4 * (B + 1), 16);
   sm.slot = reinterpret_cast<uint4*>(base + off); off += align_up(sizeof(uint4) * (B + 1), 16);
   sm.lp = reinterpret_cast<float*>(base + off); off += align_up(sizeof(float) * D * K, 16);
-  sm.ids = reinterpret_cast<int*>(base + off); off += align_up(sizeof(int) * D * K, 16);
+  sm.ids = nullptr;
   sm.stage = reinterpret_cast<uint32_t*>(base + off);
   return sm;
 }
 
-// One request per warp; NSL = key registers per lane, 32 * NSL >= B + 1 slots.
+// One request per warp (blockDim.x / 32 requests per CTA); NSL = key registers
+// per lane, 32 * NSL >= B + 1 slots.
 template <int NSL>
 __global__ void __launch_bounds__(kBuildWarps * 32)
 ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
@@ -285,14 +291,14 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
-  const int req = blockIdx.x * kBuildWarps + wib;
+  const int req = blockIdx.x * (blockDim.x >> 5) + wib;
   pdl_wait();
   pdl_trigger();
   if (req >= n_req) return;
-  const WarpSmem sm = carve_warp_smem(smem_raw + build_warp_bytes(D, K, B) * wib, D, K, B);
+  WarpSmem sm = carve_warp_smem(smem_raw + build_warp_bytes(D, K, B) * wib, D, K, B);
   const float* lp_r = lp_g + (size_t)req * D * K;
-  const int32_t* ids_r = ids_g + (size_t)req * D * K;
-  for (int i = lane; i < D * K; i += 32) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
+  sm.ids = ids_g + (size_t)req * D * K;
+  for (int i = lane; i < D * K; i += 32) sm.lp[i] = lp_r[i];
   __syncwarp();
   const int n = seq_build<NSL>(sm, D, K, B, lane, root_tok[req]);
   write_tree(sm, n, B, req, lane, n_nodes_out, tok_out, parent_out, depth_out, rank_out,
@@ -409,7 +415,7 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
       const int slot = atomicAdd(&misc[0], 1);
       f.ckey[slot] = key;
       f.cpar[slot] = fi;
-      f.cdr[slot] = (d << 8) | (r + 1);
+      f.cdr[slot] = (d << 16) | (r + 1);
     }
     __syncthreads();
     if (misc[1]) return -1;
@@ -529,7 +535,7 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
   for (int i = tid; i < n_p; i += T) {
     const int idx = f.sidx[i];
     const int dr = f.pdr[cur][idx];
-    const int dd = dr >> 8, rr = dr & 255;
+    const int dd = dr >> 16, rr = dr & 0xFFFF;
     const int par = f.ppar[cur][idx];
     *reinterpret_cast<uint4*>(sm.node + 4 * (i + 1)) =
         make_uint4(static_cast<uint32_t>(sm.ids[(dd - 1) * K + (rr - 1)]),
@@ -561,11 +567,11 @@ ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict
   pdl_wait();
   pdl_trigger();
   if (req >= n_req) return;
-  const WarpSmem sm = carve_warp_smem(smem_raw, D, K, B);
+  WarpSmem sm = carve_warp_smem(smem_raw, D, K, B);
   const FastSmem fs = carve_fast_smem(smem_raw + build_warp_bytes(D, K, B), K, B);
   const float* lp_r = lp_g + (size_t)req * D * K;
-  const int32_t* ids_r = ids_g + (size_t)req * D * K;
-  for (int i = threadIdx.x; i < D * K; i += blockDim.x) { sm.lp[i] = lp_r[i]; sm.ids[i] = ids_r[i]; }
+  sm.ids = ids_g + (size_t)req * D * K;
+  for (int i = threadIdx.x; i < D * K; i += blockDim.x) sm.lp[i] = lp_r[i];
   __syncthreads();
   const int32_t root = root_tok[req];
   int n = fast_build(sm, fs, D, K, B, root);
@@ -602,12 +608,16 @@ void launch_build_t(const TreeBuildLaunch& a, cudaStream_t st) {
   static bool attr_set = false;  // per instantiation, per process
   if (!attr_set) {
     cudaFuncSetAttribute(ddtree_build_kernel<NSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
+                         kBuildSmemMax);
     attr_set = true;
   }
-  const size_t smem = build_warp_bytes(a.D, a.K, a.B) * kBuildWarps;
-  dim3 grid(ceil_div(a.n_req, kBuildWarps));
-  launch_k(ddtree_build_kernel<NSL>, grid, dim3(kBuildWarps * 32), smem, st, a.n_req, a.D, a.K,
+  // as many requests per CTA (up to kBuildWarps) as the shared memory holds
+  const size_t per_warp = build_warp_bytes(a.D, a.K, a.B);
+  int wpc = static_cast<int>(kBuildSmemMax / per_warp);
+  wpc = wpc < 1 ? 1 : (wpc > kBuildWarps ? kBuildWarps : wpc);
+  const size_t smem = per_warp * wpc;
+  dim3 grid(ceil_div(a.n_req, wpc));
+  launch_k(ddtree_build_kernel<NSL>, grid, dim3(wpc * 32), smem, st, a.n_req, a.D, a.K,
            a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent, a.depth, a.rank,
            a.mask);
 }

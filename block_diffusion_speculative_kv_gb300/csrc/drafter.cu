@@ -103,7 +103,10 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
   const size_t arows = (size_t)n_req * d.n_kv * cap_chunks * G * L;
   w.apart_o = take(m.bf16 ? sizeof(float) * arows * d.head_dim : 0);
   w.apart_ml = take(m.bf16 ? sizeof(float) * arows * 2 : 0);
-  w.tpart = take(topk_part_bytes(n_req * D, 32));
+  size_t tp = topk_part_bytes(n_req * D, 32);
+  if (K > 32 && topk_large_part_bytes(n_req * D, d.vocab, K) > tp)
+    tp = topk_large_part_bytes(n_req * D, d.vocab, K);
+  w.tpart = take(tp);
   // records of the top-K fused into the LM head (batch-1 row tile)
   w.tkpart = take(m.bf16 && tc_row_tile(R) == 16 ? sizeof(float) * sms * R * kTkStride : 0);
   w.rope_blk = take(sizeof(float2) * (size_t)R * (d.head_dim / 2));
@@ -246,7 +249,7 @@ void dflash_model_destroy(dflash_model* model) { delete model; }
 
 size_t dflash_workspace_bytes(const dflash_model* model, int n_req, int max_inject_rows, int L,
                               int K) {
-  if (!model || n_req < 1 || max_inject_rows < 0 || L < 2 || L > 16 || K < 1 || K > 32)
+  if (!model || n_req < 1 || max_inject_rows < 0 || L < 2 || L > 16 || K < 1 || K > 1024)
     return 0;
   return ws_layout(*model, n_req, max_inject_rows, L, K).total;
 }
@@ -336,8 +339,10 @@ static dflash_status check_draft(const dflash_model* model, const dflash_cache* 
   if (n_req < 1 || n_req > cache->n_req)
     return set_error(DFLASH_ERR_INVALID_ARG, "n_req must be in [1, cache->n_req]");
   if (L < 2 || L > 16) return set_error(DFLASH_ERR_INVALID_ARG, "L must be in [2, 16]");
-  if (K < 1 || K > 32 || K > d.vocab)
-    return set_error(DFLASH_ERR_INVALID_ARG, "K must be in [1, min(32, vocab)]");
+  if (K < 1 || K > 1024 || K > d.vocab)
+    return set_error(DFLASH_ERR_INVALID_ARG, "K must be in [1, min(1024, vocab)]");
+  if (K > 32 && topk_large_merge_smem(d.vocab, K) > 200 * 1024)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "K = %d is too large for this vocabulary", K);
   if (max_ctx < 0 || max_ctx > cache->cap)
     return set_error(DFLASH_ERR_INVALID_ARG, "max_ctx must be in [0, cache->cap]");
   if (!anchor || !ctx_len || !topk_ids || !topk_logp)
@@ -402,7 +407,7 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   // epilogue (per-CTA records, merged by a small kernel); the logits are then
   // stored only if the caller asked for them.  Sampling rides there for K <= 8.
   const bool sampling = smp.inv_t > 0.f;
-  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16 && !(sampling && K > 8);
+  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16 && K <= 32 && !(sampling && K > 8);
   auto lm_step = [&]() {
     EpiParams el = epi_base(*model, R, d.vocab);
     el.kind = EPI_LOGITS;
@@ -525,7 +530,12 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   tk.t = smp.t;
   tk.seed = smp.seed;
   tk.row0 = smp.row0;
-  launch_topk(tk, c.st);
+  if (K > 32) {
+    st = launch_topk_large(tk, c.ws + W.tpart, c.st);
+    if (st) return st;
+  } else {
+    launch_topk(tk, c.st);
+  }
   return check_launch("top-K");
 }
 
@@ -540,6 +550,8 @@ dflash_status dflash_draft_block(const dflash_model* model, const dflash_cache* 
   SampleSpec smp;
   st = parse_sampling(sampling, &smp);
   if (st) return st;
+  if (smp.inv_t > 0.f && K > 32)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "sampling draws at most 32 tokens per position");
   const WsLayout W = ws_layout(*model, n_req, 0, L, K);
   if (!ws || ws_bytes < W.f)
     return set_error(DFLASH_ERR_WORKSPACE, "draft workspace needs %zu bytes, got %zu", W.f,
@@ -564,6 +576,8 @@ dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* 
   SampleSpec smp;
   st = parse_sampling(sampling, &smp);
   if (st) return st;
+  if (smp.inv_t > 0.f && K > 32)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "sampling draws at most 32 tokens per position");
   const WsLayout W = ws_layout(*model, n_req, n_rows, L, K);
   if (!ws || ws_bytes < W.total)
     return set_error(DFLASH_ERR_WORKSPACE, "cycle workspace needs %zu bytes, got %zu", W.total,

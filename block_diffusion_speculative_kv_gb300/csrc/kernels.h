@@ -37,6 +37,12 @@ struct TopkLaunch {
   long long row0;
 };
 int topk_splits(int rows, int vocab);
+// K in (32, 1024] (topk_large.cu): two passes, partial records in `part` of
+// topk_large_part_bytes bytes (no zeroing needed); plain top-K only.
+int topk_large_splits(int vocab);
+size_t topk_large_part_bytes(int rows, int vocab, int K);
+size_t topk_large_merge_smem(int vocab, int K);
+dflash_status launch_topk_large(const TopkLaunch& a, void* part, cudaStream_t st);
 size_t topk_part_bytes(int rows, int splits);
 void launch_topk(const TopkLaunch& a, cudaStream_t st);
 // Merge of the per-CTA records of the top-K fused into the LM-head GEMM

@@ -48,10 +48,17 @@ def test_host_validation_needs_no_gpu(libpath):
     # invalid budget and depth are rejected before anything touches the device
     assert lib.ddtree_build(1, 0, 8, 64, *([None] * 9), None) == 1
     assert lib.ddtree_build(1, 8, 8, 2000, *([None] * 9), None) == 1
-    assert lib.ddtree_build(1, 8, 40, 64, *([None] * 9), None) == 1
+    assert lib.ddtree_build(1, 8, 1025, 64, *([None] * 9), None) == 1
     assert b"K" in lib.dflash_last_error()
     assert lib.dflash_logits_topk(4, 100, 50, 1, None, 8, None, None, None, 0, None) == 1
     assert lib.dflash_topk_workspace_bytes(4, 100, 0) == 0
+    assert lib.dflash_topk_workspace_bytes(4, 100000, 1025) == 0
+    assert lib.dflash_topk_workspace_bytes(4, 100000, 1024) > 4 * 1024 * 8
+    assert lib.dflash_logits_topk(4, 2000, 2000, 0, None, 1025, None, None, None, 0, None) == 1
+    # sampling draws at most 32 tokens
+    s1 = ctypes.byref(binding.Sampling(1.0, 1, 0))
+    assert lib.dflash_logits_sample(4, 2000, 2000, 0, None, s1, 64, None, None, None, 0,
+                                    None) == 2
     # zero-sized requests are valid no-ops
     assert lib.ddtree_build(0, 8, 8, 64, *([None] * 9), None) == 0
     assert lib.dflash_chain_tree(1, 0, 1, 64, *([None] * 8), None) == 1

@@ -181,6 +181,12 @@ def test_draft_qwen3_4b_shape_fused_topk_widths(K):
     _draft_case(1, K=K)
 
 
+def test_draft_qwen3_4b_shape_large_k():
+    # K = 256 (Lemma 1's exact mode at B = 256): logits stored, then the
+    # two-pass large-K top-K
+    _draft_case(1, K=256)
+
+
 def test_draft_qwen3_4b_shape_anchor_isolated():
     # the anchor row sees no other block position (tensor-core attention mask)
     _draft_case(1, anchor_sees_block=False)

@@ -62,6 +62,25 @@ def test_topk_matches_oracle(rows, V, K, dtype, pad):
     assert np.allclose(lp, o_lp, atol=1e-5, rtol=0)
 
 
+@pytest.mark.parametrize("rows,V,K,dtype,pad", [
+    (15, 151936, 64, torch.float32, 0),      # one drafted block, K above the small-K kernels
+    (15, 151936, 1024, torch.bfloat16, 0),   # Lemma 1's exact mode at B = 1024
+    (3, 5000, 1024, torch.float32, 1),       # one chunk per row, unaligned rows
+    (2, 1000, 1000, torch.float32, 0),       # K = vocab: every token, sorted
+    (40, 20000, 256, torch.bfloat16, 3),     # many rows, two chunks per row
+    (4, 16385, 300, torch.float32, 0),       # a last chunk of one logit
+])
+def test_topk_large_k_matches_oracle(rows, V, K, dtype, pad):
+    g = torch.Generator().manual_seed(rows * 11 + K)
+    x = torch.randn(rows, V, generator=g) * 2.0
+    x = torch.round(x * 8) / 8            # exact ties across chunk boundaries
+    x = x.to(dtype)
+    ids, lp = _gpu_topk(x, K, pad=pad)
+    o_ids, o_lp = _oracle_topk(x, K)
+    assert np.array_equal(ids, o_ids)
+    assert np.allclose(lp, o_lp, atol=1e-5, rtol=0)
+
+
 def test_topk_stress_workload_full_size():
     """The stress workload's logits: 256 requests x 16 positions x 151936 bf16,
     N(0, 2) plus a planted +8 token per row.  Ids exact, logp within 1e-5."""
@@ -115,6 +134,10 @@ def _check_tree(gpu, ref_list, B):
     (4, 15, 8, 512, 0.0),      # its largest budget
     (3, 15, 8, 300, 0.0),      # a budget that is not a power of two
     (6, 15, 8, 256, 0.05),     # a few tied rows: some requests fall back
+    (2, 15, 64, 64, 0.0),      # Lemma 1's exact mode K = B: parallel construction
+    (3, 15, 256, 256, 0.2),    # K = B = 256: the sequential heap, ranks above 63
+    (2, 16, 1024, 1024, 0.3),  # K = B = 1024 (two requests per CTA in shared memory)
+    (5, 15, 1024, 1024, 0.0),
 ])
 def test_tree_build_bit_exact(n_req, D, K, B, ties):
     lp, ids = synth.random_topk_table(n_req, D, K, 50000, seed=B + D + n_req,
@@ -123,6 +146,20 @@ def test_tree_build_bit_exact(n_req, D, K, B, ties):
     gpu, _ = _gpu_tree(lp, ids, roots, B)
     refs = [odt.build_tree(lp[r], ids[r], int(roots[r]), B) for r in range(n_req)]
     _check_tree(gpu, refs, B)
+
+
+@pytest.mark.parametrize("tie_fraction", [0.0, 1.0])
+def test_tree_build_deep_ranks(tie_fraction):
+    # nearly flat lists (gaps 1/400 of the table's): the budget goes to wide
+    # levels, so ranks run into the hundreds (K = B = 1024, Lemma 1's mode)
+    lp, ids = synth.random_topk_table(2, 4, 1024, 151936, seed=5, tie_fraction=tie_fraction)
+    lp = (lp - lp[:, :, :1]) / 400.0 + lp[:, :, :1]
+    lp = np.ascontiguousarray(lp.astype(np.float32))
+    roots = np.array([7, 8], dtype=np.int32)
+    gpu, _ = _gpu_tree(lp, ids, roots, 1024)
+    refs = [odt.build_tree(lp[r], ids[r], int(roots[r]), 1024) for r in range(2)]
+    assert max(int(ref["rank"].max()) for ref in refs) > 255
+    _check_tree(gpu, refs, 1024)
 
 
 @pytest.mark.parametrize("kind", ["unsorted", "positive", "zero"])
