@@ -385,13 +385,42 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def graph_time(fn, steps, warmup):
+    """Milliseconds for `steps` replays of a CUDA graph of fn (host launch cost
+    out of the timed region), and the clock record."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return timed_region(g.replay, steps, warmup, 1)
+
+
+def traced_us(fn, reps=3):
+    """Per-kernel microseconds of one call of fn (CUDA events around each of
+    the library's launches, the host queue filled ahead by a GPU-side sleep)."""
+    from block_diffusion_speculative_kv_gb300 import binding as bd
+    tr = Tracer()
+    for _ in range(reps):
+        torch.cuda._sleep(20_000_000)
+        bd.set_trace_hook(tr)
+        fn()
+        bd.set_trace_hook(None)
+    return {k: round(sum(v) / reps, 2) for k, v in tr.durations().items()}
+
+
 def run_chain_sweep(args):
     """Vanilla DFlash (a chain of the per-position argmax at T = 0, or of one
     Gumbel-max sample per position at T = 1, drafted inside the LM-head top-K
     pass) against DDTree (top-8 per position, budget B) at block sizes L = 4,
     8, 16, on the Qwen3-8B-shaped batch-1 drafter with 8192 context slots.
     One line per (drafter, L, T): microseconds per draft cycle (inject + draft
-    + tree)."""
+    + tree) as CUDA-graph replays, and the kernels' times in one traced cycle."""
     cyc = Cycle(2)
     bd = cyc.bd
     wl = cyc.wl
@@ -417,10 +446,11 @@ def run_chain_sweep(args):
                     bd.chain_tree(ids, cyc.anchor, B, *tree)
                 else:
                     bd.ddtree_build(lq, ids, cyc.anchor, B, *tree)
-            ms, clocks = timed_region(fn, args.steps, max(args.warmup, 3), 1)
+            ms, clocks = graph_time(fn, args.steps, max(args.warmup, 3))
             assert cyc.dr.read_status() == 0
             rows.append({"drafter": drafter, "L": L, "T": T, "K": K, "B": B,
                          "us_per_cycle": round(ms * 1e3 / args.steps, 1),
+                         "kernels_us": traced_us(fn),
                          "sm_mhz": clocks.get("sm_mhz") if isinstance(clocks, dict) else None})
     print(json.dumps({"case": "chain_sweep", "workload": wl.name, "steps": args.steps,
                       "rows": rows}))
@@ -431,7 +461,8 @@ def run_budget_sweep(args):
     (8192 context slots), with the workload's K = 8 and with Lemma 1's exact
     K = B.  Per (B, K): microseconds per full cycle (inject + draft + top-K +
     tree), for the top-K alone over the cycle's 15 rows of fp32 logits, and for
-    the tree build alone; the tree's node count and depth."""
+    the tree build alone (kernel times from CUDA events around each launch; the
+    cycle as CUDA-graph replays); the tree's node count and depth."""
     cyc = Cycle(2)
     bd, wl = cyc.bd, cyc.wl
     L, D = wl.L, wl.L - 1
@@ -462,13 +493,14 @@ def run_budget_sweep(args):
             def tree_fn():
                 bd.ddtree_build(lq, ids, cyc.anchor, B, *tree)
             w = max(args.warmup, 3)
-            ms_c, clocks = timed_region(cycle_fn, args.steps, w, 1)
-            ms_k, _ = timed_region(topk_fn, args.steps, w, 1)
-            ms_t, _ = timed_region(tree_fn, args.steps, w, 1)
+            ms_c, clocks = graph_time(cycle_fn, args.steps, w)
+            tk = traced_us(topk_fn)
+            tt = traced_us(tree_fn)
             assert cyc.dr.read_status() == 0
             rows.append({"B": B, "K": K, "us_cycle": round(ms_c * 1e3 / args.steps, 1),
-                         "us_topk": round(ms_k * 1e3 / args.steps, 2),
-                         "us_tree": round(ms_t * 1e3 / args.steps, 2),
+                         "cycle_kernels_us": traced_us(cycle_fn),
+                         "us_topk": round(sum(tk.values()), 2), "topk_kernels_us": tk,
+                         "us_tree": round(sum(tt.values()), 2),
                          "n_nodes": int(tree[0].item()), "depth": int(tree[3].max().item()),
                          "max_rank": int(tree[4].max().item()),
                          "sm_mhz": clocks.get("sm_mhz") if isinstance(clocks, dict) else None})

@@ -116,7 +116,9 @@ dflash_status dflash_read_status(void* ws, int* device_status, void* stream) {
 // ---------------------------------------------------------------------------
 size_t dflash_topk_workspace_bytes(int rows, int vocab, int K) {
   if (rows < 0 || vocab <= 0 || K < 1 || K > 1024) return 0;
-  const size_t part = K > 32 ? topk_large_part_bytes(rows, vocab, K) : topk_part_bytes(rows, 32);
+  size_t part = topk_part_bytes(rows, 32);
+  if (K > 8 && topk_large_part_bytes(rows, vocab, K) > part)
+    part = topk_large_part_bytes(rows, vocab, K);
   return ws_header_bytes() + align_up(sizeof(int) * (size_t)rows, 256) + part;
 }
 
@@ -132,7 +134,7 @@ static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, co
   if (ps) return ps;
   if (smp.inv_t > 0.f && K > 32)
     return set_error(DFLASH_ERR_UNSUPPORTED, "sampling draws at most 32 tokens per row");
-  if (K > 32 && topk_large_merge_smem(vocab, K) > 200 * 1024)
+  if (K > 8 && topk_large_merge_smem(vocab, K) > 200 * 1024)
     return set_error(DFLASH_ERR_UNSUPPORTED, "K = %d is too large for a vocabulary of %d", K,
                      vocab);
   if (rows == 0) return DFLASH_OK;
@@ -150,7 +152,7 @@ static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, co
                                     align_up(sizeof(int) * (size_t)rows, 256));
   a.ids = ids; a.logp = logp;
   a.inv_t = smp.inv_t; a.t = smp.t; a.seed = smp.seed; a.row0 = smp.row0;
-  if (K > 32) {
+  if (K > 8 && smp.inv_t == 0.f) {
     const dflash_status ls = launch_topk_large(a, a.part, static_cast<cudaStream_t>(stream));
     if (ls) return ls;
   } else {

@@ -104,7 +104,7 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
   w.apart_o = take(m.bf16 ? sizeof(float) * arows * d.head_dim : 0);
   w.apart_ml = take(m.bf16 ? sizeof(float) * arows * 2 : 0);
   size_t tp = topk_part_bytes(n_req * D, 32);
-  if (K > 32 && topk_large_part_bytes(n_req * D, d.vocab, K) > tp)
+  if (K > 8 && topk_large_part_bytes(n_req * D, d.vocab, K) > tp)
     tp = topk_large_part_bytes(n_req * D, d.vocab, K);
   w.tpart = take(tp);
   // records of the top-K fused into the LM head (batch-1 row tile)
@@ -341,7 +341,7 @@ static dflash_status check_draft(const dflash_model* model, const dflash_cache* 
   if (L < 2 || L > 16) return set_error(DFLASH_ERR_INVALID_ARG, "L must be in [2, 16]");
   if (K < 1 || K > 1024 || K > d.vocab)
     return set_error(DFLASH_ERR_INVALID_ARG, "K must be in [1, min(1024, vocab)]");
-  if (K > 32 && topk_large_merge_smem(d.vocab, K) > 200 * 1024)
+  if (K > 8 && topk_large_merge_smem(d.vocab, K) > 200 * 1024)
     return set_error(DFLASH_ERR_UNSUPPORTED, "K = %d is too large for this vocabulary", K);
   if (max_ctx < 0 || max_ctx > cache->cap)
     return set_error(DFLASH_ERR_INVALID_ARG, "max_ctx must be in [0, cache->cap]");
@@ -403,11 +403,13 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
     eq.rope_cols = (d.n_q + d.n_kv) * hd;
     return Step{&model->tm_qkv[l], model->w.w_qkv[l], xn, d.d, qkv_dim, d.d, eq};
   };
-  // With one 16-row tile the log-softmax / top-K rides in the LM head's
-  // epilogue (per-CTA records, merged by a small kernel); the logits are then
-  // stored only if the caller asked for them.  Sampling rides there for K <= 8.
+  // With one 16-row tile and K <= 8 the log-softmax / top-K (or the sampling)
+  // rides in the LM head's epilogue and is merged inside the same launch; the
+  // logits are then stored only if the caller asked for them.  Otherwise the
+  // logits are stored and a top-K pass follows (the two-pass large-K one for
+  // K > 8 without sampling).
   const bool sampling = smp.inv_t > 0.f;
-  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16 && K <= 32 && !(sampling && K > 8);
+  const bool fused_topk = model->bf16 && tc_row_tile(R) == 16 && K <= 8;
   auto lm_step = [&]() {
     EpiParams el = epi_base(*model, R, d.vocab);
     el.kind = EPI_LOGITS;
@@ -416,9 +418,8 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
     el.L = L;
     el.tk_part = fused_topk ? reinterpret_cast<float*>(c.ws + W.tkpart) : nullptr;
     el.tk_K = K;
-    // K <= 8: the LM-head chain also merges the records (no separate kernel)
-    el.tk_ids = fused_topk && K <= 8 ? topk_ids : nullptr;
-    el.tk_logp = fused_topk && K <= 8 ? topk_logp : nullptr;
+    el.tk_ids = fused_topk ? topk_ids : nullptr;
+    el.tk_logp = fused_topk ? topk_logp : nullptr;
     if (fused_topk) {
       el.tk_inv_t = smp.inv_t;
       el.tk_t = smp.t;
@@ -508,12 +509,7 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
     if (st) return st;
   }
   // log-softmax + top-K
-  if (fused_topk && K <= 8) return DFLASH_OK;   // merged inside the LM-head chain
-  if (fused_topk) {
-    launch_topk_merge(reinterpret_cast<const float*>(c.ws + W.tkpart), num_sms(), n_req * D, K,
-                      topk_ids, topk_logp, c.st);
-    return check_launch("top-K merge");
-  }
+  if (fused_topk) return DFLASH_OK;   // merged inside the LM-head chain
   TopkLaunch tk{};
   tk.logits = lg;
   tk.rows = n_req * D;
@@ -530,7 +526,7 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   tk.t = smp.t;
   tk.seed = smp.seed;
   tk.row0 = smp.row0;
-  if (K > 32) {
+  if (K > 8 && !sampling) {
     st = launch_topk_large(tk, c.ws + W.tpart, c.st);
     if (st) return st;
   } else {

@@ -76,11 +76,12 @@ struct EpiParams {
   // LOGITS
   float* logits;
   int L;
-  // fused top-K of the logits rows: per-CTA records [grid][n_req*(L-1)][kTkStride]
+  // fused top-K (K <= kTkMax) of the logits rows: per-CTA records
+  // [grid][n_req*(L-1)][kTkStride]; LOGITS is the chain's last phase and the
+  // last CTAs to publish their records merge them into ids / log-probabilities
+  // [n_req*(L-1)][K]
   float* tk_part;
   int tk_K;
-  // when set (K <= 8, LOGITS the chain's last phase) the last CTA to publish its
-  // records merges them into ids / log-probabilities [n_req*(L-1)][K]
   int32_t* tk_ids;
   float* tk_logp;
   // temperature sampling (tk_inv_t > 0, K <= 8): the lists rank the Gumbel
@@ -92,7 +93,7 @@ struct EpiParams {
 };
 
 // Record of a fused top-K: max, sum of exp(x - max), K values (desc), K ids.
-constexpr int kTkMax = 32;
+constexpr int kTkMax = 8;
 constexpr int kTkStride = 2 + 2 * kTkMax;
 
 // An approximate reciprocal (rcp.approx, within about one ulp) instead of an

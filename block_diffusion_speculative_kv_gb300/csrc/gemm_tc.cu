@@ -154,84 +154,13 @@ __device__ __forceinline__ void warp_sort_desc(float& v, int& id, int lane) {
   }
 }
 
-// Fold one epilogue chunk of LM-head values (rows c0.. of the tile, this
-// thread's column col) into warp ew's per-row state: online max / sum of exp,
-// and the sorted list (value desc, id asc).  A CTA meets its tiles in column
-// order, so a value equal to the K-th kept one never displaces it.  Warp-
-// uniform; K <= kpad <= 32.
-__device__ __forceinline__ void tk_update(const EpiParams& E, float* tk, int kpad, int n_tile,
-                                          const float* buf, const float* s_scale, int c0, int nr,
-                                          int f, int col, bool cvalid, int ew, int lane) {
-  const unsigned FULL = 0xffffffffu;
-  const int K = E.tk_K;
-  const int stride = 2 + 2 * kpad;
-  for (int j = 0; j < nr; ++j) {
-    const int row = c0 + j;
-    if (row % E.L == 0) continue;   // anchor rows have no logits
-    float* st = tk + (ew * n_tile + row) * stride;
-    const float v = cvalid ? buf[j * kBufLd + f] * s_scale[row] : -CUDART_INF_F;
-    const float mx = from_ordered_bits(__reduce_max_sync(FULL, ordered_bits(v)));
-    const float m_old = st[0], s_old = st[1];
-    const float M = fmaxf(m_old, mx);
-    float e = (v == -CUDART_INF_F) ? 0.f : exp2f((v - M) * 1.4426950408889634f);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(FULL, e, off);
-    __syncwarp();
-    if (lane == 0 && M != -CUDART_INF_F) {
-      st[0] = M;
-      st[1] = (m_old == -CUDART_INF_F ? 0.f : s_old * exp2f((m_old - M) * 1.4426950408889634f)) + e;
-    }
-    const float thr = st[2 + K - 1];
-    unsigned cand = __ballot_sync(FULL, v > thr);
-    if (__popc(cand) > 2 && K <= 16) {
-      // many candidates (a warp's first tiles): sort them, then sort the list
-      // together with the best 32-K of them; with K <= 16 those hold the top K
-      float sv = v > thr ? v : -CUDART_INF_F;
-      int si = v > thr ? col : 0x7fffffff;
-      warp_sort_desc(sv, si, lane);
-      const float cv = __shfl_sync(FULL, sv, lane >= K ? lane - K : 0);
-      const int ci = __shfl_sync(FULL, si, lane >= K ? lane - K : 0);
-      float uv = lane < K ? st[2 + lane] : cv;
-      int ui = lane < K ? __float_as_int(st[2 + kpad + lane]) : ci;
-      warp_sort_desc(uv, ui, lane);
-      __syncwarp();
-      if (lane < K) {
-        st[2 + lane] = uv;
-        st[2 + kpad + lane] = __int_as_float(ui);
-      }
-      cand = 0;
-    }
-    while (cand) {
-      const int b = __ffs(cand) - 1;
-      cand &= cand - 1;
-      const float bv = __shfl_sync(FULL, v, b);
-      const int bi = __shfl_sync(FULL, col, b);
-      const float ev = lane < K ? st[2 + lane] : -CUDART_INF_F;
-      const int ei = lane < K ? __float_as_int(st[2 + kpad + lane]) : 0x7fffffff;
-      const unsigned ahead = __ballot_sync(FULL, lane < K && tk_better(ev, ei, bv, bi));
-      const int pos = __popc(ahead);
-      const float pv = __shfl_up_sync(FULL, ev, 1);
-      const int pi = __shfl_up_sync(FULL, ei, 1);
-      __syncwarp();
-      if (pos < K) {
-        if (lane < K && lane > pos) {
-          st[2 + lane] = pv;
-          st[2 + kpad + lane] = __int_as_float(pi);
-        }
-        if (lane == pos) {
-          st[2 + lane] = bv;
-          st[2 + kpad + lane] = __int_as_float(bi);
-        }
-      }
-      __syncwarp();
-    }
-    __syncwarp();
-  }
-}
-
-// The same fold for K <= 8 with one lane per tile row: lane j walks the warp's
-// 32 columns of chunk row j in column order with its state in registers (one
-// exp per value, a register insert only when the value beats the K-th kept).
+// Fold one epilogue chunk of LM-head values into warp ew's per-row state
+// (online max / sum of exp, and the sorted list of the K <= 8 best by value
+// desc, id asc) with one lane per tile row: lane j walks the warp's 32 columns
+// of chunk row j in column order with its state in registers (one exp per
+// value, a register insert only when the value beats the K-th kept; a CTA
+// meets its tiles in column order, so an equal value never displaces a kept
+// one).
 // With sampling the list ranks Gumbel scores while (max, sum) covers logits.
 __device__ __forceinline__ void tk_update_rows(const EpiParams& E, float* tk, int kpad, int n_tile,
                                                const float* buf, const float* s_scale, int c0,
@@ -819,12 +748,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                  p.n_tile, ew, pre);
             if (fused_tk) {
-              if (E.tk_K <= 8)
-                tk_update_rows(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, ftile * kTileN,
-                               ew, lane);
-              else
-                tk_update(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, f, ftile * kTileN + f,
-                          ftile * kTileN + f < E.N_feat, ew, lane);
+              tk_update_rows(E, tk, p.tk_kpad, p.n_tile, buf, s_scale, c0, nr, ftile * kTileN,
+                             ew, lane);
               __syncwarp();
             }
             ptx::named_bar_sync(1, kEpiThreads);
@@ -846,8 +771,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int K = E.tk_K;
         const int n_out = E.M_rows / E.L * (E.L - 1);
         const int n_rows = min(p.n_tile, E.M_rows);
-        // K <= 8: eight rows per warp pass, lane = 4 * row slot + warp state
-        for (int base = ew; K <= 8 && base < n_rows; base += 32) {
+        // eight rows per warp pass, lane = 4 * row slot + warp state
+        for (int base = ew; base < n_rows; base += 32) {
           const int row = base + 4 * (lane >> 2);
           const bool live = row < n_rows && row % E.L != 0;
           const float* st = tk + ((lane & 3) * p.n_tile + (live ? row : 0)) * tk_stride;
@@ -872,46 +797,6 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 rec[2 + q] = tv[q];
                 rec[2 + kTkMax + q] = __int_as_float(ti[q]);
               }
-          }
-        }
-        for (int row = ew; K > 8 && row < n_rows; row += 4) {
-          if (row % E.L == 0) continue;
-          const int orow = row / E.L * (E.L - 1) + row % E.L - 1;
-          float* rec = E.tk_part + ((size_t)c * n_out + orow) * kTkStride;
-          const float* st = tk + ((lane & 3) * p.n_tile + row) * tk_stride;
-          float m = lane < 4 ? st[0] : -CUDART_INF_F;
-          float sm = lane < 4 ? st[1] : 0.f;
-#pragma unroll
-          for (int off = 1; off < 4; off <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-            const float s2 = __shfl_xor_sync(0xffffffffu, sm, off);
-            const float M = fmaxf(m, m2);
-            sm = (M == -CUDART_INF_F) ? 0.f
-                 : (m == -CUDART_INF_F ? 0.f : sm * exp2f((m - M) * 1.4426950408889634f)) +
-                       (m2 == -CUDART_INF_F ? 0.f : s2 * exp2f((m2 - M) * 1.4426950408889634f));
-            m = M;
-          }
-          int ptr = 0;   // lanes 0-3: next entry of warp (lane)'s list
-          for (int r = 0; r < K; ++r) {
-            float bv = (lane < 4 && ptr < K) ? st[2 + ptr] : -CUDART_INF_F;
-            int bi = (lane < 4 && ptr < K) ? __float_as_int(st[2 + p.tk_kpad + ptr]) : 0x7fffffff;
-            const float ov = bv;
-            const int oi = bi;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-              const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
-              const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
-              if (tk_better(v2, i2, bv, bi)) { bv = v2; bi = i2; }
-            }
-            if (lane < 4 && ptr < K && ov == bv && oi == bi) ++ptr;
-            if (lane == 0) {
-              rec[2 + r] = bv;
-              rec[2 + kTkMax + r] = __int_as_float(bi);
-            }
-          }
-          if (lane == 0) {
-            rec[0] = m;
-            rec[1] = sm;
           }
         }
         if (E.tk_ids != nullptr) {
@@ -1075,11 +960,9 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
   for (int k = 0; k < n_phases; ++k)
     if (ph[k].epi.kind == EPI_LOGITS && ph[k].epi.tk_part != nullptr) {
       p.tk_kpad = (ph[k].epi.tk_K + 7) / 8 * 8;
-      if (ph[k].epi.tk_ids != nullptr && (k != n_phases - 1 || ph[k].epi.tk_K > 8))
+      if (ph[k].epi.tk_ids == nullptr || k != n_phases - 1 || ph[k].epi.tk_K > kTkMax)
         return set_error(DFLASH_ERR_INVALID_ARG,
-                         "in-chain top-K merge: LM head must be the last phase, K <= 8");
-      if (ph[k].epi.tk_inv_t > 0.f && ph[k].epi.tk_ids == nullptr)
-        return set_error(DFLASH_ERR_INVALID_ARG, "fused sampling needs the in-chain merge");
+                         "fused top-K: outputs set, LM head the last phase, K <= %d", kTkMax);
     }
   for (int k = 0; k < n_phases; ++k) {
     const TcPlan pl = tc_plan(M_rows, ph[k].N, ph[k].K, G, p.tk_kpad);

@@ -45,10 +45,6 @@ size_t topk_large_merge_smem(int vocab, int K);
 dflash_status launch_topk_large(const TopkLaunch& a, void* part, cudaStream_t st);
 size_t topk_part_bytes(int rows, int splits);
 void launch_topk(const TopkLaunch& a, cudaStream_t st);
-// Merge of the per-CTA records of the top-K fused into the LM-head GEMM
-// (part: [n_rec][rows][kTkStride] floats, see epilogue.cuh) into ids / logp.
-void launch_topk_merge(const float* part, int n_rec, int rows, int K, int32_t* ids, float* logp,
-                       cudaStream_t st);
 
 // ---- DDTree (ddtree.cu) ----
 struct TreeBuildLaunch {

@@ -347,91 +347,7 @@ void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
   (void)VN;
 }
 
-// Final step of the top-K fused into the LM-head GEMM: row `blockIdx.x` has
-// n_rec records (one per GEMM CTA, layout of kTkStride floats: max, sum of exp,
-// kTkMax values, kTkMax ids); each thread folds its records into a register
-// list, warps run tournaments, warp 0 merges the warps' lists.
-template <int KMAX>
-__global__ void __launch_bounds__(kTopkThreads)
-topk_merge_kernel(const float* __restrict__ part, int n_rec, int rows, int K,
-                  int32_t* __restrict__ ids_out, float* __restrict__ logp_out) {
-  __shared__ float s_wv[kTopkThreads / kWarp][KMAX];
-  __shared__ int s_wi[kTopkThreads / kWarp][KMAX];
-  __shared__ float s_m[kTopkThreads / kWarp], s_s[kTopkThreads / kWarp];
-  const int row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
-  pdl_trigger();
-  float m = -CUDART_INF_F, s = 0.f, thr = -CUDART_INF_F;
-  float tv[KMAX];
-  int ti[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) { tv[j] = -CUDART_INF_F; ti[j] = 0x7fffffff; }
-  for (int r = tid; r < n_rec; r += kTopkThreads) {
-    const float* rec = part + ((size_t)r * rows + row) * kTkStride;
-    merge_ms(m, s, __ldcg(rec), __ldcg(rec + 1));
-    float v[KMAX];
-    int id[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      v[j] = j < K ? __ldcg(rec + 2 + j) : -CUDART_INF_F;
-      id[j] = j < K ? __float_as_int(__ldcg(rec + 2 + kTkMax + j)) : 0x7fffffff;
-    }
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      if (j < K && better(v[j], id[j], tv[K - 1 < KMAX ? K - 1 : KMAX - 1],
-                          ti[K - 1 < KMAX ? K - 1 : KMAX - 1]))
-        list_insert<KMAX>(tv, ti, K, v[j], id[j], thr);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    merge_ms(m, s, m2, s2);
-  }
-  if (lane == 0) { s_m[warp] = m; s_s[warp] = s; }
-  for (int r = 0; r < K; ++r) {
-    float bv = tv[0]; int bi = ti[0];
-    warp_best(bv, bi);
-    if (bv == tv[0] && bi == ti[0]) {
-#pragma unroll
-      for (int j = 0; j < KMAX - 1; ++j) { tv[j] = tv[j + 1]; ti[j] = ti[j + 1]; }
-      tv[KMAX - 1] = -CUDART_INF_F; ti[KMAX - 1] = 0x7fffffff;
-    }
-    if (lane == 0) { s_wv[warp][r] = bv; s_wi[warp][r] = bi; }
-  }
-  __syncthreads();
-  if (warp != 0) return;
-  float cm = -CUDART_INF_F, cs = 0.f;
-  for (int w = 0; w < kTopkThreads / kWarp; ++w) merge_ms(cm, cs, s_m[w], s_s[w]);
-  const float lse = cm + logf(cs);
-  int p = 0;
-  for (int r = 0; r < K; ++r) {
-    float v = (lane < kTopkThreads / kWarp && p < K) ? s_wv[lane][p] : -CUDART_INF_F;
-    int i = (lane < kTopkThreads / kWarp && p < K) ? s_wi[lane][p] : 0x7fffffff;
-    float bv = v; int bi = i;
-    warp_best(bv, bi);
-    if (lane < kTopkThreads / kWarp && p < K && bv == v && bi == i) ++p;
-    if (lane == 0) {
-      ids_out[(long long)row * K + r] = bi;
-      logp_out[(long long)row * K + r] = bv - lse;
-    }
-  }
-}
-
 }  // namespace
-
-void launch_topk_merge(const float* part, int n_rec, int rows, int K, int32_t* ids, float* logp,
-                       cudaStream_t st) {
-  if (rows <= 0) return;
-  TraceScope ts("lse_topk_merge", st);
-  if (K <= 8)
-    launch_k(topk_merge_kernel<8>, dim3(rows), dim3(kTopkThreads), 0, st, part, n_rec, rows, K,
-             ids, logp);
-  else
-    launch_k(topk_merge_kernel<32>, dim3(rows), dim3(kTopkThreads), 0, st, part, n_rec, rows, K,
-             ids, logp);
-}
 
 int topk_splits(int rows, int vocab) {
   if (rows <= 0) return 1;

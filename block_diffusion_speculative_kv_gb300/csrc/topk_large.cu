@@ -9,15 +9,17 @@
 // Design: the order (logit desc, id asc) is the order of one 64-bit key per
 // element, the order-preserving bits of the logit above the complement of the
 // id, and all keys of a row are distinct.  So "the K best" is "the keys at or
-// above the K-th largest key", found by a radix select (eight passes of eight
-// bits over shared memory, a pass ending early once the bin it picks is taken
-// whole) with no tie rule left to apply.
-//   pass 1: one CTA per (row, chunk of 16384 logits): the chunk's keys in
-//           shared memory, its (max, sum of exp), its best min(K, chunk) keys
-//           to a partial record (unsorted);
-//   pass 2: one CTA per row: the partial records' keys in shared memory, the
-//           best K of them, each placed by counting the winners above it, and
-//           the log-probabilities from the merged (max, sum of exp).
+// above the K-th largest key", found by a radix select with no tie rule left
+// to apply: eight-bit digits from the top, each pass over only the candidates
+// that share the digits chosen so far (a pass emits the candidates of higher
+// bins and keeps those of the chosen bin), stopping once the kept candidates
+// are exactly the ones still needed.
+//   kernel 1: one CTA per (row, chunk of 16384 logits): the chunk's keys in
+//             shared memory, its (max, sum of exp), its best min(K, chunk)
+//             keys to a partial record (unsorted);
+//   kernel 2: one CTA per row: the partial records' keys in shared memory, the
+//             best K of them, a bitonic sort of those, and log-probabilities
+//             from the merged (max, sum of exp).
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -44,62 +46,76 @@ __device__ __forceinline__ void lg_merge(float& m, float& s, float m2, float s2)
   s = a + b;
 }
 
-// Block-wide radix select over n distinct 64-bit keys key(i): returns the k-th
-// largest (1 <= k <= n), so exactly k keys are >= the result.  Every thread of
-// the block calls it; blockDim.x is a multiple of 32.
-template <typename KeyF>
-__device__ uint64_t block_select(int n, int k, KeyF key, int* hist, int* misc) {
+// Block-wide selection of the k largest among nc distinct 64-bit keys
+// (1 <= k <= nc).  Candidates are indices into the caller's arrays; pass 0
+// takes 0..nc-1 directly.  Each pass histograms the next eight key bits of the
+// candidates (all of which share the bits above), finds the bin holding the
+// k-th largest, hands every candidate of a higher bin to emit(idx) and keeps
+// the candidates of that bin for the next pass; once the kept candidates are
+// exactly the ones still needed they are all emitted.  emit is called exactly
+// k times, in no particular order.  Every thread of the block calls this.
+template <typename KeyF, typename EmitF>
+__device__ void block_topk(int nc, int k, uint16_t* cand_a, uint16_t* cand_b, KeyF key,
+                           EmitF emit, int* hist, int* misc) {
   const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  uint64_t prefix = 0, pmask = 0;
-  int need = k;
+  bool identity = true;
   for (int pass = 0; pass < 8; ++pass) {
+    if (nc == k) {
+      for (int c = tid; c < nc; c += T) emit(identity ? c : static_cast<int>(cand_a[c]));
+      return;
+    }
     const int shift = 56 - 8 * pass;
     for (int i = tid; i < 256; i += T) hist[i] = 0;
+    if (tid == 0) misc[3] = 0;
     __syncthreads();
-    for (int base = tid - lane; base < n; base += T) {
-      const int i = base + lane;
-      bool match = false;
-      int bin = 0;
-      if (i < n) {
-        const uint64_t c = key(i);
-        match = (c & pmask) == prefix;
-        bin = static_cast<int>((c >> shift) & 255u);
-      }
-      // lanes with the same bin add once (the first passes see few bins)
-      const unsigned peers = __match_any_sync(0xffffffffu, match ? bin : 256 + lane);
-      if (match && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+    for (int base = tid - lane; base < nc; base += T) {
+      const int c = base + lane;
+      int bin = 256 + lane;   // no bin: a lane past the end
+      if (c < nc) bin = static_cast<int>((key(identity ? c : cand_a[c]) >> shift) & 255u);
+      // lanes with the same bin add once
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
-      int c[8], sum = 0;
+      int cnt[8], sum = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - 8 * lane - j]; sum += c[j]; }
+      for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * lane - j]; sum += cnt[j]; }
       int incl = sum;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
       }
-      int run = incl - sum;   // keys in bins above this lane's
+      int run = incl - sum;   // candidates in bins above this lane's
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (run < need && run + c[j] >= need) {
+        if (run < k && run + cnt[j] >= k) {
           misc[0] = 255 - 8 * lane - j;
           misc[1] = run;
-          misc[2] = c[j];
+          misc[2] = cnt[j];
         }
-        run += c[j];
+        run += cnt[j];
       }
     }
     __syncthreads();
-    const int bin = misc[0], above = misc[1], cnt = misc[2];
-    prefix |= static_cast<uint64_t>(bin) << shift;
-    pmask |= 0xFFull << shift;
-    need -= above;
-    __syncthreads();   // misc is rewritten by the next pass
-    if (cnt == need) break;   // the whole bin is taken: its keys all lie at or above prefix
+    const int b = misc[0], above = misc[1], in_bin = misc[2];
+    for (int c = tid; c < nc; c += T) {
+      const int idx = identity ? c : static_cast<int>(cand_a[c]);
+      const int d = static_cast<int>((key(idx) >> shift) & 255u);
+      if (d > b) emit(idx);
+      else if (d == b) cand_b[atomicAdd(&misc[3], 1)] = static_cast<uint16_t>(idx);
+    }
+    __syncthreads();
+    k -= above;
+    nc = in_bin;
+    uint16_t* t = cand_a;
+    cand_a = cand_b;
+    cand_b = t;
+    identity = false;
   }
-  return prefix;
+  // all 64 bits resolved: the keys are distinct, so one candidate is left
+  for (int c = tid; c < nc && c < k; c += T) emit(static_cast<int>(cand_a[c]));
 }
 
 __device__ __forceinline__ void block_ms(float& m, float& s, float* s_m, float* s_s) {
@@ -129,11 +145,14 @@ __global__ void __launch_bounds__(kLgThreads)
 topk_large_part_kernel(const T* __restrict__ logits, long long ld, int vocab, int K, int splits,
                        int chunk, float* __restrict__ pv, int* __restrict__ pi,
                        float2* __restrict__ pms) {
-  extern __shared__ uint32_t skey[];   // [chunk]
+  extern __shared__ __align__(16) uint32_t skey[];   // [kLgChunk] keys, then 2 x [kLgChunk] u16
+  uint16_t* cand_a = reinterpret_cast<uint16_t*>(skey + kLgChunk);
+  uint16_t* cand_b = cand_a + kLgChunk;
   __shared__ int hist[256];
   __shared__ int misc[4];
   __shared__ float s_m[32], s_s[32];
   __shared__ int s_cnt;
+  constexpr int kPer = kLgChunk / kLgThreads;
   const int row = blockIdx.x / splits, split = blockIdx.x % splits;
   const int tid = threadIdx.x;
   const int v0 = split * chunk;
@@ -141,16 +160,22 @@ topk_large_part_kernel(const T* __restrict__ logits, long long ld, int vocab, in
   const T* rp = logits + (long long)row * ld + v0;
   pdl_wait();
   pdl_trigger();
-  float m = -CUDART_INF_F, s = 0.f;
-  for (int i = tid; i < n; i += kLgThreads) {
-    const float x = to_f32<T>(rp[i]);
-    skey[i] = ordered_bits(x);
-    if (x > m) {
-      s = (m == -CUDART_INF_F) ? 1.f : s * exp2f((m - x) * kLgLog2e) + 1.f;
-      m = x;
-    } else if (x != -CUDART_INF_F) {
-      s += exp2f((x - m) * kLgLog2e);
-    }
+  // all of a thread's loads in flight together, then the (max, sum of exp)
+  float x[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid + j * kLgThreads;
+    x[j] = i < n ? to_f32<T>(rp[i]) : -CUDART_INF_F;
+  }
+  float m = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) m = fmaxf(m, x[j]);
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid + j * kLgThreads;
+    if (i < n) skey[i] = ordered_bits(x[j]);
+    if (x[j] != -CUDART_INF_F) s += exp2f((x[j] - m) * kLgLog2e);
   }
   block_ms(m, s, s_m, s_s);
   const size_t rec = (size_t)row * splits + split;
@@ -159,28 +184,23 @@ topk_large_part_kernel(const T* __restrict__ logits, long long ld, int vocab, in
     s_cnt = 0;
   }
   __syncthreads();
-  const int k = min(K, n);
-  const uint64_t cut =
-      k < n ? block_select(n, k, [&](int i) { return rank_key(skey[i], v0 + i); }, hist, misc)
-            : 0ull;
   float* ov = pv + rec * K;
   int* oi = pi + rec * K;
-  for (int i = tid; i < n; i += kLgThreads) {
-    if (rank_key(skey[i], v0 + i) >= cut) {
-      const int slot = atomicAdd(&s_cnt, 1);
-      if (slot < k) {
-        ov[slot] = from_ordered_bits(skey[i]);
-        oi[slot] = v0 + i;
-      }
-    }
-  }
+  block_topk(n, min(K, n), cand_a, cand_b,
+             [&](int i) { return rank_key(skey[i], v0 + i); },
+             [&](int i) {
+               const int slot = atomicAdd(&s_cnt, 1);
+               ov[slot] = from_ordered_bits(skey[i]);
+               oi[slot] = v0 + i;
+             },
+             hist, misc);
 }
 
 __global__ void __launch_bounds__(kLgThreads)
 topk_large_merge_kernel(int vocab, int K, int splits, int chunk, const float* __restrict__ pv,
                         const int* __restrict__ pi, const float2* __restrict__ pms,
                         int32_t* __restrict__ ids_out, float* __restrict__ logp_out) {
-  extern __shared__ uint32_t smem2[];
+  extern __shared__ __align__(16) uint32_t smem2[];
   __shared__ int hist[256];
   __shared__ int misc[4];
   __shared__ float s_m[32], s_s[32];
@@ -191,10 +211,13 @@ topk_large_merge_kernel(int vocab, int K, int splits, int chunk, const float* __
   const int ck = min(K, chunk);                                   // records of a full chunk
   const int n_last = vocab - (splits - 1) * chunk;
   const int N = (splits - 1) * ck + min(K, n_last);
-  uint32_t* ckey = smem2;                                         // [N]
-  int* cid = reinterpret_cast<int*>(smem2 + N);                   // [N]
-  uint32_t* wkey = smem2 + 2 * N;                                 // [K]
-  int* wid = reinterpret_cast<int*>(smem2 + 2 * N + K);           // [K]
+  int P = 1;
+  while (P < K) P <<= 1;
+  uint64_t* win = reinterpret_cast<uint64_t*>(smem2);             // [P] winners, sorted here
+  uint32_t* ckey = smem2 + 2 * P;                                 // [N]
+  int* cid = reinterpret_cast<int*>(ckey + N);                    // [N]
+  uint16_t* cand_a = reinterpret_cast<uint16_t*>(cid + N);        // [N]
+  uint16_t* cand_b = cand_a + N;                                  // [N]
   pdl_wait();
   pdl_trigger();
   for (int e = tid; e < N; e += kLgThreads) {
@@ -203,6 +226,7 @@ topk_large_merge_kernel(int vocab, int K, int splits, int chunk, const float* __
     ckey[e] = ordered_bits(__ldcg(pv + at));
     cid[e] = __ldcg(pi + at);
   }
+  for (int i = K + tid; i < P; i += kLgThreads) win[i] = 0ull;   // below every real key
   float m = -CUDART_INF_F, s = 0.f;
   for (int sp = tid; sp < splits; sp += kLgThreads) {
     const float2 ms = __ldcg(pms + (size_t)row * splits + sp);
@@ -214,27 +238,28 @@ topk_large_merge_kernel(int vocab, int K, int splits, int chunk, const float* __
     s_cnt = 0;
   }
   __syncthreads();
-  const uint64_t cut =
-      K < N ? block_select(N, K, [&](int i) { return rank_key(ckey[i], cid[i]); }, hist, misc)
-            : 0ull;
-  for (int i = tid; i < N; i += kLgThreads) {
-    if (rank_key(ckey[i], cid[i]) >= cut) {
-      const int slot = atomicAdd(&s_cnt, 1);
-      if (slot < K) {
-        wkey[slot] = ckey[i];
-        wid[slot] = cid[i];
+  block_topk(N, K, cand_a, cand_b, [&](int i) { return rank_key(ckey[i], cid[i]); },
+             [&](int i) { win[atomicAdd(&s_cnt, 1)] = rank_key(ckey[i], cid[i]); }, hist, misc);
+  __syncthreads();
+  // bitonic sort of the P winner keys, descending
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += kLgThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const uint64_t a = win[i], b = win[j];
+          const bool desc = (i & size) == 0;
+          if (desc ? a < b : a > b) { win[i] = b; win[j] = a; }
+        }
       }
+      __syncthreads();
     }
   }
-  __syncthreads();
-  // each winner's place is the number of winners above it
   const float lse = s_lse;
-  for (int i = tid; i < K; i += kLgThreads) {
-    const uint64_t me = rank_key(wkey[i], wid[i]);
-    int r = 0;
-    for (int j = 0; j < K; ++j) r += rank_key(wkey[j], wid[j]) > me ? 1 : 0;
-    ids_out[(size_t)row * K + r] = wid[i];
-    logp_out[(size_t)row * K + r] = from_ordered_bits(wkey[i]) - lse;
+  for (int r = tid; r < K; r += kLgThreads) {
+    const uint64_t w = win[r];
+    ids_out[(size_t)row * K + r] = static_cast<int32_t>(~static_cast<uint32_t>(w));
+    logp_out[(size_t)row * K + r] = from_ordered_bits(static_cast<uint32_t>(w >> 32)) - lse;
   }
 }
 
@@ -254,7 +279,10 @@ size_t topk_large_merge_smem(int vocab, int K) {
   const int ck = K < chunk ? K : chunk;
   const int n_last = vocab - (splits - 1) * chunk;
   const size_t N = (size_t)(splits - 1) * ck + (K < n_last ? K : n_last);
-  return sizeof(uint32_t) * (2 * N + 2 * (size_t)K);
+  size_t P = 1;
+  while (P < (size_t)K) P <<= 1;
+  if (N > 65535) return (size_t)1 << 40;   // candidate indices are 16-bit
+  return sizeof(uint64_t) * P + (sizeof(uint32_t) + sizeof(int) + 2 * sizeof(uint16_t)) * N;
 }
 
 dflash_status launch_topk_large(const TopkLaunch& a, void* part, cudaStream_t st) {
@@ -270,7 +298,7 @@ dflash_status launch_topk_large(const TopkLaunch& a, void* part, cudaStream_t st
   int* pi = reinterpret_cast<int*>(p + align_up(recs * a.K * sizeof(float), 256));
   float2* pms = reinterpret_cast<float2*>(p + align_up(recs * a.K * sizeof(float), 256) +
                                           align_up(recs * a.K * sizeof(int), 256));
-  const size_t smem1 = sizeof(uint32_t) * kLgChunk;
+  const size_t smem1 = (sizeof(uint32_t) + 2 * sizeof(uint16_t)) * kLgChunk;
   static bool attr = false;   // per process
   if (!attr) {
     cudaFuncSetAttribute(topk_large_part_kernel<float>,

@@ -174,10 +174,10 @@ def test_draft_qwen3_4b_shape():
     _draft_case(1)
 
 
-@pytest.mark.parametrize("K", [5, 16, 32])
-def test_draft_qwen3_4b_shape_fused_topk_widths(K):
-    # batch 1: the top-K rides in the LM-head epilogue; K <= 8 takes the
-    # row-per-lane fold, larger K the warp-wide one (sorted merges up to 16)
+@pytest.mark.parametrize("K", [1, 5, 16, 32])
+def test_draft_qwen3_4b_shape_topk_widths(K):
+    # batch 1: K <= 8 rides in the LM-head epilogue (row-per-lane fold, merged
+    # in the same launch); larger K stores the logits for the two-pass top-K
     _draft_case(1, K=K)
 
 
