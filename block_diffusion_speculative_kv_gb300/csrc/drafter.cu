@@ -63,8 +63,8 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
     off = align_up(off + bytes, 256);
     return o;
   };
-  int n_counters = 4096 > R ? 4096 : R;
-  if (n_counters < gemm_counter_ints()) n_counters = gemm_counter_ints();
+  // the GEMM chains' counters, then one arrival counter per top-K row
+  const int n_counters = gemm_counter_ints() + (4096 > R ? 4096 : R);
   w.counters = take(sizeof(int) * n_counters);
   w.x = take(sizeof(float) * (size_t)R * d.d);
   w.xn = take(es * (size_t)R * d.d);
@@ -519,7 +519,7 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   tk.K = K;
   tk.splits = topk_splits(tk.rows, d.vocab);
   tk.part = reinterpret_cast<float*>(c.ws + W.tpart);
-  tk.counters = c.counters;
+  tk.counters = c.counters + gemm_counter_ints();
   tk.ids = topk_ids;
   tk.logp = topk_logp;
   tk.inv_t = smp.inv_t;

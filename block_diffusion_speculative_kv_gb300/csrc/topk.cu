@@ -22,6 +22,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "sampling.cuh"
+#include "topk8.cuh"
 
 #include <math_constants.h>
 
@@ -231,97 +232,168 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
     }
   }
 
-  // ---- CTA merge: (m, s) and the K best of 256 sorted lists ----
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    merge_ms(m, s, m2, s2);
-  }
-  if (lane == 0) { s_m[warp] = m; s_s[warp] = s; }
-  // warp tournament: every lane offers the head of its sorted list; the winner
-  // shifts its list by one, so the head always sits in register slot 0
-  for (int r = 0; r < K; ++r) {
-    float bv = tv[0]; int bi = ti[0];
-    warp_best(bv, bi);
-    if (bv == tv[0] && bi == ti[0]) {
-#pragma unroll
-      for (int j = 0; j < KMAX - 1; ++j) { tv[j] = tv[j + 1]; ti[j] = ti[j + 1]; }
-      tv[KMAX - 1] = -CUDART_INF_F; ti[KMAX - 1] = 0x7fffffff;
-    }
-    if (lane == 0) { s_wv[warp][r] = bv; s_wi[warp][r] = bi; }
-  }
-  __syncthreads();
-
-  float cm = -CUDART_INF_F, cs = 0.f;
-  if (warp == 0) {
-    for (int w = 0; w < kTopkThreads / kWarp; ++w) merge_ms(cm, cs, s_m[w], s_s[w]);
-    int p = 0;
-    for (int r = 0; r < K; ++r) {
-      float v = (lane < kTopkThreads / kWarp && p < K) ? s_wv[lane][p] : -CUDART_INF_F;
-      int i = (lane < kTopkThreads / kWarp && p < K) ? s_wi[lane][p] : 0x7fffffff;
-      float bv = v; int bi = i;
-      warp_best(bv, bi);
-      if (lane < kTopkThreads / kWarp && p < K && bv == v && bi == i) ++p;
-      if (lane == 0) { s_v[r] = bv; s_i[r] = bi; }
-      __syncwarp();
-    }
-  }
-
-  if (splits == 1) {
-    if (warp == 0) {
-      const float lse = cm + logf(cs);
-      for (int r = lane; r < K; r += 32) {
-        ids_out[(long long)row * K + r] = s_i[r];
-        logp_out[(long long)row * K + r] = out_logp<SAMPLE>(s_v[r], s_i[r], row, lse, smp);
-      }
-    }
-    return;
-  }
-
-  // ---- multi-split: publish the partial record, the last CTA of the row merges ----
-  float* rec = part.base + ((long long)row * splits + split) * part.stride;
-  if (warp == 0) {
-    if (lane == 0) { rec[0] = cm; rec[1] = cs; }
-    for (int r = lane; r < K; r += 32) {
-      rec[2 + r] = s_v[r];
-      rec[2 + KMAX + r] = __int_as_float(s_i[r]);
-    }
-    __threadfence();
-    __syncwarp();
+  if constexpr (KMAX == 8) {
+    // ---- K <= 8: butterfly merges of the register lists ----
+    tk_lane_merge(tv, ti, m, s, 1, 16);   // every lane: the warp's list
     if (lane == 0) {
-      int prev = atomicAdd(&counters[row], 1);
-      s_last = (prev == splits - 1);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { s_wv[warp][q] = tv[q]; s_wi[warp][q] = ti[q]; }
+      s_m[warp] = m;
+      s_s[warp] = s;
     }
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (warp != 0) return;
-
-  const float* recs = part.base + (long long)row * splits * part.stride;
-  float M = -CUDART_INF_F, S = 0.f;
-  for (int sp = 0; sp < splits; ++sp)
-    merge_ms(M, S, __ldcg(recs + sp * part.stride), __ldcg(recs + sp * part.stride + 1));
-  const float lse = M + logf(S);
-  // splits <= 32 is enforced by the launcher: one split per lane
-  {
-    int p = 0;
-    const bool own = lane < splits;
-    const float* my = recs + (own ? lane : 0) * part.stride;
-    for (int r = 0; r < K; ++r) {
-      float v = (own && p < K) ? __ldcg(my + 2 + p) : -CUDART_INF_F;
-      int i = (own && p < K) ? __float_as_int(__ldcg(my + 2 + KMAX + p)) : 0x7fffffff;
-      float bv = v; int bi = i;
-      warp_best(bv, bi);
-      if (own && p < K && bv == v && bi == i) ++p;
+    __syncthreads();
+    if (warp != 0) return;
+    constexpr int kWarps = kTopkThreads / kWarp;   // 8: lanes 0..7 take one warp each
+    const bool own = lane < kWarps;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      tv[q] = own ? s_wv[own ? lane : 0][q] : -CUDART_INF_F;
+      ti[q] = own ? s_wi[own ? lane : 0][q] : 0x7fffffff;
+    }
+    m = own ? s_m[lane] : -CUDART_INF_F;
+    s = own ? s_s[lane] : 0.f;
+    tk_lane_merge(tv, ti, m, s, 1, kWarps / 2);   // lanes 0..7: the CTA's list
+    if (splits == 1) {
       if (lane == 0) {
-        ids_out[(long long)row * K + r] = bi;
-        logp_out[(long long)row * K + r] = out_logp<SAMPLE>(bv, bi, row, lse, smp);
+        const float lse = m + logf(s);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < K) {
+            ids_out[(long long)row * K + q] = ti[q];
+            logp_out[(long long)row * K + q] = out_logp<SAMPLE>(tv[q], ti[q], row, lse, smp);
+          }
+      }
+      return;
+    }
+    float* rec = part.base + ((long long)row * splits + split) * part.stride;
+    if (lane == 0) {
+      rec[0] = m;
+      rec[1] = s;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        rec[2 + q] = tv[q];
+        rec[2 + KMAX + q] = __int_as_float(ti[q]);
+      }
+      __threadfence();
+      s_last = atomicAdd(&counters[row], 1) == splits - 1;
+    }
+    __syncwarp();
+    if (!s_last) return;
+    __threadfence();
+    // the last CTA of the row: lane sp takes split sp's record (splits <= 32)
+    const bool has = lane < splits;
+    const float* my = part.base + ((long long)row * splits + (has ? lane : 0)) * part.stride;
+    m = has ? __ldcg(my) : -CUDART_INF_F;
+    s = has ? __ldcg(my + 1) : 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      tv[q] = has ? __ldcg(my + 2 + q) : -CUDART_INF_F;
+      ti[q] = has ? __float_as_int(__ldcg(my + 2 + KMAX + q)) : 0x7fffffff;
+    }
+    tk_lane_merge(tv, ti, m, s, 1, 16);
+    if (lane == 0) {
+      const float lse = m + logf(s);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < K) {
+          ids_out[(long long)row * K + q] = ti[q];
+          logp_out[(long long)row * K + q] = out_logp<SAMPLE>(tv[q], ti[q], row, lse, smp);
+        }
+      counters[row] = 0;
+    }
+  } else {
+    // ---- CTA merge: (m, s) and the K best of 256 sorted lists ----
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+      merge_ms(m, s, m2, s2);
+    }
+    if (lane == 0) { s_m[warp] = m; s_s[warp] = s; }
+    // warp tournament: every lane offers the head of its sorted list; the winner
+    // shifts its list by one, so the head always sits in register slot 0
+    for (int r = 0; r < K; ++r) {
+      float bv = tv[0]; int bi = ti[0];
+      warp_best(bv, bi);
+      if (bv == tv[0] && bi == ti[0]) {
+#pragma unroll
+        for (int j = 0; j < KMAX - 1; ++j) { tv[j] = tv[j + 1]; ti[j] = ti[j + 1]; }
+        tv[KMAX - 1] = -CUDART_INF_F; ti[KMAX - 1] = 0x7fffffff;
+      }
+      if (lane == 0) { s_wv[warp][r] = bv; s_wi[warp][r] = bi; }
+    }
+    __syncthreads();
+
+    float cm = -CUDART_INF_F, cs = 0.f;
+    if (warp == 0) {
+      for (int w = 0; w < kTopkThreads / kWarp; ++w) merge_ms(cm, cs, s_m[w], s_s[w]);
+      int p = 0;
+      for (int r = 0; r < K; ++r) {
+        float v = (lane < kTopkThreads / kWarp && p < K) ? s_wv[lane][p] : -CUDART_INF_F;
+        int i = (lane < kTopkThreads / kWarp && p < K) ? s_wi[lane][p] : 0x7fffffff;
+        float bv = v; int bi = i;
+        warp_best(bv, bi);
+        if (lane < kTopkThreads / kWarp && p < K && bv == v && bi == i) ++p;
+        if (lane == 0) { s_v[r] = bv; s_i[r] = bi; }
+        __syncwarp();
       }
     }
+
+    if (splits == 1) {
+      if (warp == 0) {
+        const float lse = cm + logf(cs);
+        for (int r = lane; r < K; r += 32) {
+          ids_out[(long long)row * K + r] = s_i[r];
+          logp_out[(long long)row * K + r] = out_logp<SAMPLE>(s_v[r], s_i[r], row, lse, smp);
+        }
+      }
+      return;
+    }
+
+    // ---- multi-split: publish the partial record, the last CTA of the row merges ----
+    float* rec = part.base + ((long long)row * splits + split) * part.stride;
+    if (warp == 0) {
+      if (lane == 0) { rec[0] = cm; rec[1] = cs; }
+      for (int r = lane; r < K; r += 32) {
+        rec[2 + r] = s_v[r];
+        rec[2 + KMAX + r] = __int_as_float(s_i[r]);
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        int prev = atomicAdd(&counters[row], 1);
+        s_last = (prev == splits - 1);
+      }
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp != 0) return;
+
+    const float* recs = part.base + (long long)row * splits * part.stride;
+    float M = -CUDART_INF_F, S = 0.f;
+    for (int sp = 0; sp < splits; ++sp)
+      merge_ms(M, S, __ldcg(recs + sp * part.stride), __ldcg(recs + sp * part.stride + 1));
+    const float lse = M + logf(S);
+    // splits <= 32 is enforced by the launcher: one split per lane
+    {
+      int p = 0;
+      const bool own = lane < splits;
+      const float* my = recs + (own ? lane : 0) * part.stride;
+      for (int r = 0; r < K; ++r) {
+        float v = (own && p < K) ? __ldcg(my + 2 + p) : -CUDART_INF_F;
+        int i = (own && p < K) ? __float_as_int(__ldcg(my + 2 + KMAX + p)) : 0x7fffffff;
+        float bv = v; int bi = i;
+        warp_best(bv, bi);
+        if (own && p < K && bv == v && bi == i) ++p;
+        if (lane == 0) {
+          ids_out[(long long)row * K + r] = bi;
+          logp_out[(long long)row * K + r] = out_logp<SAMPLE>(bv, bi, row, lse, smp);
+        }
+      }
+    }
+    if (lane == 0) counters[row] = 0;
   }
-  if (lane == 0) counters[row] = 0;
 }
 
 template <typename T, int KMAX, bool SAMPLE>
