@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
                                        "topk_b1", "tree_stress", "tree_b1", "tree_attention",
-                                       "chain_sweep", "budget_sweep"],
+                                       "chain_sweep", "budget_sweep", "steady_state"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
     return ap.parse_args()
 
@@ -508,8 +508,77 @@ def run_budget_sweep(args):
                       "rows": rows}))
 
 
+def run_steady_state(args):
+    """Chained cycles on the device at the Qwen3-8B batch-1 shape: each cycle
+    injects the previous cycle's accepted path (dflash_draft_cycle with the
+    rows, positions and features dflash_commit_accepted wrote), drafts from the
+    bonus token, builds the tree (B = 256), walks it against a device-side
+    stand-in for the target's choices, and commits.  One captured CUDA graph
+    of a cycle replayed `steps` times; the context grows by tau per cycle."""
+    from block_diffusion_speculative_kv_gb300 import binding as bd
+    from block_diffusion_speculative_kv_gb300 import synth
+    from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
+    from block_diffusion_speculative_kv_gb300.drafter import Drafter
+    torch.cuda.set_device(0)
+    wl = WORKLOADS[2]
+    s = wl.shape
+    L, D, B = wl.L, wl.L - 1, wl.B
+    n_cycles = args.steps + max(args.warmup, 3) + 3
+    ctx0 = int(wl.ctx[1])
+    cap = ctx0 + (n_cycles + 2) * L
+    w = synth.drafter_weights(s, wl.seed, device="cuda")
+    dr = Drafter(s, w, n_req=1, cap=cap, max_inject_rows=ctx0, L=L, K=wl.K)
+    fd = s.n_feat * s.d_feat
+    i32 = dict(dtype=torch.int32, device="cuda")
+    pre = synth.features(ctx0, s, wl.seed, stream=101, device="cuda")
+    dr.inject_kv(pre[:ctx0 - L], torch.tensor([0, ctx0 - L], **i32), torch.zeros(1, **i32))
+    feats = pre[ctx0 - L:].contiguous()
+    del pre
+    tree_feats = synth.features(B + 1, s, wl.seed, stream=103, device="cuda").reshape(1, B + 1, fd)
+    row_off = torch.tensor([0, L], **i32)
+    pos0 = torch.tensor([ctx0 - L], **i32)
+    ctx_len = torch.tensor([ctx0], **i32)
+    anchor = torch.as_tensor(synth.anchors(1, s.vocab, s.mask_id, wl.seed), **i32)
+    ids = torch.empty(1, D, wl.K, **i32)
+    lp = torch.empty(1, D, wl.K, dtype=torch.float32, device="cuda")
+    tree = bd.tree_buffers(1, B, "cuda")
+    al, acc, bonus = torch.empty(1, **i32), torch.empty(1, D, **i32), torch.empty(1, **i32)
+    taus = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def cycle():
+        dr.draft_cycle(feats, row_off, pos0, anchor, ctx_len, cap, ids, lp)
+        bd.ddtree_build(lp, ids, anchor, B, *tree)
+        target = synth.target_first_child(tree[0], tree[1], tree[2])
+        bd.ddtree_accept(D, B, tree[0], tree[1], tree[2], target, al, acc, bonus)
+        bd.commit_accepted(D, tree_feats, al, acc, bonus, ctx_len, anchor, row_off, pos0, feats)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        cycle()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cycle()
+    torch.cuda.synchronize()
+    c0 = int(ctx_len.item())
+    ms, clocks = timed_region(g.replay, args.steps, max(args.warmup, 3), 1)
+    c1 = int(ctx_len.item())
+    assert dr.read_status() == 0
+    cycles = args.steps + max(args.warmup, 3)
+    us = ms * 1e3 / args.steps
+    print(json.dumps({"case": "steady_state", "workload": wl.name, "cycles": cycles,
+                      "us_per_cycle": round(us, 1), "mean_tau": round((c1 - c0) / cycles, 3),
+                      "tokens_per_s_drafter_side": round((c1 - c0) / cycles / (us * 1e-6), 1),
+                      "ctx_start": c0, "ctx_end": c1, "clocks": clocks,
+                      "timed": "CUDA graph of one cycle (draft_cycle + ddtree_build + target "
+                               "stand-in + ddtree_accept + commit), replayed"}))
+
+
 def run_case(args):
     """One kernel on its own, launched back to back (inputs larger than L2)."""
+    if args.case == "steady_state":
+        return run_steady_state(args)
     if args.case == "chain_sweep":
         return run_chain_sweep(args)
     if args.case == "budget_sweep":

@@ -96,6 +96,8 @@ _SIGS = {
     "dflash_chain_tree": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ddtree_build": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ddtree_accept": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_commit_accepted": (_i, [_i, _i, _i, _i, _i, _vp, C.c_longlong, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp, _vp]),
     "dflash_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "dflash_linear_bf16": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_set_trace_hook": (None, [_vp, _vp]),
@@ -268,6 +270,17 @@ def ddtree_accept(D: int, B: int, n_nodes, tok, parent, target_tok, accept_len, 
     _check(lib().ddtree_accept(n_req, D, B, _ptr(n_nodes), _ptr(tok), _ptr(parent),
                                _ptr(target_tok), _ptr(accept_len), _ptr(accepted), _ptr(bonus),
                                _stream(stream)))
+
+
+def commit_accepted(D: int, tree_feats: torch.Tensor, accept_len, accepted, bonus, ctx_len,
+                    anchor, row_off, pos0, feats, stream=None):
+    """The accepted path into the next cycle's injection inputs (in place):
+    tree_feats [n_req, B+1, feat_dim], feats [n_req*(D+1), feat_dim]."""
+    n_req, B1, fd = tree_feats.shape
+    _check(lib().dflash_commit_accepted(n_req, D, B1 - 1, fd, _dtype_code(tree_feats),
+                                        _ptr(tree_feats), tree_feats.stride(1), _ptr(accept_len),
+                                        _ptr(accepted), _ptr(bonus), _ptr(ctx_len), _ptr(anchor),
+                                        _ptr(row_off), _ptr(pos0), _ptr(feats), _stream(stream)))
 
 
 def tree_buffers(n_req: int, B: int, device="cuda"):

@@ -213,6 +213,33 @@ dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* t
   return check_launch("chain_tree");
 }
 
+dflash_status dflash_commit_accepted(int n_req, int D, int B, int feat_dim, int dtype,
+                                    const void* tree_feats, long long tree_ld,
+                                    const int32_t* accept_len, const int32_t* accepted,
+                                    const int32_t* bonus, int32_t* ctx_len, int32_t* anchor,
+                                    int32_t* row_off, int32_t* pos0, void* feats, void* stream) {
+  DFL_REQUIRE(n_req >= 0, "n_req must be >= 0");
+  DFL_REQUIRE(D >= 1 && D <= 16, "need 1 <= D <= 16");
+  DFL_REQUIRE(B >= 0 && B <= 1024, "need 0 <= B <= 1024");
+  DFL_REQUIRE(dtype == DFLASH_F32 || dtype == DFLASH_BF16, "dtype must be F32 or BF16");
+  const int esz = dtype == DFLASH_F32 ? 4 : 2;
+  DFL_REQUIRE(feat_dim >= 1 && ((long long)feat_dim * esz) % 16 == 0,
+              "feature rows must be a multiple of 16 bytes");
+  DFL_REQUIRE(tree_ld >= feat_dim && (tree_ld * esz) % 16 == 0,
+              "tree_ld must be >= feat_dim and a multiple of 16 bytes");
+  if (n_req == 0) return DFLASH_OK;
+  DFL_REQUIRE(tree_feats && accept_len && accepted && bonus && ctx_len && anchor && row_off &&
+                  pos0 && feats,
+              "null pointer argument");
+  DFL_REQUIRE(((reinterpret_cast<uintptr_t>(tree_feats) | reinterpret_cast<uintptr_t>(feats)) &
+               15u) == 0,
+              "feature buffers must be 16-byte aligned");
+  CommitLaunch a{n_req, D, B, feat_dim * esz, tree_feats, tree_ld * esz, accept_len, accepted,
+                 bonus, ctx_len, anchor, row_off, pos0, feats};
+  launch_commit(a, static_cast<cudaStream_t>(stream));
+  return check_launch("commit_accepted");
+}
+
 dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes, const int32_t* tok,
                             const int32_t* parent, const int32_t* target_tok,
                             int32_t* accept_len, int32_t* accepted, int32_t* bonus,

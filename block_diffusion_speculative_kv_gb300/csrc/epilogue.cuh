@@ -197,6 +197,7 @@ __device__ __forceinline__ void epi_preload(const EpiParams& e, int col0, int cr
       const int kind = (col / kvd) & 1;
       const int i = (col % kvd) % e.head_dim;
       const int half = e.head_dim >> 1;
+      const int n_used = e.row_off[e.n_req];   // rows past it are computed, not stored
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) {
         const int row = crow0 + (r < nrows ? r : 0);
@@ -206,7 +207,9 @@ __device__ __forceinline__ void epi_preload(const EpiParams& e, int col0, int cr
             (kind == 0) ? e.rope[(size_t)row * half + (i % half)] : make_float2(1.f, 0.f);
         pre.a[r] = cs.x;
         pre.b[r] = cs.y;
-        pre.s[r] = (r >= nrows || pos < 0 || pos >= e.cap) ? -1 : (req * e.n_kv) * e.cap + pos;
+        pre.s[r] = (r >= nrows || row >= n_used || pos < 0 || pos >= e.cap)
+                       ? -1
+                       : (req * e.n_kv) * e.cap + pos;
       }
       break;
     }

@@ -64,6 +64,23 @@ void launch_tree_build(const TreeBuildLaunch& a, cudaStream_t st);
 // The chain of topk_ids[.][.][0] in the same layout (topk_logp unused).
 void launch_chain_tree(const TreeBuildLaunch& a, cudaStream_t st);
 
+// The accepted path into the next injection's inputs (commit.cu).
+struct CommitLaunch {
+  int n_req, D, B;
+  int row_bytes;              // bytes of one feature row (a multiple of 16)
+  const void* tree_feats;     // [n_req][B+1] rows of tree_row_bytes
+  long long tree_row_bytes;
+  const int32_t* accept_len;
+  const int32_t* accepted;
+  const int32_t* bonus;
+  int32_t* ctx_len;
+  int32_t* anchor;
+  int32_t* row_off;
+  int32_t* pos0;
+  void* feats;                // [n_req * (D+1)] rows of row_bytes
+};
+void launch_commit(const CommitLaunch& a, cudaStream_t st);
+
 struct TreeAcceptLaunch {
   int n_req, D, B;
   const int32_t* n_nodes;

@@ -195,7 +195,9 @@ dflash_status dflash_read_status(void* ws, int* device_status, void* stream);
  *   K_l,pos = RoPE(U_K,l f, pos),  V_l,pos = U_V,l f    for every layer l
  * stored at cache slot pos = pos0[r] + i of request r.
  *   row_off  int32 [n_req+1] (device) prefix offsets, row_off[0] = 0,
- *            row_off[n_req] = n_rows
+ *            row_off[n_req] <= n_rows; rows at or past row_off[n_req] are
+ *            computed but stored nowhere (a fixed n_rows can then serve a
+ *            device-side row count, as dflash_commit_accepted writes it)
  *   pos0     int32 [n_req]   (device) first cache slot written per request;
  *            pos0[r] + rows of r must not exceed cache->cap (not checked on
  *            the device: the caller guarantees it)
@@ -320,6 +322,32 @@ dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* t
                                 const int32_t* root_tok, int32_t* n_nodes, int32_t* tok,
                                 int32_t* parent, int32_t* depth, int32_t* rank, uint32_t* mask,
                                 void* stream);
+
+/* Steady state between two cycles (DFlash page, 3.4.3: verified tokens are
+ * injected as context and the cache is reused across cycles; DDTree page,
+ * 3.4.5: only the accepted path stays).  Per request r with a = accept_len[r]
+ * (ddtree_accept's outputs for this cycle's tree of budget B and depth D):
+ *   the accepted path is node 0 (this cycle's anchor) then accepted[r][0..a),
+ *   at positions ctx_len[r] .. ctx_len[r] + a;
+ *   feats row row_off[r] + i = tree_feats[r][node i of the path], i <= a
+ *   (the target's hidden features of the tree nodes, rows of feat_dim
+ *   elements, tree_ld elements apart, [n_req][B+1]);
+ *   row_off = prefix sums of a + 1 ([n_req+1]); pos0[r] = ctx_len[r];
+ *   then ctx_len[r] += a + 1 and anchor[r] = bonus[r].
+ * So a following dflash_draft_cycle with n_rows = n_req * (D+1) and these
+ * row_off / pos0 / feats appends exactly the accepted path to the cache and
+ * drafts from the bonus token; every size is on the device, so the cycle can
+ * be captured in a CUDA graph and replayed.  The drafter's block keys and
+ * values never enter the cache, so rejected positions need no rollback.
+ * Requires 1 <= D <= 16, 0 <= B <= 1024, feature rows and tree_ld multiples
+ * of 16 bytes, 16-byte aligned buffers; dtype DFLASH_BF16 or DFLASH_F32.  The
+ * caller guarantees ctx_len[r] + D + 1 <= the cache capacity (not checked on
+ * the device).  Needs no workspace. */
+dflash_status dflash_commit_accepted(int n_req, int D, int B, int feat_dim, int dtype,
+                                     const void* tree_feats, long long tree_ld,
+                                     const int32_t* accept_len, const int32_t* accepted,
+                                     const int32_t* bonus, int32_t* ctx_len, int32_t* anchor,
+                                     int32_t* row_off, int32_t* pos0, void* feats, void* stream);
 
 /* Step a8: greedy verifier walk (DDTree page, 3.4.5).  From the root, while the
  * current node has a child whose token equals target_tok[current], move to it.

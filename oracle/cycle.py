@@ -29,3 +29,35 @@ def tau_of_cycle(accept_len: int) -> int:
 def tau_bounds(gamma: int):
     """The range tau can take with gamma draft tokens per cycle: [1, gamma + 1]."""
     return 1, gamma + 1
+
+
+def commit(accept_len, accepted, bonus, ctx_len, tree_feats):
+    """Steady-state bookkeeping after one verified cycle (DFlash page, section
+    3.4.3: verified tokens enter the drafter's cache as context, the cache is
+    reused across cycles; DDTree page, section 3.4.5: only the accepted path
+    stays).
+
+    Per request r with a = accept_len[r]: the accepted path is node 0 (the
+    cycle's anchor) followed by accepted[r][:a]; it occupies positions
+    ctx_len[r] .. ctx_len[r] + a, so the next injection takes its a + 1 feature
+    rows (tree_feats[r][node]) at pos0[r] = ctx_len[r]; then the context grows
+    by a + 1 and the bonus token becomes the next anchor.
+
+    Returns (row_off [n_req+1], pos0 [n_req], feats [sum of a+1, feat_dim],
+    new ctx_len [n_req], new anchor [n_req]).
+    """
+    import numpy as np
+    n_req = len(accept_len)
+    row_off = [0]
+    pos0, rows, new_ctx, new_anchor = [], [], [], []
+    for r in range(n_req):
+        a = int(accept_len[r])
+        path = [0] + [int(x) for x in accepted[r][:a]]
+        for node in path:
+            rows.append(np.asarray(tree_feats[r][node]))
+        row_off.append(row_off[-1] + len(path))
+        pos0.append(int(ctx_len[r]))
+        new_ctx.append(int(ctx_len[r]) + a + 1)
+        new_anchor.append(int(bonus[r]))
+    return (np.array(row_off), np.array(pos0), np.stack(rows), np.array(new_ctx),
+            np.array(new_anchor))
