@@ -548,7 +548,7 @@ def run_steady_state(args):
     def cycle():
         dr.draft_cycle(feats, row_off, pos0, anchor, ctx_len, cap, ids, lp)
         bd.ddtree_build(lp, ids, anchor, B, *tree)
-        target = synth.target_first_child(tree[0], tree[1], tree[2])
+        target = synth.target_first_child(tree[0], tree[1], tree[2], s.vocab)
         bd.ddtree_accept(D, B, tree[0], tree[1], tree[2], target, al, acc, bonus)
         bd.commit_accepted(D, tree_feats, al, acc, bonus, ctx_len, anchor, row_off, pos0, feats)
 

@@ -104,7 +104,8 @@ class Loop:
         self.dr.draft_cycle(self.feats, self.row_off, self.pos0, self.anchor, self.ctx_len,
                             self.cap, self.ids, self.lp)
         bd.ddtree_build(self.lp, self.ids, self.anchor, self.B, *self.tree)
-        target = synth.target_first_child(self.tree[0], self.tree[1], self.tree[2])
+        target = synth.target_first_child(self.tree[0], self.tree[1], self.tree[2],
+                                           self.s.vocab)
         bd.ddtree_accept(self.D, self.B, self.tree[0], self.tree[1], self.tree[2], target,
                          self.al, self.acc, self.bonus)
         bd.commit_accepted(self.D, self.tree_feats, self.al, self.acc, self.bonus, self.ctx_len,
