@@ -319,8 +319,9 @@ ddtree_build_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp
 // hands the request to the exact one-pop-at-a-time path.
 // ---------------------------------------------------------------------------
 constexpr int kFastThreads = 256;
-constexpr int kFastMaxB = 512;
-constexpr int kFastMaxCand = 4096;   // B * K
+constexpr int kFastMaxB = 1024;
+constexpr int kFastMaxCand = 8192;   // candidate slots of one depth
+constexpr int kFastSmemMax = 227 * 1024;
 
 struct FastSmem {
   uint32_t* pkey[2];   // kept nodes: order-preserving score bits   [B]
@@ -344,17 +345,18 @@ __host__ __device__ inline int pow2_at_least(int x) {
   return p;
 }
 
-__host__ __device__ inline size_t fast_scratch_bytes(int K, int B) {
-  const size_t BK = (size_t)B * K, N2 = pow2_at_least(B > 0 ? B : 1);
+// cap: candidate slots of one depth (children above the current cut)
+__host__ __device__ inline size_t fast_scratch_bytes(int cap, int B) {
+  const size_t BK = (size_t)cap, N2 = pow2_at_least(B > 0 ? B : 1);
   const size_t W = (B + 1 + 31) / 32;
   return align_up(sizeof(int) * (6 * (size_t)B + 3 * BK + 2 * (size_t)B + 2 * N2 + 256 + 8), 16) +
          sizeof(uint32_t) * (kFastThreads / 32) * 32 * W;
 }
 
-__device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int K, int B) {
+__device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int cap, int B) {
   FastSmem f;
   int* q = reinterpret_cast<int*>(base);
-  const int BK = B * K, N2 = pow2_at_least(B > 0 ? B : 1);
+  const int BK = cap, N2 = pow2_at_least(B > 0 ? B : 1);
   for (int b = 0; b < 2; ++b) {
     f.pkey[b] = reinterpret_cast<uint32_t*>(q); q += B;
     f.ppar[b] = q; q += B;
@@ -378,7 +380,8 @@ __device__ __forceinline__ FastSmem carve_fast_smem(unsigned char* base, int K, 
 
 // Returns n (sm.node[0..n] filled) or -1 when the exact sequential path must
 // decide.  Every thread of the CTA calls it; all branches are CTA-uniform.
-__device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, int B, int32_t root) {
+__device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, int B, int cap,
+                          int32_t root) {
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
   int* misc = f.misc;   // [0] count, [1] fallback, [2] kept, [3] frontier, [4..6] select, [7] min
@@ -400,26 +403,70 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
   for (int d = 1; d <= D; ++d) {
     if (tid == 0) misc[0] = 0;
     __syncthreads();
-    // candidates: children of the depth d-1 nodes still kept
+    // candidates: children of the depth d-1 nodes still kept.  A depth's list
+    // is non-increasing, so the children of a kept node that clear the cut
+    // are a prefix of its ranks: count them by binary search, then lay them
+    // out by prefix sums (offsets in newpos, free until the compaction).
     const uint32_t* pk = f.pkey[cur];
-    const int pairs = n_front * K;
-    for (int q = tid; q < pairs; q += T) {
-      const int fi = f.front[q / K];
-      const int r = q - (q / K) * K;
+    const float* lpd = sm.lp + (d - 1) * K;
+    int* offs = f.newpos;
+    for (int i = tid; i < n_front; i += T) {
+      const int fi = f.front[i];
       const float ps = fi < 0 ? 0.f : from_ordered_bits(pk[fi]);
-      const uint32_t key = ordered_bits(__fadd_rn(ps, sm.lp[(d - 1) * K + r]));
-      if (full && key <= tau) {
-        if (key == tau) misc[1] = 1;
-        continue;
+      int lo = 0;
+      if (!full) {
+        lo = K;
+      } else {
+        int hi = K;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (ordered_bits(__fadd_rn(ps, lpd[mid])) > tau) lo = mid + 1;
+          else hi = mid;
+        }
+        if (lo < K && ordered_bits(__fadd_rn(ps, lpd[lo])) == tau) misc[1] = 1;
       }
-      const int slot = atomicAdd(&misc[0], 1);
-      f.ckey[slot] = key;
-      f.cpar[slot] = fi;
-      f.cdr[slot] = (d << 16) | (r + 1);
+      offs[i] = lo;
     }
     __syncthreads();
     if (misc[1]) return -1;
+    if (warp == 0) {
+      // exclusive scan of the counts: lane l sums a contiguous segment
+      const int seg = (n_front + 31) / 32;
+      const int b0 = min(lane * seg, n_front), b1 = min(b0 + seg, n_front);
+      int sum = 0;
+      for (int i = b0; i < b1; ++i) sum += offs[i];
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int run = incl - sum;
+      for (int i = b0; i < b1; ++i) {
+        const int c = offs[i];
+        offs[i] = run;
+        run += c;
+      }
+      if (lane == 31) misc[0] = incl;
+    }
+    __syncthreads();
     const int n_c = misc[0];
+    if (n_c > cap) return -1;   // more survivors than slots: the exact path decides
+    for (int q = tid; q < n_c; q += T) {
+      int lo = 0, hi = n_front - 1;   // the frontier node whose range holds q
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= q) lo = mid;
+        else hi = mid - 1;
+      }
+      const int fi = f.front[lo];
+      const int r = q - offs[lo];
+      const float ps = fi < 0 ? 0.f : from_ordered_bits(pk[fi]);
+      f.ckey[q] = ordered_bits(__fadd_rn(ps, lpd[r]));
+      f.cpar[q] = fi;
+      f.cdr[q] = (d << 16) | (r + 1);
+    }
+    __syncthreads();
     if (n_c == 0) break;
     const int total = n_p + n_c;
     if (total <= B) {
@@ -556,7 +603,7 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
 // sequential one; warp 0 writes the tree.
 template <int NSL>
 __global__ void __launch_bounds__(kFastThreads)
-ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict__ lp_g,
+ddtree_build_fast_kernel(int n_req, int D, int K, int B, int cap, const float* __restrict__ lp_g,
                          const int32_t* __restrict__ ids_g, const int32_t* __restrict__ root_tok,
                          int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ tok_out,
                          int32_t* __restrict__ parent_out, int32_t* __restrict__ depth_out,
@@ -568,13 +615,13 @@ ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict
   pdl_trigger();
   if (req >= n_req) return;
   WarpSmem sm = carve_warp_smem(smem_raw, D, K, B);
-  const FastSmem fs = carve_fast_smem(smem_raw + build_warp_bytes(D, K, B), K, B);
+  const FastSmem fs = carve_fast_smem(smem_raw + build_warp_bytes(D, K, B), cap, B);
   const float* lp_r = lp_g + (size_t)req * D * K;
   sm.ids = ids_g + (size_t)req * D * K;
   for (int i = threadIdx.x; i < D * K; i += blockDim.x) sm.lp[i] = lp_r[i];
   __syncthreads();
   const int32_t root = root_tok[req];
-  int n = fast_build(sm, fs, D, K, B, root);
+  int n = fast_build(sm, fs, D, K, B, cap, root);
   if (n < 0) {
     // (uniform: every thread saw the same flag)
     if (warp == 0) {
@@ -590,18 +637,26 @@ ddtree_build_fast_kernel(int n_req, int D, int K, int B, const float* __restrict
 
 template <int NSL>
 void launch_build_t(const TreeBuildLaunch& a, cudaStream_t st) {
-  const bool fast = a.B >= 1 && a.B <= kFastMaxB && (long long)a.B * a.K <= kFastMaxCand;
+  // candidate slots per depth: B * K when that fits, else as many as the
+  // shared memory holds (a depth with more survivors takes the exact path)
+  int cap = (long long)a.B * a.K < kFastMaxCand ? a.B * a.K : kFastMaxCand;
+  while (cap > 1024 &&
+         build_warp_bytes(a.D, a.K, a.B) + fast_scratch_bytes(cap, a.B) > (size_t)kFastSmemMax)
+    cap /= 2;
+  const size_t fast_smem = build_warp_bytes(a.D, a.K, a.B) + fast_scratch_bytes(cap, a.B);
+  const bool fast = a.B >= 1 && a.B <= kFastMaxB && cap >= a.K &&
+                    fast_smem <= (size_t)kFastSmemMax;
   TraceScope ts("ddtree_build", st);
   if (fast) {
     static bool attr_fast = false;  // per instantiation, per process
     if (!attr_fast) {
       cudaFuncSetAttribute(ddtree_build_fast_kernel<NSL>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemMax);
       attr_fast = true;
     }
-    const size_t smem = build_warp_bytes(a.D, a.K, a.B) + fast_scratch_bytes(a.K, a.B);
+    const size_t smem = fast_smem;
     launch_k(ddtree_build_fast_kernel<NSL>, dim3(a.n_req), dim3(kFastThreads), smem, st, a.n_req,
-             a.D, a.K, a.B, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
+             a.D, a.K, a.B, cap, a.topk_logp, a.topk_ids, a.root_tok, a.n_nodes, a.tok, a.parent,
              a.depth, a.rank, a.mask);
     return;
   }

@@ -273,13 +273,14 @@ def target_tokens(n_nodes: Sequence[int], depth: np.ndarray, topk_logp: np.ndarr
 # ---------------------------------------------------------------------------
 
 def target_first_child(n_nodes: torch.Tensor, tok: torch.Tensor, parent: torch.Tensor,
-                       vocab: int, agree_mod: int = 3) -> torch.Tensor:
+                       vocab: int, agree_pct: int = 90) -> torch.Tensor:
     """target_tok [n_req, B+1] for a flattened tree: at node i the token of its
-    first child in pop order (its best-scored child) when tok[i] % agree_mod is
-    not 0, else that token + 1 (or, at a leaf, the node's token + 1) modulo
-    vocab, so walks stop at data-dependent depths and the bonus token is always
-    a valid id.  Torch ops only, so a cycle that calls it can be captured in a
-    CUDA graph."""
+    first child in pop order (its best-scored child) when a multiplicative hash
+    of that child's token falls below agree_pct percent, else that token + 1
+    (or, at a leaf, the node's token + 1) modulo vocab, so walks stop at
+    data-dependent depths (each step agrees with probability about agree_pct
+    percent over random tokens) and the bonus token is always a valid id.
+    Torch ops only, so a cycle that calls it can be captured in a CUDA graph."""
     n_req, W = tok.shape
     idx = torch.arange(W, device=tok.device).expand(n_req, W)
     valid = (idx >= 1) & (idx <= n_nodes.long()[:, None])
@@ -289,6 +290,7 @@ def target_first_child(n_nodes: torch.Tensor, tok: torch.Tensor, parent: torch.T
     first = first[:, :W]
     child_tok = torch.gather(tok.long(), 1, first.clamp(max=W - 1))
     has_child = first < W
-    agree = has_child & (tok.long().remainder(agree_mod) != 0)
+    h = (child_tok * 2654435761).remainder(1 << 32) // 65536
+    agree = has_child & (h.remainder(100) < agree_pct)
     other = (torch.where(has_child, child_tok, tok.long()) + 1).remainder(vocab)
     return torch.where(agree, child_tok, other).to(torch.int32)

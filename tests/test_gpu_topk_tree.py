@@ -134,6 +134,8 @@ def _check_tree(gpu, ref_list, B):
     (4, 15, 8, 512, 0.0),      # its largest budget
     (3, 15, 8, 300, 0.0),      # a budget that is not a power of two
     (6, 15, 8, 256, 0.05),     # a few tied rows: some requests fall back
+    (2, 15, 8, 1024, 0.0),     # the largest budget, parallel construction
+    (3, 16, 8, 1024, 0.1),     # the same with some tied rows
     (2, 15, 64, 64, 0.0),      # Lemma 1's exact mode K = B: parallel construction
     (3, 15, 256, 256, 0.2),    # K = B = 256: the sequential heap, ranks above 63
     (2, 16, 1024, 1024, 0.3),  # K = B = 1024 (two requests per CTA in shared memory)
