@@ -19,7 +19,15 @@
  *   dflash_tree_attention / dflash_tree_rope
  *                       the verification pass's attention over the flattened
  *                       tree (ancestor mask, depth position ids)
- *                       (DDTree page, section 3.4.5).
+ *                       (DDTree page, section 3.4.5);
+ *   dflash_commit_accepted
+ *                       the accepted path becomes the next cycle's injected
+ *                       context (sizes stay on the device, so a whole cycle
+ *                       replays as one CUDA graph).
+ * dflash_draft_cycle runs the first two calls as one.  With a dflash_sampling
+ * the drafter draws tokens at temperature T (vanilla DFlash), and
+ * dflash_chain_tree lays the drafted block out as a chain in ddtree_build's
+ * layout.  dflash_logits_topk / dflash_logits_sample run step a6 alone.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -175,7 +183,7 @@ void dflash_model_destroy(dflash_model* model);
 
 /* Workspace bytes for calls on this model with at most n_req requests,
  * max_inject_rows feature rows per dflash_inject_kv call, block length L <= 16
- * and top-K K <= 32.  The same workspace also serves dflash_logits_topk for up
+ * and top-K K <= 1024.  The same workspace also serves dflash_logits_topk for up
  * to n_req*(L-1) rows of this model's vocabulary.  0 on invalid arguments. */
 size_t dflash_workspace_bytes(const dflash_model* model, int n_req, int max_inject_rows,
                               int L, int K);
@@ -217,7 +225,10 @@ dflash_status dflash_inject_kv(const dflash_model* model, const dflash_cache* ca
  *             cache, 0 <= ctx_len[r] <= max_ctx <= cache->cap
  *   max_ctx   host bound on ctx_len used to size the attention grid
  *   L         block length, 2 <= L <= 16; D = L-1 draft positions
- *   K         1 <= K <= 32 (and K <= vocab)
+ *   K         1 <= K <= 1024 (and K <= vocab; with sampling K <= 32).  At
+ *             batch 1 (n_req * L <= 16) and K <= 8 on bf16 models the top-K
+ *             rides in the LM head's epilogue; otherwise the logits are
+ *             stored in the workspace and a top-K pass follows
  *   topk_ids  int32 [n_req][L-1][K] (device) out: token ids by (logit desc,
  *             id asc)
  *   topk_logp fp32  [n_req][L-1][K] (device) out: logit - logsumexp(row)
@@ -250,7 +261,10 @@ dflash_status dflash_draft_cycle(const dflash_model* model, const dflash_cache* 
  *   logits  [rows][ld] of dtype (DFLASH_F32 or DFLASH_BF16), vocab <= ld
  *   ids     int32 [rows][K], logp fp32 [rows][K] (device) out; order is
  *           (logit desc, token id asc); logp = logit - logsumexp over the row
- * Requires 1 <= K <= 32, K <= vocab, rows >= 0; ws of at least
+ * Requires 1 <= K <= 1024, K <= vocab, rows >= 0 (K > 8: a two-pass radix
+ * select whose merge holds a row's per-chunk lists in shared memory, so K
+ * times the number of 16384-logit chunks is bounded; DFLASH_ERR_UNSUPPORTED
+ * beyond); ws of at least
  * dflash_topk_workspace_bytes(rows, vocab, K) bytes (zero-initialised once). */
 size_t dflash_topk_workspace_bytes(int rows, int vocab, int K);
 dflash_status dflash_logits_topk(int rows, int vocab, int ld, int dtype, const void* logits,
@@ -302,7 +316,7 @@ dflash_status dflash_logits_topk_noalloc(int rows, int vocab, int ld, int dtype,
  * Entries past node n are -1 (mask rows 0).  Scores: the candidate score is the
  * parent's score plus logp, one fp32 add; the heap pops the highest score and,
  * on equal scores, the candidate created first (each pop creates its next
- * sibling before its first child).  Requires 0 <= B <= 1024, 1 <= K <= 32,
+ * sibling before its first child).  Requires 0 <= B <= 1024, 1 <= K <= 1024,
  * 1 <= D <= 16.  Needs no workspace. */
 dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_logp,
                            const int32_t* topk_ids, const int32_t* root_tok,
@@ -317,7 +331,7 @@ dflash_status ddtree_build(int n_req, int D, int K, int B, const float* topk_log
  * i has bits 0..i.  The walk over a chain accepts the longest prefix the
  * target agrees with.  topk_ids int32 [n_req][D][K]; outputs as ddtree_build
  * (entries past node n are -1, mask rows 0).  Requires 1 <= D <= 16,
- * 1 <= K <= 32, 0 <= B <= 1024.  Needs no workspace. */
+ * 1 <= K <= 1024, 0 <= B <= 1024.  Needs no workspace. */
 dflash_status dflash_chain_tree(int n_req, int D, int K, int B, const int32_t* topk_ids,
                                 const int32_t* root_tok, int32_t* n_nodes, int32_t* tok,
                                 int32_t* parent, int32_t* depth, int32_t* rank, uint32_t* mask,
