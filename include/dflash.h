@@ -286,11 +286,12 @@ dflash_status dflash_logits_sample(int rows, int vocab, int ld, int dtype, const
  * memory when they run this step (a serving loop whose device memory is carved
  * up once at start-up and that must not call cudaMalloc afterwards, since that
  * can synchronise the device; a plugin host that passes inputs and outputs but
- * offers no scratch).  Same arguments, kernel and results as
- * dflash_logits_topk, without ws: the scratch lives in a fixed array inside the
- * library image (about 286 KB on every device that loads the library, held
- * until the process exits).  Limits: rows <= 4096, larger requests return
- * DFLASH_ERR_UNSUPPORTED.  The first call on each device looks up the array's
+ * offers no scratch).  Same arguments and results as dflash_logits_topk,
+ * without ws, for K <= 32 (always the single-pass kernel, which dflash_logits_topk
+ * uses for K <= 8 only): the scratch lives in a fixed array inside the library
+ * image (about 286 KB on every device that loads the library, held until the
+ * process exits).  Limits: rows <= 4096 and K <= 32, larger requests return
+ * DFLASH_ERR_UNSUPPORTED (rows) or DFLASH_ERR_INVALID_ARG (K).  The first call on each device looks up the array's
  * device address (cudaGetSymbolAddress) and caches it; make that first call
  * before any stream capture.  Every call on a device shares the array and
  * clears its counters first, so calls that overlap on the GPU race: order them
