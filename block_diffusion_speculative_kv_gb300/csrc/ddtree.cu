@@ -493,6 +493,7 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
     // radix select of the B-th largest key over kept + candidates
     uint32_t prefix = 0, pmask = 0;
     int need = B;
+    bool whole_bin = false;   // the chosen bin is taken whole: no cut inside it
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       for (int i = tid; i < 256; i += T) f.hist[i] = 0;
@@ -527,18 +528,24 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
       prefix |= static_cast<uint32_t>(misc[4]) << shift;
       pmask |= 0xFFu << shift;
       need -= misc[5];
+      if (misc[6] == need) {   // every key of the bin is kept: the bits below need no pass
+        whole_bin = true;
+        break;
+      }
     }
-    if (misc[6] > 1) return -1;   // equal scores at (or above) the cut: creation order decides
-    const uint32_t cut = prefix;
+    // equal scores straddling the cut: creation order decides
+    if (!whole_bin && misc[6] > 1) return -1;
+    const uint32_t cut = prefix;   // the kept keys are exactly those >= cut
     // compaction into the other buffer; accepted candidates form the next frontier
     const int nxt = cur ^ 1;
-    if (tid == 0) { misc[2] = 0; misc[3] = 0; }
+    if (tid == 0) { misc[2] = 0; misc[3] = 0; misc[7] = -1; }
     __syncthreads();
     for (int i = tid; i < total; i += T) {
       const bool old = i < n_p;
       const uint32_t key = old ? f.pkey[cur][i] : f.ckey[i - n_p];
       int slot = -1;
       if (key >= cut) {
+        atomicMin(reinterpret_cast<unsigned int*>(&misc[7]), key);   // the new B-th best
         slot = atomicAdd(&misc[2], 1);
         f.pkey[nxt][slot] = key;
         f.ppar[nxt][slot] = old ? f.ppar[cur][i] : f.cpar[i - n_p];
@@ -558,7 +565,7 @@ __device__ int fast_build(const WarpSmem& sm, const FastSmem& f, int D, int K, i
     __syncthreads();
     cur = nxt;
     full = true;
-    tau = cut;
+    tau = static_cast<uint32_t>(misc[7]);   // the smallest kept key (>= cut)
     if (n_front == 0) break;
   }
 
