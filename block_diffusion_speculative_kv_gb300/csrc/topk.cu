@@ -176,8 +176,11 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
   if (v1 > v0) {
     const int nvec = (v1 - v0) / VN;
     constexpr int U = 4;
-    constexpr int kStep = (kTopkThreads / kWarp) * 32 * U;
-    auto load_step = [&](int kb, float (&x)[U][VN], bool (&ok)[U]) {
+    // warp-uniform loop: a warp step covers U*32 consecutive vectors, lane-major
+    bool first = true;
+    for (int kb = warp * 32 * U; kb < nvec; kb += (kTopkThreads / kWarp) * 32 * U) {
+      float x[U][VN];
+      bool ok[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int idx = kb + u * 32 + lane;
@@ -191,23 +194,6 @@ topk_kernel(const T* __restrict__ logits, int rows, int vocab, long long ld, int
           for (int e = 0; e < VN; ++e) x[u][e] = -CUDART_INF_F;
         }
       }
-    };
-    // warp-uniform loop: a warp step covers U*32 consecutive vectors, lane-major;
-    // the next step's loads are issued before this step's values are used
-    bool first = true;
-    float xn[U][VN];
-    bool okn[U];
-    if (warp * 32 * U < nvec) load_step(warp * 32 * U, xn, okn);
-    for (int kb = warp * 32 * U; kb < nvec; kb += kStep) {
-      float x[U][VN];
-      bool ok[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        ok[u] = okn[u];
-#pragma unroll
-        for (int e = 0; e < VN; ++e) x[u][e] = xn[u][e];
-      }
-      if (kb + kStep < nvec) load_step(kb + kStep, xn, okn);
       float y[U][VN];
 #pragma unroll
       for (int u = 0; u < U; ++u) rank_values(x[u], y[u], VN, v0 + (kb + u * 32 + lane) * VN);
