@@ -67,7 +67,7 @@ extern "C" {
 typedef enum {
   DFLASH_OK = 0,
   DFLASH_ERR_INVALID_ARG = 1,   /* null pointer, bad size, unsupported shape    */
-  DFLASH_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement  */
+  DFLASH_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement */
   DFLASH_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required   */
   DFLASH_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed            */
   DFLASH_ERR_TIMEOUT = 5        /* device-side bounded wait expired (status word)*/
