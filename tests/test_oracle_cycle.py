@@ -91,3 +91,74 @@ def test_commit_matches_the_walk_and_eq1_tau():
         total += ctx2 - ctx
         ctx = ctx2
     assert list(ctx) == list(np.array([10, 20]) + total)
+
+
+def test_steady_state_cycles_equal_one_injection_of_the_history():
+    # Several oracle cycles at the tiny fp32 shape (inject the previous accepted
+    # path, draft, top-K, tree, walk against a first-child target, commit).  The
+    # cache they leave must equal one injection of the whole accepted history at
+    # its positions, and the next block's logits must agree: a wrong pos0, an
+    # off-by-one in tau or a path row out of order fails one of the two.
+    from block_diffusion_speculative_kv_gb300 import synth
+    from block_diffusion_speculative_kv_gb300.configs import TINY_DRAFTER
+    from oracle import ddtree as odt
+    from oracle import drafter as od
+    s = TINY_DRAFTER
+    L, K, B, D = 8, 3, 12, 7
+    w = synth.drafter_weights(s, 3)
+    ow = {k: ([od.f64(t) for t in v] if isinstance(v, list) else od.f64(v)) for k, v in w.items()}
+    dims = dict(n_layers=s.n_layers, d=s.d, n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim,
+                vocab=s.vocab, mask_id=s.mask_id, rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+    cap, ctx = 64, 10
+    fd = s.n_feat * s.d_feat
+    rng = np.random.default_rng(9)
+    ck = [np.zeros((s.n_kv, cap, s.head_dim)) for _ in range(s.n_layers)]
+    cv = [np.zeros((s.n_kv, cap, s.head_dim)) for _ in range(s.n_layers)]
+
+    def inject(rows, pos):
+        f = od.fuse_features(rows, ow["w_proj"])
+        for l in range(s.n_layers):
+            k_, v_ = od.inject_kv(f, ow["uk"][l], ow["uv"][l], pos, s.n_kv, s.head_dim,
+                                  s.rope_theta)
+            ck[l][:, pos] = k_
+            cv[l][:, pos] = v_
+
+    history = [rng.normal(size=(ctx, fd))]
+    inject(history[0], np.arange(ctx))
+    anchor, pending, pos0 = 5, None, None
+    taus = []
+    for cyc in range(4):
+        if pending is not None:
+            inject(pending, pos0 + np.arange(len(pending)))
+        logits = od.drafter_block(ow, dims, ck, cv, ctx, anchor, L)
+        ids, lp, _ = od.logits_topk(logits, K)
+        t = odt.build_tree(lp.astype(np.float32), ids.astype(np.int32), anchor, B)
+        target = np.full(B + 1, (anchor + 1) % s.vocab)
+        for i in range(t["n_nodes"] + 1):      # agree with the first child, except at odd tokens
+            ch = [c for c in range(1, t["n_nodes"] + 1) if t["parent"][c] == i]
+            if ch and t["tok"][ch[0]] % 2 == 0:
+                target[i] = t["tok"][ch[0]]
+        a, acc, bonus = odt.accept_walk(t["tok"], t["parent"], t["n_nodes"], target, D)
+        tree_feats = rng.normal(size=(1, B + 1, fd))
+        row_off, p0, rows, ctx2, anchor2 = oc.commit([a], [acc], [bonus], [ctx], tree_feats)
+        assert row_off[-1] == a + 1 and p0[0] == ctx and ctx2[0] == ctx + a + 1
+        history.append(rows)
+        pending, pos0, ctx, anchor = rows, int(p0[0]), int(ctx2[0]), int(anchor2[0])
+        taus.append(a + 1)
+    inject(pending, pos0 + np.arange(len(pending)))
+    # one injection of the whole history into a fresh cache
+    full = np.concatenate(history)
+    assert full.shape[0] == ctx == 10 + sum(taus)
+    ck_ref = [np.zeros_like(c) for c in ck]
+    cv_ref = [np.zeros_like(c) for c in cv]
+    f = od.fuse_features(full, ow["w_proj"])
+    for l in range(s.n_layers):
+        k_, v_ = od.inject_kv(f, ow["uk"][l], ow["uv"][l], np.arange(ctx), s.n_kv, s.head_dim,
+                              s.rope_theta)
+        ck_ref[l][:, :ctx] = k_
+        cv_ref[l][:, :ctx] = v_
+        assert np.allclose(ck[l], ck_ref[l], atol=1e-12) and np.allclose(cv[l], cv_ref[l], atol=1e-12)
+    a1 = od.drafter_block(ow, dims, ck, cv, ctx, anchor, L)
+    a2 = od.drafter_block(ow, dims, ck_ref, cv_ref, ctx, anchor, L)
+    assert np.allclose(a1, a2, atol=1e-12)
+    assert max(taus) > 1      # some cycle accepted a draft token
