@@ -70,3 +70,27 @@ def test_host_validation_needs_no_gpu(libpath):
                                         None) == 1, t
     s = ctypes.byref(binding.Sampling(0.0, 1, 0))
     assert lib.dflash_logits_sample(0, 100, 100, 0, None, s, 1, None, None, None, 0, None) == 0
+
+
+def test_sampling_struct_layout_matches_the_header():
+    # typedef struct { float temperature; uint64_t seed; int64_t row_offset; }
+    S = binding.Sampling
+    assert ctypes.sizeof(S) == 24
+    assert S.temperature.offset == 0 and S.seed.offset == 8 and S.row_offset.offset == 16
+    assert binding.sampling_arg(None) is None
+    a = binding.sampling_arg((0.5, -1, 7))._obj
+    assert a.temperature == 0.5 and a.seed == 2 ** 64 - 1 and a.row_offset == 7
+
+
+def test_commit_host_validation_needs_no_gpu(libpath):
+    lib = binding.lib()
+    f = lib.dflash_commit_accepted
+    # depth, budget, dtype and feature-row size are checked before any launch
+    assert f(1, 0, 8, 64, 1, None, 64, *([None] * 8), None) == 1          # D = 0
+    assert f(1, 4, 2000, 64, 1, None, 64, *([None] * 8), None) == 1       # B > 1024
+    assert f(1, 4, 8, 63, 1, None, 64, *([None] * 8), None) == 1          # 126-byte rows
+    assert f(1, 4, 8, 64, 7, None, 64, *([None] * 8), None) == 1          # bad dtype
+    assert f(1, 4, 8, 64, 1, None, 32, *([None] * 8), None) == 1          # tree_ld < feat_dim
+    assert f(1, 4, 8, 64, 1, None, 64, *([None] * 8), None) == 1          # null pointers
+    assert f(0, 4, 8, 64, 1, None, 64, *([None] * 8), None) == 0          # nothing to do
+
