@@ -341,3 +341,24 @@ def test_exact_tie_pop_order_by_creation():
     got = _node_tuples(t)
     assert got == [(1,), (2,), (1, 1), (2, 1), (1, 2), (2, 2),
                    (1, 1, 1), (2, 1, 1), (1, 2, 1), (2, 2, 1)]
+
+
+@pytest.mark.parametrize("V,D,B,seed", [(12, 4, 6, 0), (9, 3, 9, 1), (20, 5, 16, 2)])
+def test_lemma1_top_b_lists_suffice(V, D, B, seed):
+    # Lemma 1 (DDTree page, 3.4.4): the best tree of budget B only uses tokens of
+    # rank <= B at each depth, so the tree over the full sorted vocabulary (K = V)
+    # and the tree over the top-min(B, V) lists are the same tree.
+    rng = np.random.default_rng(seed)
+    raw = rng.normal(size=(D, V)) * 1.7
+    lp_full = raw - np.log(np.exp(raw).sum(axis=1, keepdims=True))
+    order = np.argsort(-lp_full, axis=1, kind="stable")
+    lp_sorted = np.take_along_axis(lp_full, order, axis=1).astype(np.float32)
+    ids_sorted = order.astype(np.int32)
+    full = odt.build_tree(lp_sorted, ids_sorted, 3, B)
+    k = min(B, V)
+    cut = odt.build_tree(lp_sorted[:, :k], ids_sorted[:, :k], 3, B)
+    for key in ("n_nodes", "tok", "parent", "depth", "rank"):
+        assert np.array_equal(np.asarray(full[key]), np.asarray(cut[key])), key
+    assert np.array_equal(full["mask"], cut["mask"])
+    # no node of the full-vocabulary tree uses a rank above B
+    assert int(np.max(full["rank"])) <= B
