@@ -484,6 +484,7 @@ dflash_status dflash_tree_rope(int n_req, int B, int n_heads, int head_dim, floa
   DFL_REQUIRE(n_req >= 0 && B >= 0 && n_heads >= 1, "bad sizes");
   if (n_req == 0) return DFLASH_OK;
   DFL_REQUIRE(head_dim >= 2 && head_dim % 2 == 0 && head_dim <= 128, "head_dim: even, <= 128");
+  DFL_REQUIRE(theta > 0.f, "rope theta must be > 0");
   DFL_REQUIRE(ld >= (long long)n_heads * head_dim, "row stride too small");
   DFL_REQUIRE(ctx_len && depth && x, "null pointer argument");
   DFL_REQUIRE(dtype == DFLASH_BF16 || dtype == DFLASH_F32, "dtype must be bf16 or f32");

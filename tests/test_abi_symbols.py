@@ -94,3 +94,30 @@ def test_commit_host_validation_needs_no_gpu(libpath):
     assert f(1, 4, 8, 64, 1, None, 64, *([None] * 8), None) == 1          # null pointers
     assert f(0, 4, 8, 64, 1, None, 64, *([None] * 8), None) == 0          # nothing to do
 
+
+def test_verify_and_linear_host_validation_needs_no_gpu(libpath):
+    lib = binding.lib()
+    N = None
+    ws = lib.dflash_tree_attention_workspace_bytes
+    assert ws(1, 32, 8, 128, 256, 8192) > 0
+    assert ws(1, 32, 8, 64, 256, 8192) == 0          # head_dim 128 only
+    assert ws(1, 30, 8, 128, 256, 8192) == 0         # n_q not a multiple of n_kv
+    ta = lib.dflash_tree_attention
+    p = ctypes.c_void_p(16)                          # never dereferenced: rejected first
+    args = lambda n_q, n_kv, hd, B, max_ctx, cap, ld: (
+        1, n_q, n_kv, hd, B, p, max_ctx, cap, p, p, p, ld, p, p, ld, p, p, p, ld, N, 0, N)
+    assert ta(*args(32, 8, 64, 256, 100, 100, 4096)) == 1     # head_dim
+    assert ta(*args(40, 8, 128, 256, 100, 100, 5120)) == 1    # 5 query heads per KV head
+    assert ta(*args(32, 8, 128, 2000, 100, 100, 4096)) == 1   # B > 1024
+    assert ta(*args(32, 8, 128, 256, 200, 100, 4096)) == 1    # max_ctx > cap
+    assert ta(*args(32, 8, 128, 256, 100, 100, 4000)) == 1    # strides
+    assert ta(*args(32, 8, 128, 256, 100, 100, 4096)) == 3    # workspace missing
+    tr = lib.dflash_tree_rope
+    assert tr(1, 8, 2, 127, 1e6, p, p, p, 256, 1, N) == 1     # odd head_dim
+    assert tr(1, 8, 2, 128, 0.0, p, p, p, 256, 1, N) == 1     # theta
+    assert tr(1, 8, 2, 128, 1e6, p, p, p, 200, 1, N) == 1     # row stride
+    assert lib.dflash_linear_workspace_bytes(16, 100, 64) == 0
+    assert lib.dflash_linear_bf16(16, 100, 64, p, p, p, N, 0, N) == 1
+    assert lib.dflash_linear_bf16(0, 128, 64, N, N, N, N, 0, N) == 0
+    assert lib.dflash_workspace_bytes(N, 1, 16, 16, 8) == 0
+
