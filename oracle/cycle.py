@@ -7,6 +7,7 @@ commits, tau, and the speedup is the autoregressive per-token latency divided by
 that.  tau counts the bonus token, so a cycle with gamma draft tokens commits
 between 1 and gamma + 1 tokens.
 """
+import numpy as np
 
 
 def per_token_latency(t_draft: float, t_verify: float, tau: float) -> float:
@@ -46,7 +47,6 @@ def commit(accept_len, accepted, bonus, ctx_len, tree_feats):
     Returns (row_off [n_req+1], pos0 [n_req], feats [sum of a+1, feat_dim],
     new ctx_len [n_req], new anchor [n_req]).
     """
-    import numpy as np
     n_req = len(accept_len)
     row_off = [0]
     pos0, rows, new_ctx, new_anchor = [], [], [], []
