@@ -6,6 +6,9 @@ Equation 1: the per-token latency of speculative decoding is the cycle time
 commits, tau, and the speedup is the autoregressive per-token latency divided by
 that.  tau counts the bonus token, so a cycle with gamma draft tokens commits
 between 1 and gamma + 1 tokens.
+
+It also holds the steady state between cycles (`commit`): the accepted path
+becomes drafter context (DFlash page, section 3.4.3; DDTree page, section 3.4.5).
 """
 import numpy as np
 
