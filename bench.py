@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
+    ap.add_argument("--oracle-cycle-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
                                        "topk_b1", "tree_stress", "tree_b1", "tree_attention",
                                        "chain_sweep", "budget_sweep", "steady_state"],
@@ -199,6 +200,7 @@ class Cycle:
         from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
         from block_diffusion_speculative_kv_gb300.drafter import Drafter
         self.bd = bd
+        self.wl_id = wid
         self.wl = wl = WORKLOADS[wid]
         self.s = s = wl.shape
         dev = "cuda"
@@ -320,60 +322,141 @@ def traffic_from_profile(kernel_src):
         return None
 
 
+class HostCycle:
+    """One request's cycle of a workload, as host arrays for the oracle.
+
+    Nothing here touches the CUDA library: the weights are either drawn on
+    the host from the workload's seed or copied from tensors the caller
+    already holds, the context cache [0, T) is a seeded N(0, 1) prefix (the
+    same distribution an injected context has), and the cycle's L newest
+    feature rows are drawn on the host."""
+
+    def __init__(self, wid, weights=None):
+        from block_diffusion_speculative_kv_gb300 import synth
+        from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
+        self.wl = wl = WORKLOADS[wid]
+        self.s = s = wl.shape
+        w = weights if weights is not None else synth.drafter_weights(s, wl.seed, device="cpu")
+        self.w = {k: ([_F64(t) for t in v] if isinstance(v, list) else _F64(v))
+                  for k, v in w.items()}
+        self.T = int(synth.context_lengths(wl)[0])
+        ks, vs = synth.cache_prefix(s, 1, self.T, wl.seed, device="cpu")
+        self.ck = [_F64(k[0]) for k in ks]
+        self.cv = [_F64(v[0]) for v in vs]
+        self.feats = _F64(synth.features(wl.L, s, wl.seed, stream=102, device="cpu"))
+        self.anchor = int(synth.anchors(1, s.vocab, s.mask_id, wl.seed)[0])
+        self.dims = dict(n_layers=s.n_layers, d=s.d, n_q=s.n_q, n_kv=s.n_kv,
+                         head_dim=s.head_dim, vocab=s.vocab, mask_id=s.mask_id,
+                         rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+
+    def run(self):
+        """One oracle cycle: inject the L newest rows, the block pass, log-softmax
+        and top-K, Algorithm 1.  Returns its wall time in seconds."""
+        from oracle import ddtree as odt
+        from oracle import drafter as od
+        s, wl = self.s, self.wl
+        t0 = time.perf_counter()
+        f = od.fuse_features(self.feats, self.w["w_proj"])
+        pos = self.T - wl.L + np.arange(wl.L)
+        for l in range(s.n_layers):
+            od.inject_kv(f, self.w["uk"][l], self.w["uv"][l], pos, s.n_kv, s.head_dim,
+                         s.rope_theta)
+        logits = od.drafter_block(self.w, self.dims, self.ck, self.cv, self.T, self.anchor,
+                                  wl.L)
+        ids, lp, _ = od.logits_topk(logits, wl.K)
+        odt.build_tree(lp.astype(np.float32), ids, self.anchor, wl.B)
+        return time.perf_counter() - t0
+
+
+class _F64:
+    """Lazy float64 view of a host tensor (bf16 has no NumPy dtype)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, i):
+        return self.t[i].float().numpy().astype(np.float64)
+
+    def __array__(self, dtype=None, copy=None):
+        return self.t.float().numpy().astype(np.float64)
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+SAMPLE_TEXT = ("one full oracle cycle of request 0 (inject of the L newest rows, every layer "
+               "over the whole context, LM head over the vocabulary, top-K, Algorithm 1), "
+               "NumPy float64; inputs built on the host (context cache: seeded N(0,1) prefix)")
+
+
+def one_core_oracle(wid, timeout_s=600):
+    """The same oracle cycle pinned to one core, in a child process whose BLAS
+    thread count is fixed before NumPy loads.  Returns seconds or an error."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+              "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-cycle-child", "--workload",
+           str(wid)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=timeout_s)
+    except subprocess.TimeoutExpired:
+        return {"error": f"over {timeout_s} s"}
+    for line in r.stdout.splitlines()[::-1]:
+        if line.startswith("{"):
+            return json.loads(line)
+    return {"error": (r.stderr or r.stdout)[-300:]}
+
+
+def oracle_cycle_child(wid):
+    """Entry of the one-core child: pin to one core, time one oracle cycle."""
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    torch.set_num_threads(1)
+    hc = HostCycle(wid)
+    dt = hc.run()
+    print(json.dumps({"seconds": dt, "cores": _cores()}))
+
+
 def cpu_baseline(cyc, budget_s):
-    """Time the CPU oracle on one request's cycle (inject of the L newest rows,
-    the block pass, log-softmax/top-K, Algorithm 1) on this host's cores."""
-    from oracle import ddtree as odt
-    from oracle import drafter as od
-
-    class F64:
-        def __init__(self, t):
-            self.t = t
-
-        def __getitem__(self, i):
-            return self.t[i].float().numpy().astype(np.float64)
-
-        def __array__(self, dtype=None, copy=None):
-            return self.t.float().numpy().astype(np.float64)
-
-    s, wl = cyc.s, cyc.wl
-    host = {k: ([F64(t.cpu()) for t in v] if isinstance(v, list) else F64(v.cpu()))
-            for k, v in cyc.w.items()}
-    ck = [F64(cyc.dr.cache_k[l][0].cpu()) for l in range(s.n_layers)]
-    cv = [F64(cyc.dr.cache_v[l][0].cpu()) for l in range(s.n_layers)]
-    feats = F64(cyc.feats[:wl.L].cpu())
-    dims = dict(n_layers=s.n_layers, d=s.d, n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim,
-                vocab=s.vocab, mask_id=s.mask_id, rope_theta=s.rope_theta, rms_eps=s.rms_eps)
-    T = int(cyc.ctx[0])
-    anchor = int(cyc.anchor[0].item())
-    t0 = time.perf_counter()
-    f = od.fuse_features(feats, host["w_proj"])
-    pos = T - wl.L + np.arange(wl.L)
-    for l in range(s.n_layers):
-        od.inject_kv(f, host["uk"][l], host["uv"][l], pos, s.n_kv, s.head_dim, s.rope_theta)
-    logits = od.drafter_block(host, dims, ck, cv, T, anchor, wl.L)
-    ids, lp, _ = od.logits_topk(logits, wl.K)
-    odt.build_tree(lp.astype(np.float32), ids, anchor, wl.B)
-    dt = time.perf_counter() - t0
-    return {"value": 1.0 / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "one full cycle of request 0 (inject of 16 rows, 5 layers over 8192 "
-                      "context entries, LM head over 151936 tokens, top-8, B=256 tree), "
-                      "NumPy float64 with its threaded BLAS; %.1f s" % dt}
+    """Time the CPU oracle on one request's cycle on this host's cores (all of
+    them, then one), with the bench's weights copied to the host and the rest
+    of the inputs built there."""
+    hc = HostCycle(cyc.wl_id, weights={k: ([t.cpu() for t in v] if isinstance(v, list)
+                                          else v.cpu()) for k, v in cyc.w.items()})
+    dt = hc.run()
+    one = one_core_oracle(cyc.wl_id, timeout_s=max(60.0, 10 * budget_s))
+    out = {"value": 1.0 / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+           "sample": SAMPLE_TEXT + "; %.1f s on all cores" % dt}
+    if "seconds" in one:
+        out["one_core"] = {"value": 1.0 / one["seconds"], "unit": UNIT, "cores": one["cores"],
+                           "seconds": round(one["seconds"], 2)}
+    else:
+        out["one_core"] = {"value": None, "error": one.get("error")}
+    return out
 
 
 def run_reference(args, rank, world):
+    """The oracle arm: full oracle cycles on the host cores, inputs built on
+    the host (the CUDA library is never loaded)."""
     if rank != 0:
         return
-    torch.cuda.set_device(0)
-    cyc = Cycle(args.workload)
+    hc = HostCycle(args.workload)
     times = []
     t_start = time.perf_counter()
     steps_done = 0
     warm = max(args.warmup, 3)
     for i in range(warm + args.steps):
-        b = cpu_baseline(cyc, args.cpu_budget_s)
+        dt = hc.run()
         if i >= warm:
-            times.append(1.0 / b["value"])
+            times.append(dt)
             steps_done += 1
         if time.perf_counter() - t_start > 240 and steps_done >= 1:
             break
@@ -382,11 +465,10 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
             "steps": steps_done, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cyc.wl.name},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": os.cpu_count(),
-                             "kind": "oracle",
-                             "sample": "full oracle cycles of request 0; steps capped to end "
-                                       "within a few minutes"},
+            "config": {"workload": hc.wl.name},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": SAMPLE_TEXT + "; steps capped to end within a few "
+                                                     "minutes"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -682,13 +764,17 @@ def run_case(args):
 
 def main():
     args = parse()
+    if args.oracle_cycle_child:
+        oracle_cycle_child(args.workload)
+        return
     if args.case:
         run_case(args)
         return
-    rank, world, local = dist_init()
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        # host-only: rank 0 times the oracle, other ranks exit without work
+        run_reference(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
         return
+    rank, world, local = dist_init()
     from block_diffusion_speculative_kv_gb300 import binding as bd
     cyc = Cycle(args.workload)
     s, wl = cyc.s, cyc.wl

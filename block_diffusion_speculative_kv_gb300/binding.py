@@ -78,6 +78,7 @@ _SIGS = {
     "dflash_workspace_bytes": (_sz, [_vp, _i, _i, _i, _i]),
     "dflash_workspace_init": (_i, [_vp, _sz, _vp]),
     "dflash_read_status": (_i, [_vp, C.POINTER(_i), _vp]),
+    "dflash_workspace_set_wait_limit": (_i, [_vp, _sz, C.c_uint64, _vp]),
     "dflash_inject_kv": (_i, [_vp, C.POINTER(Cache), _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash_draft_block": (_i, [_vp, C.POINTER(Cache), _i, _vp, _vp, _i, _i, _i,
                                 C.POINTER(Sampling), _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -181,6 +182,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def workspace_init(ws: torch.Tensor, stream=None):
     _check(lib().dflash_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def workspace_set_wait_limit(ws: torch.Tensor, limit_ns: int, stream=None):
+    _check(lib().dflash_workspace_set_wait_limit(_ptr(ws), ws.numel() * ws.element_size(),
+                                                 int(limit_ns), _stream(stream)))
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

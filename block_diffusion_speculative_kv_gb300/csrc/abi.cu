@@ -99,6 +99,17 @@ dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   return DFLASH_OK;
 }
 
+dflash_status dflash_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                              void* stream) {
+  DFL_REQUIRE(ws != nullptr && ws_bytes >= ws_header_bytes(), "workspace missing or too small");
+  // a pageable source is staged before cudaMemcpyAsync returns
+  const uint64_t v = limit_ns;
+  cudaError_t e = cudaMemcpyAsync(static_cast<char*>(ws) + 8, &v, sizeof(v),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error(DFLASH_ERR_CUDA, "set wait limit: %s", cudaGetErrorString(e));
+  return DFLASH_OK;
+}
+
 dflash_status dflash_read_status(void* ws, int* device_status, void* stream) {
   DFL_REQUIRE(ws != nullptr && device_status != nullptr, "null argument");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

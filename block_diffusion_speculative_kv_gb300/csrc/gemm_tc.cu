@@ -29,15 +29,17 @@
 //
 // Roles (7 warps): warp 0 lane 0 loads weight tiles into a multi-stage shared
 // memory ring (evict-first in L2); warp 6 lane 0 loads the matching activation
-// tiles (evict-last); both arrive on the stage's full barrier.  Warp 1 owns the
+// tiles (evict-last); each producer completes its own full barrier of the stage
+// (so that, when a CTA gives up, each can wait for exactly its own copies).  Warp 1 owns the
 // TMEM allocation and its lane 0 issues tcgen05.mma (128 x n_tile x 16, four
 // per 64-wide K block) and tcgen05.commit to release ring slots; warps 2-5
 // drain TMEM (tcgen05.ld, 32 lanes each) and run the epilogue.  A CTA's tiles
 // alternate between two TMEM accumulators, so the MMAs of the next tile never
 // wait for the epilogue of the previous one.  Every wait (mbarrier or phase
-// counter) is bounded in time; on expiry the CTA records DFLASH_ERR_TIMEOUT in
-// the status word, drains its outstanding copies and MMAs (again bounded),
-// frees TMEM and exits.
+// counter) is bounded in time (2 s, or the limit stored in the workspace
+// header by dflash_workspace_set_wait_limit); on expiry the CTA records
+// DFLASH_ERR_TIMEOUT in the status word, drains its outstanding copies and
+// MMAs (bounded by 2 s), frees TMEM and exits.
 #include <cstring>
 #include <mutex>
 
@@ -102,7 +104,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile, int tk
   L.a_off = 0;
   L.b_off = stages * kABytes;
   L.bar_off = L.b_off + stages * b_bytes;
-  const uint32_t bar_bytes = (2 * stages + 5) * 8 + 16 + 16;
+  const uint32_t bar_bytes = (3 * stages + 5) * 8 + 16 + 16;
   L.buf_off = (L.bar_off + bar_bytes + 15) / 16 * 16;
   L.scale_off = L.buf_off + kChunk * kBufLd * 4;
   L.red_off = L.scale_off + n_tile * 4;
@@ -122,18 +124,28 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v)
                : "memory");
 }
-// Wait until *p >= target (bounded; false on expiry or abort).
+// Wait until *p >= target (bounded by limit_ns; false on expiry or abort).
 // The polling thread backs off between reads: a hot loop takes issue slots
 // from the epilogue warp that shares its scheduler.
-__device__ __forceinline__ bool wait_counter(const int* p, int target, const volatile int* abort) {
+__device__ __forceinline__ bool wait_counter(const int* p, int target, const volatile int* abort,
+                                             uint64_t limit_ns) {
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     __nanosleep(32);
     if (ld_acquire(p) >= target) return true;
     if (abort && *abort) return false;
-    if (global_ns() - t0 > kTimeoutNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The wait limit of this launch: the workspace header's 64-bit field at byte 8
+// (the status word is at byte 0); 0, or anything above a minute, means the
+// default.  Only host copies write it, so it may be read before the grid
+// dependency wait.
+__device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return (v == 0 || v > 60000000000ull) ? kTimeoutNs : v;
 }
 
 
@@ -286,8 +298,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const uint32_t b_bytes = p.n_tile * 128;
   uint8_t* sA = smem + SL.a_off;
   uint8_t* sB = smem + SL.b_off;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL.bar_off);
-  uint64_t* empty = full + p.stages;
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(smem + SL.bar_off);   // weight copy landed
+  uint64_t* full_x = full_w + p.stages;                                  // activation copy landed
+  uint64_t* empty = full_x + p.stages;
   uint64_t* accf = empty + p.stages;   // [2] accumulator a holds a finished tile
   uint64_t* acce = accf + 2;           // [2] accumulator a has been drained
   uint64_t* drain = acce + 2;
@@ -308,7 +321,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      ptx::mbar_init(&full[s], 2);   // weight producer + activation producer
+      ptx::mbar_init(&full_w[s], 1);
+      ptx::mbar_init(&full_x[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -335,6 +349,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint64_t lim = wait_limit_ns(p.status);
   // Weights are never written by a kernel: the weight stream starts before the
   // previous kernel completes; everything else waits for it.
   // L2 prefetch of the residual rows the first phase's epilogue will read (a
@@ -365,6 +380,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const bool wprod = warp == 0;
       const uint64_t pol = wprod ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const uint32_t bytes = wprod ? static_cast<uint32_t>(kABytes) : b_bytes;
+      uint64_t* full = wprod ? full_w : full_x;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0;   // bit s: stage s has an issued copy
@@ -377,7 +393,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const long long u_end = c < Gk ? (long long)(c + 1) * U / Gk : 0;
         const int KB = P.kblocks;
         if (!wprod && k > 0) {
-          if (!wait_counter(&p.sync[k - 1], G, flags)) {
+          if (!wait_counter(&p.sync[k - 1], G, flags, lim)) {
             record_status(p.status, DFLASH_ERR_TIMEOUT);
             flags[0] = 1;
             break;
@@ -392,7 +408,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           // stores, delays the phase hand-over and costs more than it saves.
           const uint64_t t0 = global_ns();
           while (flags[2] < k) {
-            if (flags[0] || global_ns() - t0 > kTimeoutNs) break;
+            if (flags[0] || global_ns() - t0 > lim) break;
             __nanosleep(32);   // (the epilogue warp on this scheduler is busy)
           }
           if (flags[2] < k) {
@@ -409,7 +425,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const int kb = static_cast<int>(u - (long long)t * KB);
           const int ftile = t / P.n_rtiles;
           const int rtile = t - ftile * P.n_rtiles;
-          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, kTimeoutNs, flags)) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, lim, flags)) {
             record_status(p.status, DFLASH_ERR_TIMEOUT);
             flags[0] = 1;
             break;
@@ -423,7 +439,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
       }
       if (flags[0]) {
-        // drain: every issued copy must land before the CTA may exit
+        // drain: every copy this producer issued must land before the CTA may
+        // exit (its own barrier of the stage completes exactly then)
         for (int s = 0; s < p.stages; ++s)
           if (issued_mask & (1u << s))
             ptx::mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kTimeoutNs, nullptr);
@@ -451,7 +468,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const int acc = tile_i & 1;
           const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.n_tile);
-          if (!ptx::mbar_wait_bounded(&acce[acc], acc_phase ^ 1u, kTimeoutNs, flags)) {
+          if (!ptx::mbar_wait_bounded(&acce[acc], acc_phase ^ 1u, lim, flags)) {
             record_status(p.status, DFLASH_ERR_TIMEOUT);
             flags[0] = 1;
             break;
@@ -459,7 +476,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           ptx::tc_fence_after();
           bool ok = true;
           for (int i = 0; i < n; ++i) {
-            if (!ptx::mbar_wait_bounded(&full[stage], phase, kTimeoutNs, flags)) {
+            if (!ptx::mbar_wait_bounded(&full_w[stage], phase, lim, flags) ||
+                !ptx::mbar_wait_bounded(&full_x[stage], phase, lim, flags)) {
               record_status(p.status, DFLASH_ERR_TIMEOUT);
               flags[0] = 1;
               ok = false;
@@ -506,7 +524,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       if (k > 0) {
         // the epilogue reads what earlier phases wrote (row norms, residual)
         bool ok = true;
-        if (etid == 0) ok = wait_counter(&p.sync[k - 1], G, flags);
+        if (etid == 0) ok = wait_counter(&p.sync[k - 1], G, flags, lim);
         if (ptx::named_bar_or(1, kEpiThreads, !ok)) {
           record_status(p.status, DFLASH_ERR_TIMEOUT);
           flags[0] = 1;
@@ -574,7 +592,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         if (early && reducer) {
           bool got = true;
-          if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
+          if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags, lim);
           if (ptx::named_bar_or(1, kEpiThreads, !got)) {
             record_status(p.status, DFLASH_ERR_TIMEOUT);
             flags[0] = 1;
@@ -608,7 +626,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
         }
 
-        const bool ok = ptx::mbar_wait_bounded(&accf[acc], acc_phase, kTimeoutNs, flags);
+        const bool ok = ptx::mbar_wait_bounded(&accf[acc], acc_phase, lim, flags);
         if (!ok) {
           record_status(p.status, DFLASH_ERR_TIMEOUT);
           flags[0] = 1;
@@ -645,7 +663,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
           if (reducer && !early) {
             bool got = true;
-            if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags);
+            if (etid == 0) got = wait_counter(&P.counters[c_first], nslots - 1, flags, lim);
             if (ptx::named_bar_or(1, kEpiThreads, !got)) {
               record_status(p.status, DFLASH_ERR_TIMEOUT);
               flags[0] = 1;
@@ -763,7 +781,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           if (slot >= 0) {
             bool ok = true;
             if (etid == 0) {
-              ok = wait_counter(arrive, G, flags);
+              ok = wait_counter(arrive, G, flags, lim);
               __threadfence();
             }
             if (ptx::named_bar_or(1, kEpiThreads, !ok)) {

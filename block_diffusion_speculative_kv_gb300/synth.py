@@ -114,6 +114,24 @@ def random_gains(shape: DrafterShape, seed: int, device="cpu") -> Dict[str, obje
     }
 
 
+def tied_lm_head(shape: DrafterShape, seed: int, device="cpu") -> torch.Tensor:
+    """An LM head [V, d] whose logits tie exactly, for tie-breaking tests.
+
+    Row v has one nonzero entry, at a random column c(v), of value
+    +-{1/4, 1/2, 1}: every logit is then a single product of the normed
+    activation and a power of two (exact in fp32 whatever the summation
+    order), so tokens that share (c, value) tie bit for bit, and they sit at
+    random ids spread over the whole vocabulary."""
+    g = _gen(seed, 998, device)
+    cols = torch.randint(0, shape.d, (shape.vocab,), generator=g, device=device)
+    mag = torch.randint(0, 3, (shape.vocab,), generator=g, device=device)
+    sign = torch.randint(0, 2, (shape.vocab,), generator=g, device=device) * 2 - 1
+    vals = sign.float() * torch.pow(2.0, -mag.float())
+    w = torch.zeros(shape.vocab, shape.d, dtype=torch.float32, device=device)
+    w[torch.arange(shape.vocab, device=device), cols] = vals
+    return w.to(_torch_dtype(shape.dtype))
+
+
 def features(n_rows: int, shape: DrafterShape, seed: int, stream: int = 100,
              device="cpu") -> torch.Tensor:
     """Target hidden features [n_rows, n_feat*d_feat], N(0, 1)."""

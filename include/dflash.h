@@ -196,6 +196,22 @@ dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * *device_status receives DFLASH_OK or the first device-side error recorded. */
 dflash_status dflash_read_status(void* ws, int* device_status, void* stream);
 
+/* Set the time limit of every bounded device-side wait of the tensor-core GEMM
+ * launches that use this workspace (ring slots, the phase counters of a GEMM
+ * chain, split-tile partial sums, the fused top-K's arrivals).  The pages have
+ * no counterpart: this is the failure-detection hook.  limit_ns = 0 restores
+ * the default of 2 s; values above 60 s also mean the default.  A wait that
+ * runs out records DFLASH_ERR_TIMEOUT in the status word; the CTA then waits
+ * (up to 2 s) for its own copies and MMAs in flight, frees its tensor memory
+ * and returns, so the context stays usable.  The outputs of that call are
+ * undefined and the workspace must go through dflash_workspace_init (which
+ * also restores the default limit) before its next use.  The limit is stored
+ * in the workspace header (bytes 8..15) by an asynchronous copy on `stream`.
+ * Errors: DFLASH_ERR_INVALID_ARG for a null or too small workspace,
+ * DFLASH_ERR_CUDA if the copy cannot be queued. */
+dflash_status dflash_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                              void* stream);
+
 /* Step a1 + a2: KV injection (DFlash page, 3.4.3).
  * For each request r and each of its feature rows i (global row
  * row_off[r] + i, i < row_off[r+1] - row_off[r]):

@@ -4,12 +4,16 @@ same seeded inputs.
 
 Tolerances (from the pages' bar and the arithmetic): logits per row
 max|l_gpu - l_ora| / max|l_ora| <= 2e-2 for bf16 models, 1e-4 for fp32;
-injected cache entries the same per (layer, position).  The top-K sets may
-differ only by tokens whose oracle logit lies within delta of the oracle's
-K-th logit, delta = 2 * (that row's max logit error) + 1e-3 nats: both sides
-take the top-K decision on their own logits, so the decision can only flip
-where the logit error can reach (the 1e-3 nat tie window applies to identical
-logits, checked in test_gpu_topk_tree)."""
+injected cache entries the same per (layer, position).
+
+Top-K, two checks.  (1) On identical logits: the oracle's log-softmax/top-K
+of the fp32 logits the GPU itself returned must give the GPU's ids bit for
+bit (ties to the smaller id) and its log-probs within 1e-5 nats.  The fused
+LM-head fold ranks exactly the values it stores, so this holds the in-path
+kernel to the exact bar.  (2) End to end: against the oracle's own logits
+the sets may differ only by tokens whose oracle logit lies within delta of
+the oracle's K-th logit, delta = 2 * (that row's max logit error) + 1e-3
+nats, since each side decides on its own logits."""
 import numpy as np
 import pytest
 import torch
@@ -104,7 +108,15 @@ def test_inject_matches_oracle(wid, rows_per_req, pos0):
 # the block pass
 # ---------------------------------------------------------------------------
 
+def _check_topk_on_own_logits(gpu_logits, gpu_ids, gpu_lp, K):
+    o_ids, o_lp, _ = od.logits_topk(gpu_logits, K)
+    bad = np.nonzero(np.any(o_ids != gpu_ids, axis=1))[0]
+    assert bad.size == 0, (bad[:4].tolist(), o_ids[bad[:1]].tolist(), gpu_ids[bad[:1]].tolist())
+    assert np.max(np.abs(gpu_lp - o_lp)) <= 1e-5, float(np.max(np.abs(gpu_lp - o_lp)))
+
+
 def _check_logits_topk(ref_logits, gpu_logits, gpu_ids, gpu_lp, K, tolerance):
+    _check_topk_on_own_logits(gpu_logits, gpu_ids, gpu_lp, K)
     rows = ref_logits.shape[0]
     err = np.max(np.abs(gpu_logits - ref_logits), axis=1)
     scale = np.max(np.abs(ref_logits), axis=1)
@@ -122,14 +134,17 @@ def _check_logits_topk(ref_logits, gpu_logits, gpu_ids, gpu_lp, K, tolerance):
         assert np.all(np.diff(gpu_lp[r]) <= 0)
 
 
-def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None, K=None):
+def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None, K=None, ctx=None,
+                tied_head=False):
     wl = WORKLOADS[wid]
     s = wl.shape
     K = wl.K if K is None else K
     w = synth.drafter_weights(s, wl.seed, device=DEV)
     if gains:
         w.update(synth.random_gains(s, wl.seed, device=DEV))
-    ctx = synth.context_lengths(wl)
+    if tied_head:
+        w["lm_head"] = synth.tied_lm_head(s, wl.seed, device=DEV)
+    ctx = synth.context_lengths(wl) if ctx is None else np.asarray(ctx, dtype=np.int32)
     max_ctx = int(ctx.max())
     dr = Drafter(s, w, n_req=wl.n_req, cap=wl.cap, max_inject_rows=0, L=wl.L, K=K,
                  anchor_sees_block=anchor_sees_block)
@@ -194,6 +209,24 @@ def test_draft_qwen3_4b_shape_anchor_isolated():
 
 def test_draft_qwen3_8b_shape_long_context():
     _draft_case(2)
+
+
+@pytest.mark.parametrize("wid,ctx", [
+    (1, [0]),      # no context at all: the block attends to itself only
+    (1, [37]),     # a context shorter than one 64-key attention tile
+    (0, [0]),      # the fp32 model without context
+    (0, [5]),
+])
+def test_draft_empty_and_short_context(wid, ctx):
+    _draft_case(wid, ctx=ctx)
+
+
+@pytest.mark.parametrize("K", [8, 5])
+def test_draft_fused_topk_exact_ties(K):
+    # a sparse power-of-two LM head: equal logits recur, bit for bit, at ids
+    # spread over every CTA's vocabulary range, so the fold's tie-break by id
+    # and its cross-CTA merges decide the top-K
+    _draft_case(1, K=K, tied_head=True)
 
 
 def test_draft_batched_ragged_sampled():

@@ -1,7 +1,13 @@
 """The allocation-free top-K entry point (for callers that cannot allocate
 device memory when they run this step, e.g. a serving loop that must not call
 cudaMalloc after start-up) gives the same results as the workspace variant,
-on two calls in a row, through the C ABI.
+on two calls in a row, through the C ABI, and matches the oracle: ids bit
+for bit (ties to the smaller id), log-probs within 1e-5 nats.
+
+K <= 8 runs the same kernel as the workspace variant; 8 < K <= 32 runs the
+single-pass 32-entry kernel, which only this entry point reaches (the
+workspace variant sends K > 8 to the two-pass radix select), so those cases
+are compared with the oracle alone.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test."""
@@ -10,8 +16,30 @@ import pytest
 import torch
 
 from block_diffusion_speculative_kv_gb300 import binding as bd
+from oracle import drafter as od
 
 pytestmark = pytest.mark.gpu
+
+
+def _logits(rows, V, dtype, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    # N(0, 4) rounded to bf16 repeats values often: exact ties are common
+    return (torch.randn(rows, V, generator=g, device="cuda") * 2.0).to(dtype)
+
+
+def _run_noalloc(x, K):
+    rows = x.shape[0]
+    ids = torch.full((rows, K), -1, dtype=torch.int32, device="cuda")
+    lp = torch.full((rows, K), float("nan"), dtype=torch.float32, device="cuda")
+    bd.logits_topk_noalloc(x, K, ids, lp)
+    torch.cuda.synchronize()
+    return ids, lp
+
+
+def _check_oracle(x, ids, lp, K):
+    o_ids, o_lp, _ = od.logits_topk(x.float().cpu().numpy(), K)
+    assert np.array_equal(ids.cpu().numpy(), o_ids)
+    assert np.max(np.abs(lp.cpu().numpy() - o_lp)) <= 1e-5
 
 
 @pytest.mark.parametrize("rows,V,K,dtype", [
@@ -19,19 +47,33 @@ pytestmark = pytest.mark.gpu
     (300, 4099, 5, torch.bfloat16),     # one CTA per row, ragged vocabulary
 ])
 def test_noalloc_topk_matches_workspace_variant(rows, V, K, dtype):
-    g = torch.Generator(device="cuda").manual_seed(rows + K)
-    x = (torch.randn(rows, V, generator=g, device="cuda") * 2.0).to(dtype)
+    x = _logits(rows, V, dtype, rows + K)
     ids_ref = torch.empty(rows, K, dtype=torch.int32, device="cuda")
     lp_ref = torch.empty(rows, K, dtype=torch.float32, device="cuda")
     ws = torch.zeros(bd.topk_workspace_bytes(rows, V, K), dtype=torch.uint8, device="cuda")
     bd.logits_topk(x, K, ids_ref, lp_ref, ws)
     for _ in range(2):
-        ids = torch.full((rows, K), -1, dtype=torch.int32, device="cuda")
-        lp = torch.full((rows, K), float("nan"), dtype=torch.float32, device="cuda")
-        bd.logits_topk_noalloc(x, K, ids, lp)
-        torch.cuda.synchronize()
+        ids, lp = _run_noalloc(x, K)
         assert torch.equal(ids, ids_ref)
         assert np.allclose(lp.cpu().numpy(), lp_ref.cpu().numpy(), atol=1e-5, rtol=0)
+    _check_oracle(x, ids, lp, K)
+
+
+@pytest.mark.parametrize("rows,V,dtype", [
+    (15, 151936, torch.float32),
+    (300, 4099, torch.bfloat16),
+])
+@pytest.mark.parametrize("K", [9, 16, 32])
+def test_noalloc_topk_wide_k_matches_oracle(rows, V, dtype, K):
+    x = _logits(rows, V, dtype, 7 * rows + K)
+    first = None
+    for _ in range(2):
+        ids, lp = _run_noalloc(x, K)
+        _check_oracle(x, ids, lp, K)
+        if first is None:
+            first = (ids.clone(), lp.clone())
+        else:
+            assert torch.equal(ids, first[0]) and torch.equal(lp, first[1])
 
 
 def test_noalloc_topk_rejects_too_many_rows():
