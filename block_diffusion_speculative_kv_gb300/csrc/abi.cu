@@ -163,6 +163,7 @@ static dflash_status logits_topk_impl(int rows, int vocab, int ld, int dtype, co
                                     align_up(sizeof(int) * (size_t)rows, 256));
   a.ids = ids; a.logp = logp;
   a.inv_t = smp.inv_t; a.t = smp.t; a.seed = smp.seed; a.row0 = smp.row0;
+  a.status = static_cast<int*>(ws);
   if (K > 8 && smp.inv_t == 0.f) {
     const dflash_status ls = launch_topk_large(a, a.part, static_cast<cudaStream_t>(stream));
     if (ls) return ls;

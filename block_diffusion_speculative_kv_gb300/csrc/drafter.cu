@@ -526,6 +526,7 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
   tk.t = smp.t;
   tk.seed = smp.seed;
   tk.row0 = smp.row0;
+  tk.status = c.status;
   if (K > 8 && !sampling) {
     st = launch_topk_large(tk, c.ws + W.tpart, c.st);
     if (st) return st;

@@ -35,8 +35,14 @@ struct TopkLaunch {
   float inv_t, t;
   uint64_t seed;
   long long row0;
+  int* status;    // workspace status word for a bounded wait that runs out, or null
 };
 int topk_splits(int rows, int vocab);
+// K <= 8 without sampling, 16-byte aligned rows (topk_stream.cu): the streamed
+// pass; launch_topk takes it whenever topk_stream_supported holds.
+bool topk_stream_supported(const TopkLaunch& a);
+int topk_stream_workers();   // pieces the streamed pass works on at once (its warps)
+void launch_topk_stream(const TopkLaunch& a, cudaStream_t st);
 // K in (32, 1024] (topk_large.cu): two passes, partial records in `part` of
 // topk_large_part_bytes bytes (no zeroing needed); plain top-K only.
 int topk_large_splits(int vocab);

@@ -4,6 +4,10 @@
 // section 3.4.2 (q_i = softmax(l_i)) and section 3.4.4 (Lemma 1: only the
 // top-K tokens of each depth are needed, ranked by descending probability).
 //
+// This file serves temperature sampling and 8 < K <= 32; the plain top-K
+// with K <= 8 on 16-byte aligned rows takes the streamed pass of
+// topk_stream.cu (launch_topk dispatches).
+//
 // Design (HBM-bound): each row of logits is split into `splits` contiguous
 // chunks, one CTA per chunk.  A CTA streams its chunk once with 16-byte loads
 // (8 bf16 or 4 fp32 per load), keeping per thread a running (max, sum of exp)
@@ -421,11 +425,13 @@ void launch_topk_t(const TopkLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
+// Pieces per row: one row per piece once the rows fill every worker of the
+// streamed pass (a warp), else as many pieces as the workers take (at most 32
+// per row, each at least a few thousand logits).
 int topk_splits(int rows, int vocab) {
   if (rows <= 0) return 1;
-  int s = ceil_div(2 * num_sms(), rows);
+  int s = topk_stream_workers() / rows;
   s = s < 1 ? 1 : (s > 32 ? 32 : s);
-  // keep every split at least a few thousand elements
   while (s > 1 && vocab / s < 4096) --s;
   return s;
 }
@@ -437,6 +443,10 @@ size_t topk_part_bytes(int rows, int splits) {
 
 void launch_topk(const TopkLaunch& a, cudaStream_t st) {
   if (a.rows <= 0) return;
+  if (topk_stream_supported(a)) {
+    launch_topk_stream(a, st);
+    return;
+  }
   const bool k8 = a.K <= 8;
   const bool smp = a.inv_t > 0.f;
   if (a.dtype == DFLASH_BF16) {

@@ -63,6 +63,44 @@ def test_topk_matches_oracle(rows, V, K, dtype, pad):
 
 
 @pytest.mark.parametrize("rows,V,K,dtype,pad", [
+    (7, 150003, 8, torch.bfloat16, 5),       # split rows, a last piece ending mid-vector
+    (500, 30011, 8, torch.bfloat16, 5),      # more rows than CTAs: second pieces per CTA
+    (700, 16384, 3, torch.float32, 0),       # several rows per CTA, one stage per row
+    (2, 151936, 8, torch.float32, 0),        # fp32 rows split across many CTAs
+])
+def test_topk_streamed_pass_matches_oracle(rows, V, K, dtype, pad):
+    # K <= 8 on rows whose stride is a multiple of 16 bytes: the pass that
+    # streams the logits through shared memory
+    g = torch.Generator().manual_seed(rows * 13 + K)
+    x = torch.randn(rows, V, generator=g) * 2.0
+    x = torch.round(x * 4) / 4            # exact ties inside and across pieces
+    x = x.to(dtype)
+    ids, lp = _gpu_topk(x, K, pad=pad)
+    o_ids, o_lp = _oracle_topk(x, K)
+    assert np.array_equal(ids, o_ids)
+    assert np.allclose(lp, o_lp, atol=1e-5, rtol=0)
+
+
+def test_topk_masked_logits():
+    # most logits -inf (masked tokens): the -inf ones never outrank a finite
+    # one, and a row with fewer than K finite logits completes its list with
+    # the smallest -inf ids
+    rows, V, K = 6, 40000, 8
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(rows, V, generator=g) * 2.0
+    keep = torch.rand(rows, V, generator=g) < 0.05
+    keep[5] = False
+    keep[5, [7, 30000, 39999]] = True     # three finite logits only
+    x = torch.where(keep, x, torch.full_like(x, float("-inf")))
+    ids, lp = _gpu_topk(x, K)
+    o_ids, o_lp = _oracle_topk(x, K)
+    assert np.array_equal(ids, o_ids)
+    fin = np.isfinite(o_lp)
+    assert np.array_equal(np.isfinite(lp), fin)
+    assert np.allclose(lp[fin], o_lp[fin], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("rows,V,K,dtype,pad", [
     (15, 151936, 64, torch.float32, 0),      # one drafted block, K above the small-K kernels
     (15, 151936, 1024, torch.bfloat16, 0),   # Lemma 1's exact mode at B = 1024
     (3, 5000, 1024, torch.float32, 1),       # one chunk per row, unaligned rows
