@@ -55,9 +55,14 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' sub-records")
     ap.add_argument("--cpu-budget-s", type=float, default=60.0)
     ap.add_argument("--oracle-cycle-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "topk_stress",
+    ap.add_argument("--topk-rows", type=int, default=0,
+                    help="topk_stress: time only the first N rows (a smaller profiling case)")
+    ap.add_argument("--case", choices=["lm_head_gemm", "down_gemm", "o_gemm", "gate_up_gemm_b32",
+                                       "lm_head_gemm_b32", "o_gemm_b32", "topk_stress",
                                        "topk_b1", "tree_stress", "tree_b1", "tree_attention",
                                        "chain_sweep", "budget_sweep", "steady_state"],
                     default=None, help="time one kernel alone (microbenchmark / ncu target)")
@@ -236,11 +241,11 @@ class Cycle:
         torch.cuda.synchronize()
         self.target = None
 
-    def run(self):
+    def run(self, sampling=None):
         # inject + draft as one C-ABI call (the injection's GEMMs share a
         # launch with the first QKV projection), then the tree
         self.dr.draft_cycle(self.feats, self.row_off, self.pos0, self.anchor, self.ctx_len,
-                            self.max_ctx, self.ids, self.lp)
+                            self.max_ctx, self.ids, self.lp, sampling=sampling)
         self.bd.ddtree_build(self.lp, self.ids, self.anchor, self.wl.B, *self.tree)
 
     def make_targets(self):
@@ -677,9 +682,14 @@ def run_case(args):
     from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda").manual_seed(1)
-    if args.case in ("lm_head_gemm", "down_gemm", "o_gemm"):
+    if args.case in ("lm_head_gemm", "down_gemm", "o_gemm", "gate_up_gemm_b32",
+                     "lm_head_gemm_b32", "o_gemm_b32"):
+        # batch 1 (16 rows) and the 32-request batch (512 rows) of the
+        # Qwen3-8B-shaped drafter
         M, N, K = {"lm_head_gemm": (16, 151936, 4096), "down_gemm": (16, 4096, 12288),
-                   "o_gemm": (16, 4096, 4096)}[args.case]
+                   "o_gemm": (16, 4096, 4096), "gate_up_gemm_b32": (512, 24576, 4096),
+                   "lm_head_gemm_b32": (480, 151936, 4096),
+                   "o_gemm_b32": (512, 4096, 4096)}[args.case]
         copies = max(1, int(math.ceil(400e6 / (2 * N * K))))   # rotate > L2 of weights
         X = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
         Ws = [torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
@@ -697,6 +707,8 @@ def run_case(args):
         logits, _ = synth.stress_logits(wl.n_req, wl.D, wl.vocab, wl.seed, device="cuda")
         if args.case == "topk_b1":   # the 8B batch-1 drafter's 15 rows of fp32 logits
             logits = logits[:15].float().contiguous()
+        elif args.topk_rows:
+            logits = logits[:args.topk_rows].contiguous()
         rows = logits.shape[0]
         ids = torch.empty(rows, wl.K, dtype=torch.int32, device="cuda")
         lp = torch.empty(rows, wl.K, device="cuda")
@@ -756,10 +768,133 @@ def run_case(args):
            "clocks": clocks}
     if nbytes:
         out["gbs"] = round(nbytes / (us * 1e-6) / 1e9, 1)
+    if args.case.endswith("_gemm") or args.case.endswith("_b32"):
+        if args.case.startswith(("lm_head", "down", "o_", "gate_up")):
+            out["tflops"] = round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)
     if args.case == "tree_attention":
         out["tflops"] = round(flops / (us * 1e-6) / 1e12, 1)
         out["nodes"] = nn + 1
     print(json.dumps(out))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        pk = json.load(open(path))
+        return (float(pk["hbm_gbs"]), float(pk["bf16_tflops"]),
+                float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def gemm_flops_algorithmic(s, wl):
+    """FLOPs of one cycle's GEMMs that the method needs: every projection over
+    the n_req*L block rows, the LM head over the n_req*(L-1) drafted rows."""
+    R = wl.n_req * wl.L
+    f = 0
+    for name, M, N, K in gemm_shapes(s, R, R):
+        f += 2 * (wl.n_req * (wl.L - 1) if name == "lm_head" else M) * N * K
+    return f
+
+
+def sub_cycle_record(wid, steps, warmup, sampling=None, cyc=None):
+    """One more workload's drafter cycle (CUDA-graph replays) with its roofline.
+    With `sampling` = (T, seed) the cycle is vanilla DFlash drafting at
+    temperature T: one Gumbel-max draw per block position inside the LM-head
+    pass, laid out as a chain (DDTree's own tree does not depend on T: the
+    temperature only changes how the target picks its tokens)."""
+    hbm, tc, tc_sus, src = _peaks()
+    own = cyc is None
+    if own:
+        cyc = Cycle(wid)
+    s, wl = cyc.s, cyc.wl
+    if sampling:
+        bd = cyc.bd
+        D = wl.L - 1
+        i32 = dict(dtype=torch.int32, device="cuda")
+        c_ids = torch.empty(wl.n_req, D, 1, **i32)
+        c_lq = torch.empty(wl.n_req, D, 1, dtype=torch.float32, device="cuda")
+        c_tree = bd.tree_buffers(wl.n_req, D, "cuda")
+
+        def fn():
+            cyc.dr.draft_cycle(cyc.feats, cyc.row_off, cyc.pos0, cyc.anchor, cyc.ctx_len,
+                               cyc.max_ctx, c_ids, c_lq, K=1, sampling=sampling)
+            bd.chain_tree(c_ids, cyc.anchor, D, *c_tree)
+    else:
+        fn = cyc.run
+    ms, clocks = graph_time(fn, steps, warmup)
+    us = ms * 1e3 / steps
+    if cyc.dr.read_status() != 0:
+        raise RuntimeError("device status after the timed cycles")
+    kern = traced_us(fn)
+    nbytes, _ = algorithmic_bytes(s, wl, cyc.ctx)
+    rec = {"workload": wl.name, "n_req": wl.n_req, "us_per_cycle": round(us, 1),
+           "cycles_per_s": round(1e6 / us, 2), "request_drafts_per_s": round(wl.n_req * 1e6 / us, 1),
+           "cycle_hbm": {"algorithmic_bytes": int(nbytes),
+                         "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                         "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4)},
+           "kernel_us_per_cycle": kern, "clocks": clocks,
+           "timed": "CUDA graph of inject + draft + top-K + DDTree build, replayed"}
+    if sampling:
+        rec["sampling"] = {"temperature": sampling[0], "seed": sampling[1],
+                           "drafter": "vanilla DFlash chain, K = 1 Gumbel-max draw per position"}
+        rec["timed"] = "CUDA graph of inject + draft + sampling + chain tree, replayed"
+    if wl.n_req > 1:
+        flops = gemm_flops_algorithmic(s, wl)
+        g_us = kern.get("gemm_tc", float("nan"))
+        tfl = flops / (g_us * 1e-6) / 1e12
+        rec["gemm"] = {"bound": "tensor", "kernel": "gemm_tc", "flops_per_cycle": int(flops),
+                       "us_per_cycle": g_us, "achieved": round(tfl, 1), "unit": "TFLOP/s",
+                       "peak": tc_sus, "peak_source": src + " (sustained: the GEMMs run inside "
+                                                             "a multi-ms cycle)",
+                       "frac": round(tfl / tc_sus, 4), "frac_of_burst": round(tfl / tc, 4)}
+        a_us = kern.get("attn_split", 0.0) + kern.get("attn_combine", 0.0)
+        kv = int(np.sum(cyc.ctx)) * s.n_layers * 2 * s.kv_dim * 2
+        if a_us > 0:
+            rec["attention"] = {"kv_bytes_per_cycle": kv, "us_per_cycle": round(a_us, 1),
+                                "achieved_gbs": round(kv / (a_us * 1e-6) / 1e9, 1),
+                                "frac": round(kv / (a_us * 1e-6) / 1e9 / hbm, 4)}
+    if own:
+        cyc.dr.close()
+        del cyc
+        torch.cuda.empty_cache()
+    return rec
+
+
+def stress_record(steps, warmup):
+    """The top-K + tree stress workload: 256 requests x 16 positions x 151936 bf16
+    logits, top-8 per row (HBM-bound read), then a B = 512 tree per request."""
+    from block_diffusion_speculative_kv_gb300 import binding as bd
+    from block_diffusion_speculative_kv_gb300 import synth
+    from block_diffusion_speculative_kv_gb300.configs import WORKLOADS
+    hbm, _, _, src = _peaks()
+    wl = WORKLOADS[4]
+    logits, _ = synth.stress_logits(wl.n_req, wl.D, wl.vocab, wl.seed, device="cuda")
+    rows = logits.shape[0]
+    ids = torch.empty(rows, wl.K, dtype=torch.int32, device="cuda")
+    lp = torch.empty(rows, wl.K, device="cuda")
+    ws = torch.zeros(bd.topk_workspace_bytes(rows, wl.vocab, wl.K), dtype=torch.uint8,
+                     device="cuda")
+    ms_t, clk_t = timed_region(lambda: bd.logits_topk(logits, wl.K, ids, lp, ws), steps, warmup, 1)
+    us_t = ms_t * 1e3 / steps
+    nbytes = logits.numel() * logits.element_size()
+    gbs = nbytes / (us_t * 1e-6) / 1e9
+    lp3 = lp.reshape(wl.n_req, wl.D, wl.K)
+    id3 = ids.reshape(wl.n_req, wl.D, wl.K)
+    roots = torch.zeros(wl.n_req, dtype=torch.int32, device="cuda")
+    bufs = bd.tree_buffers(wl.n_req, wl.B, "cuda")
+    ms_b, _ = timed_region(lambda: bd.ddtree_build(lp3, id3, roots, wl.B, *bufs), steps, warmup, 1)
+    if bd.read_status(ws) != 0:
+        raise RuntimeError("device status after the stress top-K")
+    rec = {"workload": wl.name, "rows": rows, "vocab": wl.vocab, "K": wl.K, "B": wl.B,
+           "topk": {"us_per_launch": round(us_t, 2), "bytes": int(nbytes),
+                    "achieved_gbs": round(gbs, 1), "peak": hbm, "peak_source": src,
+                    "frac": round(gbs / hbm, 4), "clocks": clk_t,
+                    "l2": "1.245 GB of logits per launch, larger than L2"},
+           "tree_us_per_launch": round(ms_b * 1e3 / steps, 2),
+           "tree_nodes_mean": round(float(bufs[0].float().mean().item()), 1)}
+    del logits
+    torch.cuda.empty_cache()
+    return rec
 
 
 def main():
@@ -895,6 +1030,20 @@ def main():
     ms_e2e_total, _ = timed_region(e2e_step, args.steps, 3, world)
     ms_e2e = max_over_ranks(ms_e2e_total / args.steps, world)
 
+    # ---- the other workloads, as sub-records of this line ----
+    configs = {}
+    if rank == 0 and not args.no_configs and args.workload == 2:
+        w = max(args.warmup, 3)
+        subs = [("qwen3_8b_b1_t1", lambda: sub_cycle_record(2, args.steps, w, (1.0, 12345), cyc)),
+                ("qwen3_4b_b1", lambda: sub_cycle_record(1, args.steps, w)),
+                ("qwen3_8b_batch32", lambda: sub_cycle_record(3, max(3, args.steps // 2), w)),
+                ("stress", lambda: stress_record(args.steps, w))]
+        for name, f in subs:
+            try:
+                configs[name] = f()
+            except Exception as ex:  # report, do not hide
+                configs[name] = {"error": f"{type(ex).__name__}: {ex}"}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
@@ -928,6 +1077,7 @@ def main():
         "gpu_launches": launches_per_cycle * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line))
