@@ -408,9 +408,10 @@ dflash_status ddtree_accept(int n_req, int D, int B, const int32_t* n_nodes,
  *   out  bf16 [n_req][B+1][out_ld]: rows of nodes past n_nodes[r] are zero
  * Requires head_dim == 128, n_q a multiple of n_kv with at most 4 query heads
  * per KV head, 0 <= B <= 1024, 0 <= ctx_len[r] <= max_ctx <= cap, strides that
- * are multiples of 8 elements.  Device pointers; ws of
- * dflash_tree_attention_workspace_bytes(...) bytes (no initialisation needed);
- * all of it is written on the given stream. */
+ * are multiples of 8 elements and 16-byte aligned cache, q, k and v.  Device
+ * pointers; ws of dflash_tree_attention_workspace_bytes(...) bytes, zeroed once
+ * (dflash_workspace_init) before the first call: it holds arrival counters that
+ * every call leaves at zero.  Calls sharing a workspace must not overlap. */
 size_t dflash_tree_attention_workspace_bytes(int n_req, int n_q, int n_kv, int head_dim, int B,
                                              int max_ctx);
 dflash_status dflash_tree_attention(int n_req, int n_q, int n_kv, int head_dim, int B,

@@ -138,6 +138,49 @@ def test_tree_attention_target_shape_sampled():
     _check_rows(d, out, rows)
 
 
+def test_tree_attention_target_shape_full_heads():
+    # every node of two heads at the Qwen3-8B target shape: all nine query
+    # tiles (the last holds one node), both context chunks and the tree keys
+    d = _case(5, n_req=1, n_q=32, n_kv=8, B=256, ctxs=[8192], cap=8192, D=15, K=8)
+    out = _run(d)
+    nn = int(d["n_nodes"][0])
+    _check_rows(d, out, [(0, i, h) for i in range(nn + 1) for h in (7, 28)])
+    assert torch.count_nonzero(out[0, nn + 1:]) == 0
+
+
+def test_tree_attention_two_heads_per_group_nan_past_context():
+    # G = 2 (rows 64..127 of each tile unused); cache slots past each request's
+    # context hold NaN: masked scores and zeroed value rows keep them out
+    d = _case(6, n_req=2, n_q=16, n_kv=8, B=100, ctxs=[500, 1061], cap=1200, D=6, K=5)
+    for r, c in enumerate(d["ctx"]):
+        d["ck"][r, :, int(c):] = float("nan")
+        d["cv"][r, :, int(c):] = float("nan")
+    out = _run(d)
+    assert torch.isfinite(out.float()).all()
+    rows = []
+    for r in range(2):
+        nn = int(d["n_nodes"][r])
+        rows += [(r, i, h) for i in sorted({0, 1, 31, 32, nn}) if i <= nn for h in (0, 3, 15)]
+        assert torch.count_nonzero(out[r, nn + 1:]) == 0
+    _check_rows(d, out, rows)
+
+
+def test_tree_attention_large_tree():
+    # B = 1024: 1025 nodes, 33 mask words per row, up to nine tiles of tree keys
+    d = _case(7, n_req=1, n_q=8, n_kv=2, B=1024, ctxs=[300], cap=384, D=16, K=8)
+    out = _run(d)
+    nn = int(d["n_nodes"][0])
+    rng = np.random.default_rng(1)
+    nodes = sorted(set([0, 1, 127, 128, 1000, nn] + list(rng.integers(0, nn + 1, size=12))))
+    _check_rows(d, out, [(0, int(i), h) for i in nodes if i <= nn for h in (0, 7)])
+
+
+def test_tree_attention_root_only():
+    d = _case(8, n_req=1, n_q=4, n_kv=1, B=0, ctxs=[129], cap=256)
+    out = _run(d)
+    _check_rows(d, out, [(0, 0, h) for h in range(4)])
+
+
 def test_tree_rope_matches_oracle():
     rng = np.random.default_rng(4)
     n_req, B, heads, hd, theta = 2, 30, 3, 128, 1e6
