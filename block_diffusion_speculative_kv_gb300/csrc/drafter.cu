@@ -63,8 +63,13 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
     off = align_up(off + bytes, 256);
     return o;
   };
-  // the GEMM chains' counters, then one arrival counter per top-K row
-  const int n_counters = gemm_counter_ints() + (4096 > R ? 4096 : R);
+  // the GEMM chains' counters, then one arrival counter per top-K row.  The
+  // counters persist between calls (every launch leaves them at zero), so the
+  // region's size does not depend on L or the injected rows: calls with other
+  // L or injected rows lay out the regions after it differently (up to 16 rows
+  // per request).
+  const int R16 = 16 * n_req;
+  const int n_counters = gemm_counter_ints() + (4096 > R16 ? 4096 : R16);
   w.counters = take(sizeof(int) * n_counters);
   w.x = take(sizeof(float) * (size_t)R * d.d);
   w.xn = take(es * (size_t)R * d.d);

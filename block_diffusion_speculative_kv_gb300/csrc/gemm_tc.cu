@@ -371,7 +371,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
     }
   }
-  if (!(warp == 0 && lane == 0)) pdl_wait();
+  // (griddepcontrol.wait holds the whole warp, so the weight producer's
+  // warp skips it altogether; its other lanes have no work)
+  if (warp != 0) pdl_wait();
   pdl_trigger();
 
   if (warp == 0 || warp == 6) {
