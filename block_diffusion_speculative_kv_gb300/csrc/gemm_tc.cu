@@ -288,7 +288,298 @@ __device__ __forceinline__ void tk_row_merge(const EpiParams& E, int n_rec, int 
   ptx::named_bar_sync(1, kEpiThreads);
 }
 
+// Lane r of the warp gets the sum over the 32 lanes of v[r] (a butterfly that
+// halves the values each lane keeps at every step: 31 shuffles for 32 sums).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// Eight floats of a staged row as eight bf16 (16 bytes).
+__device__ __forceinline__ uint4 pack8_bf16(const float* src) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 b = *reinterpret_cast<const float4*>(src + 4);
+  __nv_bfloat162 h[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                         __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+  return *reinterpret_cast<const uint4*>(h);
+}
+
+// Write back rows [crow0, crow0 + nr) of a 128-column tile staged in buf
+// (buf[r * kBufLd + c]: the value of tile column c; SWIGLU: output column c of
+// the tile's 64).  16-byte segments when the destination's rows and the tile
+// allow it (bf16 outputs, 16-byte aligned rows, N_feat % 8 == 0), else one
+// element per thread and step.  All epilogue threads call it.
 template <typename T>
+__device__ __forceinline__ void epi_copy_out(const EpiParams& E, const float* buf, int col0,
+                                             int crow0, int nr, int etid) {
+  static_assert(sizeof(T) == 2, "the tensor-core GEMM runs bf16");
+  const bool v16 = (E.N_feat & 7) == 0;
+  switch (E.kind) {
+    case EPI_STORE:
+    case EPI_QKV: {
+      T* out = static_cast<T*>(E.out);
+      if (v16 && (E.ldo & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+        for (int i = etid; i < nr * 16; i += kEpiThreads) {
+          const int r = i >> 4, c = (i & 15) * 8;
+          if (col0 + c < E.N_feat)
+            *reinterpret_cast<uint4*>(out + (size_t)(crow0 + r) * E.ldo + col0 + c) =
+                pack8_bf16(buf + r * kBufLd + c);
+        }
+      } else {
+        for (int i = etid; i < nr * kTileN; i += kEpiThreads) {
+          const int r = i >> 7, c = i & 127;
+          if (col0 + c < E.N_feat)
+            out[(size_t)(crow0 + r) * E.ldo + col0 + c] = from_f32<T>(buf[r * kBufLd + c]);
+        }
+      }
+      break;
+    }
+    case EPI_SWIGLU: {
+      T* out = static_cast<T*>(E.out);
+      const int oc0 = col0 >> 1;
+      const int n_out = E.N_feat >> 1;
+      if (v16 && (E.ldo & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+        for (int i = etid; i < nr * 8; i += kEpiThreads) {
+          const int r = i >> 3, c = (i & 7) * 8;
+          if (oc0 + c < n_out)
+            *reinterpret_cast<uint4*>(out + (size_t)(crow0 + r) * E.ldo + oc0 + c) =
+                pack8_bf16(buf + r * kBufLd + c);
+        }
+      } else {
+        for (int i = etid; i < nr * (kTileN / 2); i += kEpiThreads) {
+          const int r = i >> 6, c = i & 63;
+          if (oc0 + c < n_out)
+            out[(size_t)(crow0 + r) * E.ldo + oc0 + c] = from_f32<T>(buf[r * kBufLd + c]);
+        }
+      }
+      break;
+    }
+    case EPI_RESID: {
+      T* xn = static_cast<T*>(E.xn);
+      const T* gain = static_cast<const T*>(E.gain);
+      const bool vec = v16 && (reinterpret_cast<uintptr_t>(E.x) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(xn) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(gain) & 15) == 0;
+      if (vec) {
+        for (int i = etid; i < nr * 32; i += kEpiThreads) {
+          const int r = i >> 5, c = (i & 31) * 4;
+          if (col0 + c < E.N_feat)
+            *reinterpret_cast<float4*>(E.x + (size_t)(crow0 + r) * E.N_feat + col0 + c) =
+                *reinterpret_cast<const float4*>(buf + r * kBufLd + c);
+        }
+        for (int i = etid; i < nr * 16; i += kEpiThreads) {
+          const int r = i >> 4, c = (i & 15) * 8;
+          if (col0 + c >= E.N_feat) continue;
+          const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + col0 + c));
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gw);
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 gf = __bfloat1622float2(g2[q]);
+            v[2 * q] = buf[r * kBufLd + c + 2 * q] * gf.x;
+            v[2 * q + 1] = buf[r * kBufLd + c + 2 * q + 1] * gf.y;
+          }
+          *reinterpret_cast<uint4*>(xn + (size_t)(crow0 + r) * E.N_feat + col0 + c) = pack8_bf16(v);
+        }
+      } else {
+        for (int i = etid; i < nr * kTileN; i += kEpiThreads) {
+          const int r = i >> 7, c = i & 127;
+          if (col0 + c >= E.N_feat) continue;
+          const size_t idx = (size_t)(crow0 + r) * E.N_feat + col0 + c;
+          const float xv = buf[r * kBufLd + c];
+          E.x[idx] = xv;
+          xn[idx] = from_f32<T>(xv * to_f32<T>(gain[col0 + c]));
+        }
+      }
+      break;
+    }
+    case EPI_LOGITS: {
+      if (E.logits == nullptr) break;
+      const bool vec = (E.N_feat & 3) == 0 && (reinterpret_cast<uintptr_t>(E.logits) & 15) == 0;
+      for (int i = etid; i < nr * (vec ? 32 : kTileN); i += kEpiThreads) {
+        const int r = vec ? (i >> 5) : (i >> 7);
+        const int c = vec ? (i & 31) * 4 : (i & 127);
+        const int row = crow0 + r;
+        const int rq = row / E.L;
+        const int j = row - rq * E.L;
+        if (j < 1 || col0 + c >= E.N_feat) continue;
+        float* dst = E.logits + ((size_t)rq * (E.L - 1) + (j - 1)) * E.N_feat + col0 + c;
+        if (vec) *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(buf + r * kBufLd + c);
+        else *dst = buf[r * kBufLd + c];
+      }
+      break;
+    }
+    default: {   // EPI_STORE_F32
+      const bool vec = (E.N_feat & 3) == 0 && (E.ldo & 3) == 0 &&
+                       (reinterpret_cast<uintptr_t>(E.logits) & 15) == 0;
+      for (int i = etid; i < nr * (vec ? 32 : kTileN); i += kEpiThreads) {
+        const int r = vec ? (i >> 5) : (i >> 7);
+        const int c = vec ? (i & 31) * 4 : (i & 127);
+        if (col0 + c >= E.N_feat) continue;
+        float* dst = E.logits + (size_t)(crow0 + r) * E.ldo + col0 + c;
+        if (vec) *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(buf + r * kBufLd + c);
+        else *dst = buf[r * kBufLd + c];
+      }
+      break;
+    }
+  }
+}
+
+// Epilogue of rows [rs0, rs1) of a tile with more than one 16-row chunk (row
+// tiles of 32..256 activation rows), 16 rows at a time: each thread keeps its
+// tile column f, and every global load a batch needs (up to three partial-sum
+// slots, residual rows, RoPE factors) is issued before any is used, so a batch
+// costs one memory round trip (the chunk path takes one per input, after a
+// shared-memory transpose).  The sum is slot 0 + slot 1 + ... in that order
+// (deterministic): slot 0 from TMEM when `tmem` (a tile this CTA owns alone),
+// else every slot from the partial-sum buffer.  STORE, STORE_F32, QKV, RESID,
+// SWIGLU and LOGITS without a fused top-K.
+template <typename T>
+__device__ __forceinline__ void epi_tile_batched(const EpiParams& E, bool tmem, uint32_t tacc,
+                                                 int col0, int row0, int rs0, int rs1,
+                                                 int n_tile, const float* slots, int nslots,
+                                                 const float* s_scale, int srow0, float* s_red,
+                                                 float* buf, int f, int ew, int lane) {
+  constexpr int RB = kChunk;
+  const int col = col0 + f;
+  const bool cvalid = col < E.N_feat;
+  const int half = E.head_dim >> 1;
+  const float gain =
+      (E.kind == EPI_RESID && cvalid) ? to_f32<T>(static_cast<const T*>(E.gain)[col]) : 0.f;
+  const bool rot = E.kind == EPI_QKV && col < E.rope_cols;
+  const int ihalf = rot ? (col % E.head_dim) % half : 0;
+  // the row scales and the zeroed sums of squares are written by all threads
+  ptx::named_bar_sync(1, kEpiThreads);
+  for (int rb = rs0; rb < rs1; rb += RB) {
+    const int nr = min(RB, rs1 - rb);
+    float acc[RB], v0[RB], v1[RB], in_a[RB], in_b[RB];
+    // slot 0 (unless it is the TMEM accumulator), slot 1 and slot 2 at once
+    const float* pb = slots + (size_t)rb * kTileN + f;
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (!tmem) acc[r] = r < nr ? __ldcg(pb + (size_t)r * kTileN) : 0.f;
+      v0[r] = (nslots > 1 && r < nr) ? __ldcg(pb + (size_t)(n_tile + r) * kTileN) : 0.f;
+      v1[r] = (nslots > 2 && r < nr) ? __ldcg(pb + (size_t)(2 * n_tile + r) * kTileN) : 0.f;
+    }
+    if (E.kind == EPI_RESID) {
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+        in_a[r] = (r < nr && cvalid) ? __ldcg(E.x + (size_t)(row0 + rb + r) * E.N_feat + col) : 0.f;
+    } else if (rot) {
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const float2 cs = r < nr ? __ldg(E.rope + (size_t)(row0 + rb + r) * half + ihalf)
+                                 : make_float2(1.f, 0.f);
+        in_a[r] = cs.x;
+        in_b[r] = cs.y;
+      }
+    }
+    if (tmem) {
+      __syncwarp();
+      ptx::tmem_ld_32x16(tacc + static_cast<uint32_t>(rb), acc);
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) acc[r] += v0[r];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) acc[r] += v1[r];
+    // (more than three contributors: the rest in order, one slot at a time)
+    for (int s = 3; s < nslots; ++s) {
+      const float* ps = slots + ((size_t)s * n_tile + rb) * kTileN + f;
+#pragma unroll
+      for (int r = 0; r < RB; ++r) v0[r] = r < nr ? __ldcg(ps + (size_t)r * kTileN) : 0.f;
+#pragma unroll
+      for (int r = 0; r < RB; ++r) acc[r] += v0[r];
+    }
+    // the batch's values of column f
+    float val[RB];
+    switch (E.kind) {
+      case EPI_STORE:
+      case EPI_LOGITS:
+#pragma unroll
+        for (int r = 0; r < RB; ++r) val[r] = acc[r] * (r < nr ? s_scale[row0 + rb + r - srow0] : 0.f);
+        break;
+      case EPI_SWIGLU:
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const float v = acc[r] * (r < nr ? s_scale[row0 + rb + r - srow0] : 0.f);
+          const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+          val[r] = silu_f(v) * other;   // (meaningful on even columns)
+        }
+        break;
+      case EPI_RESID: {
+        float sq[32];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          val[r] = in_a[r] + acc[r];
+          sq[r] = (r < nr && cvalid) ? val[r] * val[r] : 0.f;
+          sq[r + RB] = 0.f;
+        }
+        const float rs = warp_transpose_sum32(sq, lane);
+        if (lane < nr) s_red[ew * n_tile + (row0 + rb + lane - srow0)] += rs;
+        break;
+      }
+      case EPI_QKV: {
+        // the RoPE partner column (f +- head_dim / 2) belongs to another warp:
+        // exchange through the chunk buffer
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          acc[r] *= r < nr ? s_scale[row0 + rb + r - srow0] : 0.f;
+          buf[r * kBufLd + f] = acc[r];
+        }
+        ptx::named_bar_sync(1, kEpiThreads);
+        const int i = col % E.head_dim;
+        const int pf = (i < half) ? f + half : f - half;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          val[r] = acc[r];
+          if (rot) {
+            const float pv = buf[r * kBufLd + pf];
+            val[r] = (i < half) ? (acc[r] * in_a[r] - pv * in_b[r]) : (acc[r] * in_a[r] + pv * in_b[r]);
+          }
+        }
+        ptx::named_bar_sync(1, kEpiThreads);
+        break;
+      }
+      default:   // EPI_STORE_F32
+#pragma unroll
+        for (int r = 0; r < RB; ++r) val[r] = acc[r];
+        break;
+    }
+    // Stage the batch row-major in the chunk buffer and write it back as
+    // 16-byte row segments: a thread's own column would take one store per
+    // row of 2-4 bytes per lane, and those scattered stores, not the loads,
+    // bounded this epilogue.
+    if (E.kind == EPI_SWIGLU) {
+      if ((f & 1) == 0) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r) buf[r * kBufLd + (f >> 1)] = val[r];
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < RB; ++r) buf[r * kBufLd + f] = val[r];
+    }
+    ptx::named_bar_sync(1, kEpiThreads);
+    const int etid = (ew << 5) | lane;
+    epi_copy_out<T>(E, buf, col0, row0 + rb, nr, etid);
+    ptx::named_bar_sync(1, kEpiThreads);
+  }
+  // every warp's sums of squares are in s_red (read by the flush that follows)
+  ptx::named_bar_sync(1, kEpiThreads);
+}
+
+// kMulti: row tiles of 32..256 rows (several 16-row chunks per tile); else
+// one 16-row chunk per tile.  Two instantiations keep each path's registers
+// and code apart.
+template <typename T, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -355,7 +646,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   // L2 prefetch of the residual rows the first phase's epilogue will read (a
   // hint only, so it may precede the wait below; in a layer's chain those rows
   // were written two kernels back and are long out of L2).
-  if (warp >= 2 && warp <= 5 && p.ph[0].epi.kind == EPI_RESID && p.n_tile == kChunk) {
+  if (!kMulti && warp >= 2 && warp <= 5 && p.ph[0].epi.kind == EPI_RESID) {
     const TcPhase& P0 = p.ph[0];
     const int G0 = P0.grid;
     if (c < G0) {
@@ -552,6 +843,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         ptx::named_bar_sync(1, kEpiThreads);
       }
+      // Several 16-row chunks per tile: a split tile's epilogue is shared by
+      // all its contributors.  Each posts its partial sums (c_first too) in
+      // a first pass over its tiles, then finishes its share of the tile's rows
+      // from all the slots in a second pass (below).
+      const bool bphase = kMulti && !fused_tk && E.kind != EPI_KV;
       while (u < u_end) {
         const int acc = tile_i & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
@@ -580,7 +876,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // blocks open their unit ranges, so they are posted early).  A partial
         // slot is then stored column-major, [128 columns][16 rows]: thread f
         // writes and reads its column's 16 values as four float4.
-        const bool early = p.n_tile == kChunk;
+        const bool early = !kMulti;
         const bool resid4 = early && E.kind == EPI_RESID && (E.N_feat & 3) == 0;
         const bool qkv4 = early && E.kind == EPI_QKV && (E.N_feat & 3) == 0 &&
                           (E.head_dim & 7) == 0 && (E.ldo & 3) == 0;
@@ -639,7 +935,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         ptx::tc_fence_after();
 
-        if (!single && !reducer) {
+        if (!single && (!reducer || bphase)) {
           float* my_part = p.part + ((size_t)c_first * P.max_slots + (c - c_first)) *
                                         (size_t)p.n_tile * kTileN;
           for (int c0 = 0; c0 < nrows; c0 += kChunk) {
@@ -652,8 +948,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               for (int q = 0; q < 4; ++q)
                 d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             } else {
+              // staged row-major in the chunk buffer, written as 16-byte segments
+              const int nr = min(kChunk, nrows - c0);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kTileN + f] = v[j];
+              for (int j = 0; j < 16; ++j) buf[j * kBufLd + f] = v[j];
+              ptx::named_bar_sync(1, kEpiThreads);
+              for (int i = etid; i < nr * 32; i += kEpiThreads) {
+                const int r = i >> 5, cc = (i & 31) * 4;
+                *reinterpret_cast<float4*>(my_part + (size_t)(c0 + r) * kTileN + cc) =
+                    *reinterpret_cast<const float4*>(buf + r * kBufLd + cc);
+              }
+              ptx::named_bar_sync(1, kEpiThreads);
             }
           }
           ptx::tc_fence_before();
@@ -674,7 +979,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             }
           }
           const float* slots = p.part + (size_t)c_first * P.max_slots * p.n_tile * kTileN;
-          for (int c0 = 0; c0 < nrows; c0 += kChunk) {
+          // several chunks per tile: 32 rows at a time, every load of a batch in flight
+          const bool batched = bphase;   // (single tiles here: reducers post instead)
+          if (batched)
+            epi_tile_batched<T>(E, true, tacc, ftile * kTileN, row0, 0, nrows, p.n_tile, slots, 1,
+                                s_scale, row0, s_red, buf, f, ew, lane);
+          for (int c0 = 0; !batched && c0 < nrows; c0 += kChunk) {
             const int nr = min(kChunk, nrows - c0);
             float sum[kChunk];
             __syncwarp();
@@ -731,6 +1041,46 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         ++tile_i;
         u += n;
+      }
+      if (bphase && !stop) {
+        // second pass: contributor j = c - c_first of a split tile finishes its
+        // rows [j nrows / nslots, (j + 1) nrows / nslots) once all have posted
+        long long u2 = c < Gk ? (long long)c * U / Gk : 0;
+        while (u2 < u_end) {
+          const int t = static_cast<int>(u2 / KB);
+          const int kb0 = static_cast<int>(u2 - (long long)t * KB);
+          const int n = static_cast<int>((KB - kb0) < (u_end - u2) ? (KB - kb0) : (u_end - u2));
+          u2 += n;
+          const int c_first = cta_of_unit((long long)t * KB, U, Gk);
+          const int nslots = cta_of_unit((long long)t * KB + KB - 1, U, Gk) - c_first + 1;
+          if (nslots == 1) continue;
+          const int ftile = t / P.n_rtiles;
+          const int row0 = (t - ftile * P.n_rtiles) * p.n_tile;
+          const int nrows = min(p.n_tile, E.M_rows - row0);
+          const int j = c - c_first;
+          const int rs0 = j * nrows / nslots, rs1 = (j + 1) * nrows / nslots;
+          bool got = true;
+          if (etid == 0) got = wait_counter(&P.counters[c_first], nslots, flags, lim);
+          if (ptx::named_bar_or(1, kEpiThreads, !got)) {
+            record_status(p.status, DFLASH_ERR_TIMEOUT);
+            flags[0] = 1;
+            stop = true;
+            break;
+          }
+          if (!scales_once)
+            epi_row_scales(E, row0 + rs0, rs1 - rs0, s_scale + rs0, etid, kEpiThreads);
+          for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
+          const float* slots = p.part + (size_t)c_first * P.max_slots * p.n_tile * kTileN;
+          epi_tile_batched<T>(E, false, 0u, ftile * kTileN, row0, rs0, rs1, p.n_tile, slots,
+                              nslots, s_scale, row0, s_red, buf, f, ew, lane);
+          if (E.kind == EPI_RESID)
+            epi_resid_flush(E, ftile, row0 + rs0, rs1 - rs0, s_red + rs0, p.n_tile, 4, etid,
+                            kEpiThreads);
+          ptx::named_bar_sync(1, kEpiThreads);
+          // the last contributor through resets the counter for the next launch
+          if (etid == 0 && atomicAdd(&P.counters[c_first], 1) == 2 * nslots - 1)
+            P.counters[c_first] = 0;
+        }
       }
       if (stop) break;
       if (fused_tk) {
@@ -852,11 +1202,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <typename T>
+template <typename T, bool kMulti>
 void set_smem_attr_once(int bytes) {
   static int done = 0;
   if (done < bytes) {
-    cudaFuncSetAttribute(gemm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(gemm_tc_kernel<T, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         bytes);
     done = bytes;
   }
 }
@@ -953,10 +1304,15 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
     if (!encode_kmajor_map(&maps.x[k], ph[k].X, M_rows, ph[k].K, ph[k].ldx, pl.n_tile))
       return set_error(DFLASH_ERR_CUDA, "cannot encode the activation TMA descriptor");
   }
-  set_smem_attr_once<__nv_bfloat16>(smem);
   TraceScope ts("gemm_tc", st);
   static_assert(sizeof(TcParams) + sizeof(TcMaps) <= 32000, "kernel parameter space");
-  launch_k(gemm_tc_kernel<__nv_bfloat16>, dim3(G), dim3(kThreads), smem, st, maps, p);
+  if (p.n_tile > kChunk) {
+    set_smem_attr_once<__nv_bfloat16, true>(smem);
+    launch_k(gemm_tc_kernel<__nv_bfloat16, true>, dim3(G), dim3(kThreads), smem, st, maps, p);
+  } else {
+    set_smem_attr_once<__nv_bfloat16, false>(smem);
+    launch_k(gemm_tc_kernel<__nv_bfloat16, false>, dim3(G), dim3(kThreads), smem, st, maps, p);
+  }
   return check_launch("gemm_tc");
 }
 
