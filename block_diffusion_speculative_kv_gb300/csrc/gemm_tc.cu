@@ -104,7 +104,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int n_tile, int tk
   L.a_off = 0;
   L.b_off = stages * kABytes;
   L.bar_off = L.b_off + stages * b_bytes;
-  const uint32_t bar_bytes = (3 * stages + 5) * 8 + 16 + 16;
+  const uint32_t bar_bytes = (3 * stages + 6) * 8 + 16 + 16;
   L.buf_off = (L.bar_off + bar_bytes + 15) / 16 * 16;
   L.scale_off = L.buf_off + kChunk * kBufLd * 4;
   L.red_off = L.scale_off + n_tile * 4;
@@ -576,6 +576,148 @@ __device__ __forceinline__ void epi_tile_batched(const EpiParams& E, bool tmem, 
   ptx::named_bar_sync(1, kEpiThreads);
 }
 
+// Share [rs0, rs1) of a split tile finished from shared memory (second pass
+// of the shared split-tile epilogue).  When a CTA gets here its MMAs are done
+// and neither producer writes the ring before this CTA publishes the phase, so
+// the ring holds the inputs: one bulk copy per partial-sum slot (a share's
+// rows are contiguous in a slot) plus the residual rows (RESID) or RoPE rows
+// (QKV), all landing on sbar.  Then warp w takes rows w, w + 4, ... and lane l
+// columns 4l .. 4l + 3: slots summed in slot order, the epilogue applied, and
+// each row written as one contiguous segment per warp.  Returns false (status
+// set) if the copies did not land in time.  Needs N_feat % 128 == 0 and the
+// inputs within ring_bytes (the caller checks).
+template <typename T>
+__device__ __forceinline__ bool epi_share_smem(const EpiParams& E, uint8_t* ring, uint64_t* sbar,
+                                               uint32_t& sphase, const float* slots, int nslots,
+                                               int n_tile, int col0, int row0, int rs0, int rs1,
+                                               int ftile, const float* s_scale, int ew, int lane,
+                                               uint64_t lim, volatile int* flags, int* status) {
+  const int R = rs1 - rs0;
+  const int half = E.head_dim >> 1;
+  const bool has_x = E.kind == EPI_RESID;
+  const bool trot = E.kind == EPI_QKV && col0 < E.rope_cols;
+  const uint32_t seg = static_cast<uint32_t>(R) * kTileN * 4;
+  const uint32_t in_bytes = has_x ? seg : trot ? static_cast<uint32_t>(R * half * 8) : 0u;
+  float* sl = reinterpret_cast<float*>(ring);
+  float* sin_ = sl + (size_t)nslots * R * kTileN;
+  if (ew == 0) {
+    // the slots and residual rows were written with ordinary stores by other
+    // CTAs (acquired before this call); the copies read them through the async proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    if (lane == 0) ptx::mbar_arrive_expect_tx(sbar, nslots * seg + in_bytes);
+    __syncwarp();
+    const uint64_t pol = ptx::policy_evict_first();
+    if (lane < nslots)
+      ptx::bulk_load(sl + (size_t)lane * R * kTileN, slots + ((size_t)lane * n_tile + rs0) * kTileN,
+                     seg, sbar, pol);
+    if (has_x)
+      for (int r = lane; r < R; r += 32)
+        ptx::bulk_load(sin_ + (size_t)r * kTileN, E.x + (size_t)(row0 + rs0 + r) * E.N_feat + col0,
+                       kTileN * 4, sbar, pol);
+    if (trot && lane == 0)
+      ptx::bulk_load(sin_, E.rope + (size_t)(row0 + rs0) * half, in_bytes, sbar, pol);
+  }
+  const bool ok = ptx::mbar_wait_bounded(sbar, sphase, lim, flags);
+  if (ptx::named_bar_or(1, kEpiThreads, !ok)) {
+    if (threadIdx.x == 64) {
+      record_status(status, DFLASH_ERR_TIMEOUT);
+      flags[0] = 1;
+      // the copies must land before the CTA exits
+      ptx::mbar_wait_bounded(sbar, sphase, kTimeoutNs, nullptr);
+    }
+    return false;
+  }
+  sphase ^= 1u;
+  const int c4 = 4 * lane;
+  const int col = col0 + c4;
+  float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (has_x) {
+    const uint2 gw = __ldg(reinterpret_cast<const uint2*>(static_cast<const T*>(E.gain) + col));
+    const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.x));
+    const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.y));
+    g4 = make_float4(ga.x, ga.y, gb.x, gb.y);
+  }
+  const int ih = (col % E.head_dim) % (half > 0 ? half : 1);
+  const bool lo = half > 0 && (col % E.head_dim) < half;
+  auto st4 = [&](T* dst, float a, float b, float c, float d) {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a, b), p1 = __floats2bfloat162_rn(c, d);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&p0);
+    w.y = *reinterpret_cast<const uint32_t*>(&p1);
+    *reinterpret_cast<uint2*>(dst) = w;
+  };
+  for (int r = ew; r < R; r += 4) {
+    const int row = row0 + rs0 + r;
+    float4 a = *reinterpret_cast<const float4*>(sl + (size_t)r * kTileN + c4);
+    for (int sidx = 1; sidx < nslots; ++sidx) {
+      const float4 b = *reinterpret_cast<const float4*>(sl + ((size_t)sidx * R + r) * kTileN + c4);
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    const float sc = s_scale[rs0 + r];
+    switch (E.kind) {
+      case EPI_STORE:
+        st4(static_cast<T*>(E.out) + (size_t)row * E.ldo + col, a.x * sc, a.y * sc, a.z * sc,
+            a.w * sc);
+        break;
+      case EPI_STORE_F32:
+        *reinterpret_cast<float4*>(E.logits + (size_t)row * E.ldo + col) = a;
+        break;
+      case EPI_LOGITS: {
+        const int rq = row / E.L;
+        const int j = row - rq * E.L;
+        if (j >= 1 && E.logits)
+          *reinterpret_cast<float4*>(E.logits + ((size_t)rq * (E.L - 1) + (j - 1)) * E.N_feat +
+                                     col) = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+        break;
+      }
+      case EPI_SWIGLU: {
+        // columns (gate, up, gate, up): two outputs
+        const float g0 = a.x * sc, u0 = a.y * sc, g1 = a.z * sc, u1 = a.w * sc;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(silu_f(g0) * u0, silu_f(g1) * u1);
+        *reinterpret_cast<__nv_bfloat162*>(static_cast<T*>(E.out) + (size_t)row * E.ldo +
+                                           (col >> 1)) = h;
+        break;
+      }
+      case EPI_RESID: {
+        const float4 xi = *reinterpret_cast<const float4*>(sin_ + (size_t)r * kTileN + c4);
+        const float4 x = make_float4(xi.x + a.x, xi.y + a.y, xi.z + a.z, xi.w + a.w);
+        *reinterpret_cast<float4*>(E.x + (size_t)row * E.N_feat + col) = x;
+        st4(static_cast<T*>(E.xn) + (size_t)row * E.N_feat + col, x.x * g4.x, x.y * g4.y,
+            x.z * g4.z, x.w * g4.w);
+        float ss = (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) E.ssq_out[(size_t)ftile * E.M_rows + row] = ss;
+        break;
+      }
+      case EPI_QKV: {
+        float v[4] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc};
+        if (trot) {
+          // the partner columns (col +- head_dim / 2) sit half / 4 lanes away
+          const int pl = half >> 2;
+          const float* cs = sin_ + ((size_t)r * half + ih) * 2;
+          float pv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) pv[q] = __shfl_xor_sync(0xffffffffu, v[q], pl);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float c = cs[2 * q], sn = cs[2 * q + 1];
+            v[q] = lo ? (v[q] * c - pv[q] * sn) : (v[q] * c + pv[q] * sn);
+          }
+        }
+        st4(static_cast<T*>(E.out) + (size_t)row * E.ldo + col, v[0], v[1], v[2], v[3]);
+        break;
+      }
+      default:
+        break;
+    }
+  }
+  // the ring's next writer is the async proxy (the next phase's copies)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  ptx::named_bar_sync(1, kEpiThreads);
+  return true;
+}
+
 // kMulti: row tiles of 32..256 rows (several 16-row chunks per tile); else
 // one 16-row chunk per tile.  Two instantiations keep each path's registers
 // and code apart.
@@ -595,7 +737,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   uint64_t* accf = empty + p.stages;   // [2] accumulator a holds a finished tile
   uint64_t* acce = accf + 2;           // [2] accumulator a has been drained
   uint64_t* drain = acce + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sbar = drain + 1;          // bulk copies of a shared split tile's inputs landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [0] abort, [2] progress
   float* buf = reinterpret_cast<float*>(smem + SL.buf_off);
   float* s_scale = reinterpret_cast<float*>(smem + SL.scale_off);
@@ -621,6 +764,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       ptx::mbar_init(&acce[a], kEpiThreads);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(sbar, 1);
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;   // phases whose epilogue this CTA has finished
@@ -805,6 +949,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     const int f = ew * 32 + lane;       // tile column (weight row) of this thread
     const int etid = threadIdx.x - 64;  // 0..127
     int tile_i = 0;
+    uint32_t sphase = 0;                // parity of sbar's next completion
     bool stop = false;
     for (int k = 0; k < p.n_phases && !stop; ++k) {
       const TcPhase& P = p.ph[k];
@@ -1069,14 +1214,34 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
           if (!scales_once)
             epi_row_scales(E, row0 + rs0, rs1 - rs0, s_scale + rs0, etid, kEpiThreads);
-          for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
           const float* slots = p.part + (size_t)c_first * P.max_slots * p.n_tile * kTileN;
-          epi_tile_batched<T>(E, false, 0u, ftile * kTileN, row0, rs0, rs1, p.n_tile, slots,
-                              nslots, s_scale, row0, s_red, buf, f, ew, lane);
-          if (E.kind == EPI_RESID)
-            epi_resid_flush(E, ftile, row0 + rs0, rs1 - rs0, s_red + rs0, p.n_tile, 4, etid,
-                            kEpiThreads);
-          ptx::named_bar_sync(1, kEpiThreads);
+          // from shared memory when the share's inputs fit in the ring
+          const size_t share_in = (size_t)(nslots + 1) * (rs1 - rs0) * kTileN * 4;
+          const uintptr_t ptr_or = reinterpret_cast<uintptr_t>(E.out) |
+                                   reinterpret_cast<uintptr_t>(E.logits) |
+                                   reinterpret_cast<uintptr_t>(E.x) |
+                                   reinterpret_cast<uintptr_t>(E.xn) |
+                                   reinterpret_cast<uintptr_t>(E.gain);
+          const bool vec_ok = (E.N_feat % kTileN) == 0 && (E.ldo & 3) == 0 &&
+                              (ptr_or & 15) == 0 &&
+                              (E.kind != EPI_QKV || (E.head_dim & 7) == 0);
+          if (vec_ok && share_in <= SL.bar_off) {
+            if (!scales_once) ptx::named_bar_sync(1, kEpiThreads);   // s_scale written
+            if (!epi_share_smem<T>(E, smem, sbar, sphase, slots, nslots, p.n_tile,
+                                   ftile * kTileN, row0, rs0, rs1, ftile, s_scale, ew, lane, lim,
+                                   flags, p.status)) {
+              stop = true;
+              break;
+            }
+          } else {
+            for (int i = etid; i < 4 * p.n_tile; i += kEpiThreads) s_red[i] = 0.f;
+            epi_tile_batched<T>(E, false, 0u, ftile * kTileN, row0, rs0, rs1, p.n_tile, slots,
+                                nslots, s_scale, row0, s_red, buf, f, ew, lane);
+            if (E.kind == EPI_RESID)
+              epi_resid_flush(E, ftile, row0 + rs0, rs1 - rs0, s_red + rs0, p.n_tile, 4, etid,
+                              kEpiThreads);
+            ptx::named_bar_sync(1, kEpiThreads);
+          }
           // the last contributor through resets the counter for the next launch
           if (etid == 0 && atomicAdd(&P.counters[c_first], 1) == 2 * nslots - 1)
             P.counters[c_first] = 0;
