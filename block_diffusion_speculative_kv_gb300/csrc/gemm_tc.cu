@@ -646,66 +646,121 @@ __device__ __forceinline__ bool epi_share_smem(const EpiParams& E, uint8_t* ring
     w.y = *reinterpret_cast<const uint32_t*>(&p1);
     *reinterpret_cast<uint2*>(dst) = w;
   };
-  for (int r = ew; r < R; r += 4) {
-    const int row = row0 + rs0 + r;
-    float4 a = *reinterpret_cast<const float4*>(sl + (size_t)r * kTileN + c4);
-    for (int sidx = 1; sidx < nslots; ++sidx) {
-      const float4 b = *reinterpret_cast<const float4*>(sl + ((size_t)sidx * R + r) * kTileN + c4);
-      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+  // Four rows per warp and step (r, r + 4, r + 8, r + 12): independent chains,
+  // so a warp has several rows' loads, math and stores in flight.
+  constexpr int RQ = 4;
+  for (int r0 = ew; r0 < R; r0 += 4 * RQ) {
+    float4 a[RQ];
+    float sc[RQ];
+#pragma unroll
+    for (int q = 0; q < RQ; ++q) {
+      const int r = min(r0 + 4 * q, R - 1);
+      a[q] = *reinterpret_cast<const float4*>(sl + (size_t)r * kTileN + c4);
+      sc[q] = s_scale[rs0 + r];
     }
-    const float sc = s_scale[rs0 + r];
+    for (int sidx = 1; sidx < nslots; ++sidx) {
+#pragma unroll
+      for (int q = 0; q < RQ; ++q) {
+        const int r = min(r0 + 4 * q, R - 1);
+        const float4 b =
+            *reinterpret_cast<const float4*>(sl + ((size_t)sidx * R + r) * kTileN + c4);
+        a[q].x += b.x; a[q].y += b.y; a[q].z += b.z; a[q].w += b.w;
+      }
+    }
     switch (E.kind) {
       case EPI_STORE:
-        st4(static_cast<T*>(E.out) + (size_t)row * E.ldo + col, a.x * sc, a.y * sc, a.z * sc,
-            a.w * sc);
+#pragma unroll
+        for (int q = 0; q < RQ; ++q)
+          if (r0 + 4 * q < R)
+            st4(static_cast<T*>(E.out) + (size_t)(row0 + rs0 + r0 + 4 * q) * E.ldo + col,
+                a[q].x * sc[q], a[q].y * sc[q], a[q].z * sc[q], a[q].w * sc[q]);
         break;
       case EPI_STORE_F32:
-        *reinterpret_cast<float4*>(E.logits + (size_t)row * E.ldo + col) = a;
+#pragma unroll
+        for (int q = 0; q < RQ; ++q)
+          if (r0 + 4 * q < R)
+            *reinterpret_cast<float4*>(E.logits + (size_t)(row0 + rs0 + r0 + 4 * q) * E.ldo + col) =
+                a[q];
         break;
       case EPI_LOGITS: {
-        const int rq = row / E.L;
-        const int j = row - rq * E.L;
-        if (j >= 1 && E.logits)
-          *reinterpret_cast<float4*>(E.logits + ((size_t)rq * (E.L - 1) + (j - 1)) * E.N_feat +
-                                     col) = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+        if (E.logits == nullptr) break;
+#pragma unroll
+        for (int q = 0; q < RQ; ++q) {
+          const int row = row0 + rs0 + r0 + 4 * q;
+          const int rq = row / E.L;
+          const int j = row - rq * E.L;
+          if (r0 + 4 * q < R && j >= 1)
+            *reinterpret_cast<float4*>(E.logits + ((size_t)rq * (E.L - 1) + (j - 1)) * E.N_feat +
+                                       col) =
+                make_float4(a[q].x * sc[q], a[q].y * sc[q], a[q].z * sc[q], a[q].w * sc[q]);
+        }
         break;
       }
       case EPI_SWIGLU: {
-        // columns (gate, up, gate, up): two outputs
-        const float g0 = a.x * sc, u0 = a.y * sc, g1 = a.z * sc, u1 = a.w * sc;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(silu_f(g0) * u0, silu_f(g1) * u1);
-        *reinterpret_cast<__nv_bfloat162*>(static_cast<T*>(E.out) + (size_t)row * E.ldo +
-                                           (col >> 1)) = h;
+        // columns (gate, up, gate, up): two outputs per row
+#pragma unroll
+        for (int q = 0; q < RQ; ++q) {
+          const float g0 = a[q].x * sc[q], u0 = a[q].y * sc[q];
+          const float g1 = a[q].z * sc[q], u1 = a[q].w * sc[q];
+          const __nv_bfloat162 h = __floats2bfloat162_rn(silu_f(g0) * u0, silu_f(g1) * u1);
+          if (r0 + 4 * q < R)
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<T*>(E.out) +
+                                               (size_t)(row0 + rs0 + r0 + 4 * q) * E.ldo +
+                                               (col >> 1)) = h;
+        }
         break;
       }
       case EPI_RESID: {
-        const float4 xi = *reinterpret_cast<const float4*>(sin_ + (size_t)r * kTileN + c4);
-        const float4 x = make_float4(xi.x + a.x, xi.y + a.y, xi.z + a.z, xi.w + a.w);
-        *reinterpret_cast<float4*>(E.x + (size_t)row * E.N_feat + col) = x;
-        st4(static_cast<T*>(E.xn) + (size_t)row * E.N_feat + col, x.x * g4.x, x.y * g4.y,
-            x.z * g4.z, x.w * g4.w);
-        float ss = (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+        float ss[RQ];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) E.ssq_out[(size_t)ftile * E.M_rows + row] = ss;
+        for (int q = 0; q < RQ; ++q) {
+          const int r = min(r0 + 4 * q, R - 1);
+          const float4 xi = *reinterpret_cast<const float4*>(sin_ + (size_t)r * kTileN + c4);
+          const float4 x = make_float4(xi.x + a[q].x, xi.y + a[q].y, xi.z + a[q].z, xi.w + a[q].w);
+          if (r0 + 4 * q < R) {
+            const size_t idx = (size_t)(row0 + rs0 + r) * E.N_feat + col;
+            *reinterpret_cast<float4*>(E.x + idx) = x;
+            st4(static_cast<T*>(E.xn) + idx, x.x * g4.x, x.y * g4.y, x.z * g4.z, x.w * g4.w);
+          }
+          ss[q] = (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+          for (int q = 0; q < RQ; ++q) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], off);
+        }
+        if (lane < RQ) {
+          float v = ss[0];
+#pragma unroll
+          for (int q = 1; q < RQ; ++q)
+            if (lane == q) v = ss[q];
+          if (r0 + 4 * lane < R)
+            E.ssq_out[(size_t)ftile * E.M_rows + row0 + rs0 + r0 + 4 * lane] = v;
+        }
         break;
       }
       case EPI_QKV: {
-        float v[4] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc};
-        if (trot) {
-          // the partner columns (col +- head_dim / 2) sit half / 4 lanes away
-          const int pl = half >> 2;
-          const float* cs = sin_ + ((size_t)r * half + ih) * 2;
-          float pv[4];
+        // the partner columns (col +- head_dim / 2) sit half / 4 lanes away
+        const int pl = half >> 2;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) pv[q] = __shfl_xor_sync(0xffffffffu, v[q], pl);
+        for (int q = 0; q < RQ; ++q) {
+          const int r = min(r0 + 4 * q, R - 1);
+          float v[4] = {a[q].x * sc[q], a[q].y * sc[q], a[q].z * sc[q], a[q].w * sc[q]};
+          if (trot) {
+            const float* cs = sin_ + ((size_t)r * half + ih) * 2;
+            float pv[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float c = cs[2 * q], sn = cs[2 * q + 1];
-            v[q] = lo ? (v[q] * c - pv[q] * sn) : (v[q] * c + pv[q] * sn);
+            for (int e = 0; e < 4; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, v[e], pl);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float c = cs[2 * e], sn = cs[2 * e + 1];
+              v[e] = lo ? (v[e] * c - pv[e] * sn) : (v[e] * c + pv[e] * sn);
+            }
           }
+          if (r0 + 4 * q < R)
+            st4(static_cast<T*>(E.out) + (size_t)(row0 + rs0 + r) * E.ldo + col, v[0], v[1],
+                v[2], v[3]);
         }
-        st4(static_cast<T*>(E.out) + (size_t)row * E.ldo + col, v[0], v[1], v[2], v[3]);
         break;
       }
       default:
