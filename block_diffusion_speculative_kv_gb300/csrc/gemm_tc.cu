@@ -1148,17 +1148,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               for (int q = 0; q < 4; ++q)
                 d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             } else {
-              // staged row-major in the chunk buffer, written as 16-byte segments
-              const int nr = min(kChunk, nrows - c0);
+              // row-major: each warp store is one 128-byte row segment
 #pragma unroll
-              for (int j = 0; j < 16; ++j) buf[j * kBufLd + f] = v[j];
-              ptx::named_bar_sync(1, kEpiThreads);
-              for (int i = etid; i < nr * 32; i += kEpiThreads) {
-                const int r = i >> 5, cc = (i & 31) * 4;
-                *reinterpret_cast<float4*>(my_part + (size_t)(c0 + r) * kTileN + cc) =
-                    *reinterpret_cast<const float4*>(buf + r * kBufLd + cc);
-              }
-              ptx::named_bar_sync(1, kEpiThreads);
+              for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kTileN + f] = v[j];
             }
           }
           ptx::tc_fence_before();
