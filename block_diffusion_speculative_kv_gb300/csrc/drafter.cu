@@ -82,12 +82,14 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
   size_t gp = 0;
   if (m.bf16) {
     // the largest need among all activation-row counts up to this call's maximum:
-    // for a fixed row tile the partial count peaks at the tile's smallest row
-    // count, so the row-tile sizes themselves cover every row count in between
+    // for a fixed row tile and row-tile count the partial count peaks at the
+    // smallest such row count, so the row-tile sizes and the first row count of
+    // every count of 256-row tiles cover every row count in between
     const int Mmax = R > max_inject_rows ? R : max_inject_rows;
-    int Ms[8];
+    int Ms[48];
     int nm = 0;
     for (int t = 16; t <= tc_row_tile(Mmax); t <<= 1) Ms[nm++] = t;
+    for (int t = 1; 256 * t < Mmax && nm < 44; ++t) Ms[nm++] = 256 * t + 1;
     Ms[nm++] = R;
     if (max_inject_rows > 0) Ms[nm++] = max_inject_rows;
     for (int mi = 0; mi < nm; ++mi) {
