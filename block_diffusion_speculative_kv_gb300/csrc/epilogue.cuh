@@ -468,15 +468,15 @@ __device__ __forceinline__ void epi_apply_resid4(const EpiParams& e, const float
   }
 }
 
-// QKV over one 16-row chunk, same mapping as epi_apply_resid4 (warp w: rows
-// w + 4i; lane l: columns 4l .. 4l + 3, which lie in one half of a head, so
-// their RoPE partners are four consecutive columns too).  Needs head_dim % 8
-// == 0 and N_feat % 4 == 0.  pre.a / pre.b[4i + j]: cos / sin of row w + 4i,
-// column 4l + j.
+// QKV (and STORE, no rotation) over one 16-row chunk, same mapping as
+// epi_apply_resid4 (warp w: rows w + 4i; lane l: columns 4l .. 4l + 3, which
+// lie in one half of a head, so their RoPE partners are four consecutive
+// columns too).  Needs head_dim % 8 == 0 (QKV) and N_feat % 4 == 0.
+// pre.a / pre.b[4i + j]: cos / sin of row w + 4i, column 4l + j.
 __device__ __forceinline__ void epi_preload_qkv4(const EpiParams& e, int col0, int crow0,
                                                  int nrows, int ew, int lane, EpiPre& pre) {
   const int col = col0 + 4 * lane;
-  const bool rot = col < e.rope_cols;
+  const bool rot = e.kind == EPI_QKV && col < e.rope_cols;
   const int half = e.head_dim >> 1;
   const int ih = (col % e.head_dim) % half;
 #pragma unroll
@@ -502,9 +502,9 @@ __device__ __forceinline__ void epi_apply_qkv4(const EpiParams& e, const float* 
                                                const EpiPre& pre) {
   const int col = col0 + 4 * lane;
   if (col >= e.N_feat) return;
-  const bool rot = col < e.rope_cols;
+  const bool rot = e.kind == EPI_QKV && col < e.rope_cols;
   const int half = e.head_dim >> 1;
-  const bool lo = (col % e.head_dim) < half;
+  const bool lo = half > 0 && (col % e.head_dim) < half;
   const int pc = 4 * lane + (lo ? half : -half);   // partner columns in the tile
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -532,6 +532,89 @@ __device__ __forceinline__ void epi_apply_qkv4(const EpiParams& e, const float* 
       *reinterpret_cast<uint2*>(dst) = pk;
     } else {
       *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+}
+
+// KV over one 16-row chunk, same mapping (warp w: rows w + 4i; lane l: columns
+// 4l .. 4l + 3 of one head, one of K or V, one layer): K rotated at the row's
+// cache position (partners four consecutive columns half a head away), every
+// row written to its cache slot as 8 bytes per lane.  Needs head_dim % 8 ==
+// 0 and n_kv * head_dim % 4 == 0.  pre.a / pre.b[4i + j]: cos / sin of row
+// w + 4i, column 4l + j (K columns); pre.s[i]: (request * n_kv) * cap +
+// position of row w + 4i, or -1 (outside the slab, or past the chunk).
+__device__ __forceinline__ void epi_preload_kv4(const EpiParams& e, int col0, int crow0,
+                                                int nrows, int ew, int lane, EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  const int kvd = e.n_kv * e.head_dim;
+  const bool cv = col < e.N_feat;
+  const bool rotk = cv && ((col / kvd) & 1) == 0;
+  const int half = e.head_dim >> 1;
+  const int ih = ((col % kvd) % e.head_dim) % half;
+  const int n_used = e.row_off[e.n_req];   // rows past it are computed, not stored
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    const int row = crow0 + (r < nrows ? r : 0);
+    const int req = row_request(e.row_off, e.n_req, row);
+    const int pos = e.pos0[req] + (row - e.row_off[req]);
+    pre.s[i] = (r >= nrows || row >= n_used || pos < 0 || pos >= e.cap)
+                   ? -1
+                   : (req * e.n_kv) * e.cap + pos;
+    float4 c01 = make_float4(1.f, 0.f, 1.f, 0.f), c23 = c01;
+    if (rotk && r < nrows) {
+      const float4* src = reinterpret_cast<const float4*>(e.rope + (size_t)row * half + ih);
+      c01 = src[0];
+      c23 = src[1];
+    }
+    pre.a[4 * i + 0] = c01.x; pre.b[4 * i + 0] = c01.y;
+    pre.a[4 * i + 1] = c01.z; pre.b[4 * i + 1] = c01.w;
+    pre.a[4 * i + 2] = c23.x; pre.b[4 * i + 2] = c23.y;
+    pre.a[4 * i + 3] = c23.z; pre.b[4 * i + 3] = c23.w;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_apply_kv4(const EpiParams& e, const float* buf, int col0,
+                                              int nrows, int ew, int lane, const EpiPre& pre) {
+  const int col = col0 + 4 * lane;
+  if (col >= e.N_feat) return;
+  const int kvd = e.n_kv * e.head_dim;
+  const int layer = col / (2 * kvd);
+  const int kind = (col / kvd) & 1;
+  const int c = col % kvd;
+  const int head = c / e.head_dim;
+  const int i0 = c % e.head_dim;
+  const int half = e.head_dim >> 1;
+  const bool lo = i0 < half;
+  const int pc = 4 * lane + (lo ? half : -half);   // partner columns in the tile
+  T* dst = static_cast<T*>(kind == 0 ? e.cache_k[layer] : e.cache_v[layer]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    if (r >= nrows || pre.s[i] < 0) continue;
+    const float4 a = *reinterpret_cast<const float4*>(buf + r * kBufLd + 4 * lane);
+    float v[4] = {a.x, a.y, a.z, a.w};
+    if (kind == 0) {
+      const float4 q = *reinterpret_cast<const float4*>(buf + r * kBufLd + pc);
+      const float pv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float cs = pre.a[4 * i + j], sn = pre.b[4 * i + j];
+        v[j] = lo ? (v[j] * cs - pv[j] * sn) : (v[j] * cs + pv[j] * sn);
+      }
+    }
+    // ((req * n_kv + head) * cap + pos) * head_dim + i0
+    T* d = dst + ((size_t)pre.s[i] + (size_t)head * e.cap) * e.head_dim + i0;
+    if constexpr (sizeof(T) == 2) {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&p0);
+      pk.y = *reinterpret_cast<uint32_t*>(&p1);
+      *reinterpret_cast<uint2*>(d) = pk;
+    } else {
+      *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
     }
   }
 }

@@ -1078,13 +1078,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // writes and reads its column's 16 values as four float4.
         const bool early = !kMulti;
         const bool resid4 = early && E.kind == EPI_RESID && (E.N_feat & 3) == 0;
-        const bool qkv4 = early && E.kind == EPI_QKV && (E.N_feat & 3) == 0 &&
-                          (E.head_dim & 7) == 0 && (E.ldo & 3) == 0;
+        const bool qkv4 = early && (E.N_feat & 3) == 0 && (E.ldo & 3) == 0 &&
+                          ((E.kind == EPI_QKV && (E.head_dim & 7) == 0) || E.kind == EPI_STORE);
+        const bool kv4 = early && E.kind == EPI_KV && (E.head_dim & 7) == 0 &&
+                         ((E.n_kv * E.head_dim) & 3) == 0 && (E.N_feat & 3) == 0;
         EpiPre pre;
         float4 psum[4];
         if (early && (single || reducer)) {
           if (resid4) epi_preload_resid4<T>(E, ftile * kTileN, row0, nrows, ew, lane, pre);
           else if (qkv4) epi_preload_qkv4(E, ftile * kTileN, row0, nrows, ew, lane, pre);
+          else if (kv4) epi_preload_kv4(E, ftile * kTileN, row0, nrows, ew, lane, pre);
           else epi_preload<T>(E, ftile * kTileN, row0, nrows, f, pre);
           epi_touch_out<T>(E, ftile * kTileN, row0, f);
         }
@@ -1214,6 +1217,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                   p.n_tile, pre);
             else if (qkv4)
               epi_apply_qkv4<T>(E, buf, ftile * kTileN, row0, nr, ew, lane, s_scale, row0, pre);
+            else if (kv4)
+              epi_apply_kv4<T>(E, buf, ftile * kTileN, nr, ew, lane, pre);
             else
               epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                  p.n_tile, ew, pre);
