@@ -536,6 +536,32 @@ __device__ __forceinline__ void epi_apply_qkv4(const EpiParams& e, const float* 
   }
 }
 
+// SWIGLU over one 16-row chunk, same mapping (warp w: rows w + 4i; lane l:
+// columns 4l .. 4l + 3 = gate, up, gate, up): two outputs per lane and row,
+// one 4-byte store.  Needs N_feat % 4 == 0 and ldo even.
+template <typename T>
+__device__ __forceinline__ void epi_apply_swiglu4(const EpiParams& e, const float* buf, int col0,
+                                                  int crow0, int nrows, int ew, int lane,
+                                                  const float* s_scale, int srow0) {
+  const int col = col0 + 4 * lane;
+  if (col >= e.N_feat) return;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ew + 4 * i;
+    if (r >= nrows) continue;
+    const float sc = s_scale[crow0 + r - srow0];
+    const float4 a = *reinterpret_cast<const float4*>(buf + r * kBufLd + 4 * lane);
+    const float h0 = silu_f(a.x * sc) * (a.y * sc);
+    const float h1 = silu_f(a.z * sc) * (a.w * sc);
+    T* dst = static_cast<T*>(e.out) + (size_t)(crow0 + r) * e.ldo + (col >> 1);
+    if constexpr (sizeof(T) == 2) {
+      *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(h0, h1);
+    } else {
+      *reinterpret_cast<float2*>(dst) = make_float2(h0, h1);
+    }
+  }
+}
+
 // KV over one 16-row chunk, same mapping (warp w: rows w + 4i; lane l: columns
 // 4l .. 4l + 3 of one head, one of K or V, one layer): K rotated at the row's
 // cache position (partners four consecutive columns half a head away), every

@@ -1082,6 +1082,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                           ((E.kind == EPI_QKV && (E.head_dim & 7) == 0) || E.kind == EPI_STORE);
         const bool kv4 = early && E.kind == EPI_KV && (E.head_dim & 7) == 0 &&
                          ((E.n_kv * E.head_dim) & 3) == 0 && (E.N_feat & 3) == 0;
+        const bool swiglu4 = early && E.kind == EPI_SWIGLU && (E.N_feat & 3) == 0 &&
+                             (E.ldo & 1) == 0;
         EpiPre pre;
         float4 psum[4];
         if (early && (single || reducer)) {
@@ -1219,6 +1221,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               epi_apply_qkv4<T>(E, buf, ftile * kTileN, row0, nr, ew, lane, s_scale, row0, pre);
             else if (kv4)
               epi_apply_kv4<T>(E, buf, ftile * kTileN, nr, ew, lane, pre);
+            else if (swiglu4)
+              epi_apply_swiglu4<T>(E, buf, ftile * kTileN, row0 + c0, nr, ew, lane, s_scale, row0);
             else
               epi_apply_chunk<T>(E, buf, ftile * kTileN, row0 + c0, nr, f, s_scale, row0, s_red,
                                  p.n_tile, ew, pre);
