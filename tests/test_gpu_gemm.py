@@ -48,6 +48,37 @@ def test_linear_matches_float64(M, N, K):
     _run(M, N, K, seed=M + N + K)
 
 
+def test_linear_unaligned_output_rows():
+    # an output 4 bytes off a 16-byte boundary: the 32..256-row tiles' epilogues
+    # take their element-wise paths (the split-tile shares from registers, one
+    # column per thread), with split tiles of many contributors (16 tiles of
+    # 256 rows for 152 SMs)
+    M, N, K = 512, 1024, 4096
+    g = torch.Generator(device="cuda").manual_seed(11)
+    X = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+    buf = torch.full((M * N + 1,), float("nan"), device="cuda")
+    Y = buf[1:].view(M, N)
+    assert Y.data_ptr() % 16 == 4
+    ws = torch.zeros(bd.linear_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    bd.linear_bf16(X, W, Y, ws)
+    torch.cuda.synchronize()
+    assert bd.read_status(ws) == 0
+    x = X.double().cpu().numpy()
+    w = W.double().cpu().numpy()
+    ref = x @ w.T
+    bound = 5e-4 * (np.abs(x) @ np.abs(w).T) + 1e-30
+    y = Y.cpu().numpy()
+    assert np.all(np.isfinite(y))
+    assert np.all(np.abs(y - ref) <= bound), float(np.max(np.abs(y - ref) / bound))
+    assert np.isnan(buf[0].item())      # nothing written before the output
+    # and the same values as through an aligned output (the same sum order)
+    Y2 = torch.empty(M, N, device="cuda")
+    bd.linear_bf16(X, W, Y2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y2)
+
+
 def test_linear_lm_head_shape():
     # vocab-sized output: 1187 column tiles streamed by one CTA per SM
     _run(16, 151936, 256, seed=7)
