@@ -438,6 +438,83 @@ attn_combine_kernel(const AttnParams p) {
   for (int i = 0; i < DPL; ++i) dst[i] = __float2bfloat16_rn(acc[i] * inv);
 }
 
+// The same merge for at most kFewParts chunks (many requests: few chunks per
+// request): a warp merges kRowsPerWarp rows of the flattened (request, KV head,
+// query row) space, every row's partials loaded before any is combined, so
+// that one round trip serves several rows.
+constexpr int kFewParts = 4;
+constexpr int kRowsPerWarp = 4;
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_combine_few_kernel(const AttnParams p) {
+  constexpr int DPL = HD / 32;
+  const int QR = p.G * p.L;
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)p.n_req * p.n_kv * QR;
+  const long long row0 = ((long long)blockIdx.x * 4 + (threadIdx.x >> 5)) * kRowsPerWarp;
+  pdl_wait();
+  pdl_trigger();
+  const int np = p.n_chunks;
+  float m[kRowsPerWarp][kFewParts], l[kRowsPerWarp][kFewParts];
+  float v[kRowsPerWarp][kFewParts][DPL];
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const long long w = row0 + j;
+    const bool live = w < total;
+    const long long ww = live ? w : 0;
+    const long long unit_g = ww / QR;          // request * n_kv + KV head
+    const int r = static_cast<int>(ww - unit_g * QR);
+    const size_t base = (size_t)unit_g * np * QR + r;
+#pragma unroll
+    for (int u = 0; u < kFewParts; ++u) {
+      const bool in = live && u < np;
+      const size_t row = base + (size_t)(in ? u : 0) * QR;
+      const float2 ml = in ? *reinterpret_cast<const float2*>(p.part_ml + row * 2)
+                           : make_float2(-CUDART_INF_F, 0.f);
+      m[j][u] = ml.x;
+      l[j][u] = ml.y;
+      const float* src = p.part_o + row * HD + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 t = in ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j][u][0] = t.x; v[j][u][1] = t.y; v[j][u][2] = t.z; v[j][u][3] = t.w;
+      } else {
+        const float2 t = in ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+        v[j][u][0] = t.x; v[j][u][1] = t.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const long long w = row0 + j;
+    if (w >= total) break;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int u = 0; u < kFewParts; ++u)
+      if (l[j][u] > 0.f) M = fmaxf(M, m[j][u]);
+    float acc[DPL], Lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kFewParts; ++u) {
+      if (l[j][u] > 0.f) {
+        const float wt = exp2f(m[j][u] - M);
+        Lsum += wt * l[j][u];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] += wt * v[j][u][i];
+      }
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    const long long unit_g = w / QR;
+    const int r = static_cast<int>(w - unit_g * QR);
+    const int req = static_cast<int>(unit_g / p.n_kv), g = static_cast<int>(unit_g % p.n_kv);
+    const int h = g * p.G + r / p.L, jj = r % p.L;
+    __nv_bfloat16* dst = p.out + ((size_t)req * p.L + jj) * p.out_ld + (size_t)h * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) dst[i] = __float2bfloat16_rn(acc[i] * inv);
+  }
+}
+
 // fp32 reference-precision path: one warp per (request, query head, token).
 template <int HD>
 __global__ void __launch_bounds__(128)
@@ -527,6 +604,10 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
   const size_t smem = attn_smem_bytes(p.G, p.L, head_dim);
   dim3 grid(p.n_chunks, p.n_kv, p.n_req);
   dim3 cgrid((QR + 3) / 4, p.n_kv, p.n_req);
+  // few chunks per (request, KV head): several rows per warp
+  const bool few = p.n_chunks <= kFewParts && p.n_qt == 0;
+  const long long few_rows = (long long)p.n_req * p.n_kv * QR;
+  const dim3 fgrid(static_cast<unsigned>((few_rows + 4 * kRowsPerWarp - 1) / (4 * kRowsPerWarp)));
   if (head_dim == 128) {
     static bool set = false;
     if (!set) {
@@ -539,7 +620,8 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
       launch_k(attn_split_kernel<128>, grid, dim3(256), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
-    launch_k(attn_combine_kernel<128>, cgrid, dim3(128), 0, st, p);
+    if (few) launch_k(attn_combine_few_kernel<128>, fgrid, dim3(128), 0, st, p);
+    else launch_k(attn_combine_kernel<128>, cgrid, dim3(128), 0, st, p);
   } else if (head_dim == 64) {
     static bool set = false;
     if (!set) {
@@ -552,7 +634,8 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
       launch_k(attn_split_kernel<64>, grid, dim3(256), smem, st, p);
     }
     TraceScope ts("attn_combine", st);
-    launch_k(attn_combine_kernel<64>, cgrid, dim3(128), 0, st, p);
+    if (few) launch_k(attn_combine_few_kernel<64>, fgrid, dim3(128), 0, st, p);
+    else launch_k(attn_combine_kernel<64>, cgrid, dim3(128), 0, st, p);
   } else {
     return set_error(DFLASH_ERR_UNSUPPORTED, "attention: head_dim must be 64 or 128");
   }
