@@ -52,5 +52,12 @@ dflash_status launch_attention_bf16(const AttnParams& p, int head_dim, cudaStrea
 // the merge of the split partials alone (grid: row blocks of 4, KV heads, blockIdx.z units)
 void launch_attn_combine(const AttnParams& p, int head_dim, dim3 cgrid, cudaStream_t st);
 dflash_status launch_attention_f32(const AttnParamsF32& p, int head_dim, cudaStream_t st);
+// The same block attention on the tensor cores (tree_attention.cu): head_dim
+// 128, G <= 4, L <= 32, p.chunk a multiple of 128 keys.  The block keys ride in
+// the chunk holding each request's context end; the last of a (request, KV
+// head)'s chunks to finish merges their partials.  arrivals: n_req * n_kv ints,
+// zero before the call and left at zero; status: the workspace status word.
+dflash_status launch_block_attention_tc(const AttnParams& p, int* arrivals, int* status,
+                                        cudaStream_t st);
 
 }  // namespace dfl

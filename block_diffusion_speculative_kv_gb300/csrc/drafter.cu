@@ -44,6 +44,7 @@ struct WsLayout {
       rope_blk,
       f, rope_inj, total;
   int attn_chunks_cap;
+  int attn_arrivals;   // first int of the tensor-core attention's arrival counters
 };
 
 int ssq_parts(const dflash_dims& d) { return (d.d + 127) / 128; }
@@ -63,13 +64,15 @@ WsLayout ws_layout(const dflash_model& m, int n_req, int max_inject_rows, int L,
     off = align_up(off + bytes, 256);
     return o;
   };
-  // the GEMM chains' counters, then one arrival counter per top-K row.  The
-  // counters persist between calls (every launch leaves them at zero), so the
-  // region's size does not depend on L or the injected rows: calls with other
-  // L or injected rows lay out the regions after it differently (up to 16 rows
-  // per request).
+  // the GEMM chains' counters, one arrival counter per top-K row, then one per
+  // (request, KV head) of the tensor-core attention.  The counters persist
+  // between calls (every launch leaves them at zero), so the region's size
+  // does not depend on L or the injected rows: calls with other L or injected
+  // rows lay out the regions after it differently (up to 16 rows per request).
   const int R16 = 16 * n_req;
-  const int n_counters = gemm_counter_ints() + (4096 > R16 ? 4096 : R16);
+  const int NKV = n_req * d.n_kv;
+  w.attn_arrivals = gemm_counter_ints() + (4096 > R16 ? 4096 : R16);
+  const int n_counters = w.attn_arrivals + (4096 > NKV ? 4096 : NKV);
   w.counters = take(sizeof(int) * n_counters);
   w.x = take(sizeof(float) * (size_t)R * d.d);
   w.xn = take(es * (size_t)R * d.d);
@@ -396,6 +399,21 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
     chunk = ((max_ctx + W.attn_chunks_cap - 1) / W.attn_chunks_cap + 63) / 64 * 64;
     n_chunks = (max_ctx + chunk - 1) / chunk;
   }
+  // With (request, KV head) pairs for half the SMs or more, the tensor-core
+  // kernel (128-key tiles, one CTA per SM) takes the attention: chunks for
+  // about four CTAs per SM over the grid, fewer where contexts are short.  A
+  // few pairs (one request) stay on the split kernel above, whose shorter
+  // per-CTA latency suits a grid of many small chunks.
+  const long long kv_pairs = (long long)n_req * d.n_kv;
+  const bool attn_tc = model->bf16 && hd == 128 && d.n_q / d.n_kv <= 4 && L <= 32 &&
+                       2 * kv_pairs >= num_sms();
+  if (attn_tc) {
+    long long nc = (4LL * num_sms() + kv_pairs - 1) / kv_pairs;
+    if (nc > W.attn_chunks_cap) nc = W.attn_chunks_cap;
+    const int mc = max_ctx > 0 ? max_ctx : 1;
+    chunk = static_cast<int>((mc + nc - 1) / nc + 127) / 128 * 128;
+    n_chunks = (mc + chunk - 1) / chunk;
+  }
 
   // GEMM steps of the pass.  A chain runs the dependent GEMMs between two
   // attention calls in one launch: [QKV_0], attention_0, [O_0, gate/up_0,
@@ -465,7 +483,8 @@ static dflash_status draft_impl(const dflash_model* model, const dflash_cache* c
       ap.part_ml = reinterpret_cast<float*>(c.ws + W.apart_ml);
       ap.out = static_cast<__nv_bfloat16*>(ao);
       ap.out_ld = qd;
-      st = launch_attention_bf16(ap, hd, c.st);
+      st = attn_tc ? launch_block_attention_tc(ap, c.counters + W.attn_arrivals, c.status, c.st)
+                   : launch_attention_bf16(ap, hd, c.st);
     } else {
       AttnParamsF32 ap{};
       ap.qkv = static_cast<const float*>(qkv);

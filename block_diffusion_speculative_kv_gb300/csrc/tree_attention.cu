@@ -78,6 +78,13 @@ struct TreeTcParams {
   int n_ctx_tiles;              // context tiles per chunk (the chunk is n_ctx_tiles * 128 keys)
   int* status;
   int* arrivals;                // [n_req * n_qt][n_kv]: chunks done, zero between calls
+  // Block attention of the drafter ("DFlash" page, 3.4.4) instead of a tree:
+  // the B1 = L block rows of a request see every block key (the anchor row only
+  // itself when anchor_iso), the context ends at the request's ctx_len, the
+  // block keys ride in the chunk that holds that end and later chunks have no
+  // work.  Partials are indexed (head, block row), G L rows per chunk.
+  int block;
+  int anchor_iso;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -128,12 +135,24 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
   const int chunk_id = blockIdx.x, g = blockIdx.y;
   const int rq = blockIdx.z, req = rq / p.n_qt, qt = rq % p.n_qt;
   const int QR = p.G * kNodesPerTile;
-  const bool last_chunk = chunk_id == p.n_chunks - 1;
   const int node0 = qt * kNodesPerTile;
-  // context tiles: fixed by the host's max_ctx (per-request lengths are masked)
   const int k_begin = chunk_id * p.chunk;
-  const int nct = tp.n_ctx_tiles;
-  const size_t part_row0 = (((size_t)rq * p.n_kv + g) * p.n_chunks + chunk_id) * QR;
+  // Tree: context tiles fixed by the host's max_ctx (per-request lengths are
+  // masked), the tree keys in the last chunk.  Block: the request's own
+  // context tiles of the chunk, the block keys in chunk cb (read before the
+  // grid dependency wait: the lengths are set kernels back, like the cache).
+  int nct = tp.n_ctx_tiles, cb = p.n_chunks - 1, bctx = 0;
+  if (tp.block) {
+    bctx = min(max(p.ctx_len[req], 0), p.cap);
+    cb = min(bctx > 0 ? (bctx - 1) / p.chunk : 0, p.n_chunks - 1);
+    if (chunk_id > cb) return;   // no keys here, and no partial to post
+    nct = min(max((bctx - k_begin + kTk - 1) / kTk, 0), tp.n_ctx_tiles);
+  }
+  const bool last_chunk = chunk_id == cb;
+  const int n_parts = cb + 1;                        // chunks that post a partial
+  const int rph = tp.block ? tp.B1 : kNodesPerTile;  // partial rows per head
+  const int QRp = p.G * rph;
+  const size_t part_row0 = (((size_t)rq * p.n_kv + g) * p.n_chunks + chunk_id) * QRp;
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -165,8 +184,8 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
   // request-dependent sizes (read after the dependency wait by everyone)
   int last = -1, tree_end = 0, ntt = 0, ctx = 0;
   auto sizes = [&]() {
-    last = min(max(tp.n_nodes[req], 0), tp.B1 - 1);
-    ctx = min(max(p.ctx_len[req], 0), p.cap);
+    last = tp.block ? tp.B1 - 1 : min(max(tp.n_nodes[req], 0), tp.B1 - 1);
+    ctx = tp.block ? bctx : min(max(p.ctx_len[req], 0), p.cap);
     tree_end = (last_chunk && node0 <= last) ? min(node0 + kNodesPerTile - 1, last) + 1 : 0;
     ntt = (tree_end + kTk - 1) / kTk;
   };
@@ -183,7 +202,8 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
         ptx::prefetch_tmap(&maps.vc);
         ptx::prefetch_tmap(&maps.vt);
       }
-      const uint64_t pol = ptx::policy_evict_last();   // nine query tiles read each tile
+      // a tree's query tiles of a KV head share its tiles; a block reads them once
+      const uint64_t pol = tp.block ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const int slab = (req * p.n_kv + g) * p.cap;
       uint64_t* full = kl ? k_full : v_full;
       uint64_t* empty = kl ? k_empty : v_empty;
@@ -313,7 +333,9 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int pair_bar = 1 + q;                  // warps q and q + 4
     const float sc = p.scale_log2;
-    const uint32_t* mrow = tp.mask + ((size_t)req * tp.B1 + (live ? node : 0)) * tp.mask_w;
+    const uint32_t* mrow =
+        tp.block ? nullptr : tp.mask + ((size_t)req * tp.B1 + (live ? node : 0)) * tp.mask_w;
+    const bool iso = tp.block && tp.anchor_iso && node == 0;   // the anchor sees block key 0 only
     float m_ref = -CUDART_INF_F, l = 0.f;
     bool ok = node0 <= last && ntiles > 0;
     for (int t = 0; t < ntiles && ok; ++t) {
@@ -329,7 +351,10 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
       const uint32_t sa = tbase + s * kTk + lane_off + 64 * kh;   // this thread's 64 scores
       // ancestor bits of keys 64 kh .. 64 kh + 63 (context tiles: all keys)
       uint32_t mb[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
-      if (tree) {
+      if (tree && tp.block) {
+        mb[0] = iso ? (kh == 0 ? 1u : 0u) : 0xFFFFFFFFu;
+        mb[1] = iso ? 0u : 0xFFFFFFFFu;
+      } else if (tree) {
         const int w0 = (key0 + 64 * kh) >> 5;
         mb[0] = live && w0 < tp.mask_w ? mrow[w0] : 0u;
         mb[1] = live && w0 + 1 < tp.mask_w ? mrow[w0 + 1] : 0u;
@@ -511,21 +536,22 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
       const float m_own = live ? m_ref : -CUDART_INF_F;
       const float l_own = live ? l : 0.f;
       bool writer = true;
-      if (p.n_chunks > 1) {
-        if (r < QR) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + (part_row0 + r) * kHd + 64 * kh);
+      const int pr = (r >> 5) * rph + (r & 31);   // partial row (= r for a tree)
+      if (n_parts > 1) {
+        if (r < QR && (r & 31) < rph) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + (part_row0 + pr) * kHd + 64 * kh);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
           if (kh == 0) {
-            p.part_ml[(part_row0 + r) * 2 + 0] = m_own;
-            p.part_ml[(part_row0 + r) * 2 + 1] = l_own;
+            p.part_ml[(part_row0 + pr) * 2 + 0] = m_own;
+            p.part_ml[(part_row0 + pr) * 2 + 1] = l_own;
           }
         }
         __threadfence();
         ptx::named_bar_sync(5, 256);
         int* arrive = tp.arrivals + (size_t)rq * p.n_kv + g;
-        if (tid == 0) *s_last = atomicAdd(arrive, 1) == p.n_chunks - 1;
+        if (tid == 0) *s_last = atomicAdd(arrive, 1) == n_parts - 1;
         ptx::named_bar_sync(5, 256);
         writer = *s_last != 0;
         if (writer) {
@@ -533,22 +559,23 @@ tree_attn_tc_kernel(const __grid_constant__ TreeTcMaps maps, const TreeTcParams 
           if (tid == 0) *arrive = 0;   // for the next call
         }
       }
-      if (writer && has_row) {
-        // merge with the other chunks' partials of this row (reference M)
-        const size_t row_base = ((size_t)rq * p.n_kv + g) * p.n_chunks * QR + r;
-        float M = l_own > 0.f ? m_own : -CUDART_INF_F;
-        for (int c = 0; c < p.n_chunks; ++c) {
-          if (c == chunk_id) continue;
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row_base + (size_t)c * QR);
+      if (writer && has_row && n_parts == 1) {
+        write_row(o, live && l_own > 0.f ? 1.f / l_own : 0.f);
+      } else if (writer && has_row) {
+        // merge every chunk's partial of this row in chunk order, the writer's
+        // own re-read (reference M): the sums do not depend on which CTA
+        // finished last
+        const size_t row_base = ((size_t)rq * p.n_kv + g) * p.n_chunks * QRp + pr;
+        float M = -CUDART_INF_F;
+        for (int c = 0; c < n_parts; ++c) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row_base + (size_t)c * QRp);
           if (ml.y > 0.f) M = fmaxf(M, ml.x);
         }
-        const float w_own = l_own > 0.f ? ex2(m_own - M) : 0.f;
-        float L = l_own * w_own;
+        float L = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) o[j] *= w_own;
-        for (int c = 0; c < p.n_chunks; ++c) {
-          if (c == chunk_id) continue;
-          const size_t rc = row_base + (size_t)c * QR;
+        for (int j = 0; j < 64; ++j) o[j] = 0.f;
+        for (int c = 0; c < n_parts; ++c) {
+          const size_t rc = row_base + (size_t)c * QRp;
           const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + rc);
           if (!(ml.y > 0.f)) continue;
           const float w = ex2(ml.x - M);
@@ -627,7 +654,54 @@ TreePlan tree_plan(int n_req, int n_kv, int B, int max_ctx) {
   return pl;
 }
 
+void set_tc_smem_attr() {
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    set = true;
+  }
+}
+
 }  // namespace
+
+dflash_status launch_block_attention_tc(const AttnParams& p, int* arrivals, int* status,
+                                        cudaStream_t st) {
+  if (p.G < 1 || p.G > 4 || p.L < 1 || p.L > kNodesPerTile || p.chunk < kTk || p.chunk % kTk ||
+      p.n_chunks < 1)
+    return set_error(DFLASH_ERR_UNSUPPORTED,
+                     "block attention: needs G <= 4, L <= 32 and chunks of 128-key tiles");
+  const long long kv_rows = (long long)p.n_req * p.n_kv * p.cap;
+  const long long blk_rows = (long long)p.n_req * p.L;
+  if (kv_rows >= (1ll << 31) || blk_rows >= (1ll << 31) || p.qkv_ld % 8)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "block attention: cache rows exceed 2^31");
+  TreeTcParams tp{};
+  tp.a = p;
+  tp.a.n_qt = 1;
+  tp.B1 = p.L;
+  tp.mask_w = 1;
+  tp.n_ctx_tiles = p.chunk / kTk;
+  tp.status = status;
+  tp.arrivals = arrivals;
+  tp.block = 1;
+  tp.anchor_iso = p.anchor_sees_block ? 0 : 1;
+  TreeTcMaps maps;
+  const __nv_bfloat16* k = p.qkv + (size_t)p.n_q * kHd;
+  const __nv_bfloat16* v = p.qkv + (size_t)(p.n_q + p.n_kv) * kHd;
+  if (!encode_kmajor_map(&maps.kc, p.cache_k, static_cast<int>(kv_rows), kHd, kHd, kTk) ||
+      !encode_kmajor_map(&maps.vc, p.cache_v, static_cast<int>(kv_rows), kHd, kHd, kTk) ||
+      !encode_kmajor_map(&maps.kt, k, static_cast<int>(blk_rows), p.n_kv * kHd, p.qkv_ld, kTk) ||
+      !encode_kmajor_map(&maps.vt, v, static_cast<int>(blk_rows), p.n_kv * kHd, p.qkv_ld, kTk) ||
+      !encode_kmajor_map(&maps.q, p.qkv, static_cast<int>(blk_rows), p.n_q * kHd, p.qkv_ld,
+                         kNodesPerTile))
+    return set_error(DFLASH_ERR_CUDA, "block attention: cannot encode the TMA descriptors");
+  set_tc_smem_attr();
+  {
+    TraceScope ts("attn_block_tc", st);
+    launch_k(tree_attn_tc_kernel, dim3(p.n_chunks, p.n_kv, p.n_req), dim3(kThreads), kSmem, st,
+             maps, tp);
+  }
+  return check_launch("block attention");
+}
 
 }  // namespace dfl
 
@@ -718,11 +792,7 @@ dflash_status dflash_tree_attention(int n_req, int n_q, int n_kv, int head_dim, 
       !encode_kmajor_map(&maps.q, q, n_req * B1, static_cast<int>(q_ld), q_ld, kNodesPerTile))
     return set_error(DFLASH_ERR_CUDA, "tree attention: cannot encode the TMA descriptors");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    set = true;
-  }
+  set_tc_smem_attr();
   {
     TraceScope ts("tree_attn_tc", st);
     launch_k(tree_attn_tc_kernel, dim3(pl.n_chunks, n_kv, n_req * pl.n_qt), dim3(kThreads), kSmem,

@@ -14,6 +14,8 @@ kernel to the exact bar.  (2) End to end: against the oracle's own logits
 the sets may differ only by tokens whose oracle logit lies within delta of
 the oracle's K-th logit, delta = 2 * (that row's max logit error) + 1e-3
 nats, since each side decides on its own logits."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -136,7 +138,7 @@ def _check_logits_topk(ref_logits, gpu_logits, gpu_ids, gpu_lp, K, tolerance):
 
 def _draft_case(wid, anchor_sees_block=True, gains=False, sample_reqs=None, K=None, ctx=None,
                 tied_head=False):
-    wl = WORKLOADS[wid]
+    wl = WORKLOADS[wid] if isinstance(wid, int) else wid
     s = wl.shape
     K = wl.K if K is None else K
     w = synth.drafter_weights(s, wl.seed, device=DEV)
@@ -235,6 +237,21 @@ def test_draft_batched_ragged_sampled():
     ctx = synth.context_lengths(wl)
     pick = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 7})
     _draft_case(3, sample_reqs=pick)
+
+
+@pytest.mark.parametrize("anchor_sees_block,pick", [
+    (True, [0, 1, 3, 5, 6, 11]),
+    (False, [0, 4, 10]),
+])
+def test_draft_batched_tensor_core_attention_edges(anchor_sees_block, pick):
+    # 12 requests x 8 KV heads take the batched attention path (tcgen05,
+    # 128-key tiles; on 152 SMs six chunks of 384 keys for a 2048-key maximum,
+    # the block keys in the chunk holding each request's context end, the last
+    # chunk to finish merging the partials).  Contexts: none, inside the first
+    # tile, at and around tile and chunk boundaries, and the whole cache.
+    wl = dataclasses.replace(WORKLOADS[1], name="qwen3-4b-drafter-b12", n_req=12)
+    ctx = [0, 1, 127, 128, 129, 383, 384, 385, 768, 1000, 2047, 2048]
+    _draft_case(wl, ctx=ctx, anchor_sees_block=anchor_sees_block, sample_reqs=pick)
 
 
 # ---------------------------------------------------------------------------
