@@ -62,13 +62,22 @@ constexpr int kABytes = kTileN * 128;  // 128 weight rows x 64 bf16
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 struct TcPhase {
-  int N_feat, K, n_rtiles, kblocks;
+  int N_feat, K, n_rtiles, n_ftiles, kblocks;
   int grid;        // CTAs sharing the units: min(launch grid, total_units)
   long long total_units;
   int max_slots;
   int* counters;   // split-tile arrival counters of this phase [grid]
   EpiParams epi;
 };
+
+// Tile t of a phase: row-tile-major, so with several row tiles the CTAs of
+// the grid's first and second halves stream the same weight tiles at about
+// the same time for different row tiles, and the second read hits L2.
+__device__ __forceinline__ void tile_coords(const TcPhase& P, long long t, int& ftile,
+                                            int& rtile) {
+  rtile = static_cast<int>(t / P.n_ftiles);
+  ftile = static_cast<int>(t - (long long)rtile * P.n_ftiles);
+}
 
 struct TcParams {
   int M_rows, n_tile, stages, n_phases;
@@ -852,8 +861,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const long long ub = (long long)c * P0.total_units / G0;
       const long long ue = (long long)(c + 1) * P0.total_units / G0;
       for (long long t = ub / P0.kblocks; t * P0.kblocks < ue; ++t) {
-        const int ftile = static_cast<int>(t / P0.n_rtiles);
-        const int row0 = static_cast<int>(t - (long long)ftile * P0.n_rtiles) * p.n_tile;
+        int ftile, rtile;
+        tile_coords(P0, t, ftile, rtile);
+        const int row0 = rtile * p.n_tile;
         // only the CTA that applies the epilogue of tile t (its first units)
         if (cta_of_unit(t * P0.kblocks, P0.total_units, G0) == c)
           epi_prefetch_inputs<T>(P0.epi, ftile * kTileN, row0,
@@ -915,8 +925,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (long long u = u_begin; u < u_end; ++u) {
           const int t = static_cast<int>(u / KB);
           const int kb = static_cast<int>(u - (long long)t * KB);
-          const int ftile = t / P.n_rtiles;
-          const int rtile = t - ftile * P.n_rtiles;
+          int ftile, rtile;
+          tile_coords(P, t, ftile, rtile);
           if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, lim, flags)) {
             record_status(p.status, DFLASH_ERR_TIMEOUT);
             flags[0] = 1;
@@ -1056,8 +1066,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int t = static_cast<int>(u / KB);
         const int kb0 = static_cast<int>(u - (long long)t * KB);
         const int n = static_cast<int>((KB - kb0) < (u_end - u) ? (KB - kb0) : (u_end - u));
-        const int ftile = t / P.n_rtiles;
-        const int rtile = t - ftile * P.n_rtiles;
+        int ftile, rtile;
+        tile_coords(P, t, ftile, rtile);
         const int row0 = rtile * p.n_tile;
         const int nrows = min(p.n_tile, E.M_rows - row0);
         const int c_first = cta_of_unit((long long)t * KB, U, Gk);
@@ -1255,8 +1265,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const int c_first = cta_of_unit((long long)t * KB, U, Gk);
           const int nslots = cta_of_unit((long long)t * KB + KB - 1, U, Gk) - c_first + 1;
           if (nslots == 1) continue;
-          const int ftile = t / P.n_rtiles;
-          const int row0 = (t - ftile * P.n_rtiles) * p.n_tile;
+          int ftile, rtile;
+          tile_coords(P, t, ftile, rtile);
+          const int row0 = rtile * p.n_tile;
           const int nrows = min(p.n_tile, E.M_rows - row0);
           const int j = c - c_first;
           const int rs0 = j * nrows / nslots, rs1 = (j + 1) * nrows / nslots;
@@ -1515,6 +1526,7 @@ dflash_status launch_gemm_chain(const GemmPhase* ph, int n_phases, int M_rows, f
     P.N_feat = ph[k].N;
     P.K = ph[k].K;
     P.n_rtiles = pl.n_rtiles;
+    P.n_ftiles = pl.n_ftiles;
     P.kblocks = pl.kblocks;
     P.grid = pl.grid;
     P.total_units = pl.total_units;
