@@ -352,6 +352,37 @@ __device__ __forceinline__ void epi_copy_out(const EpiParams& E, const float* bu
       }
       break;
     }
+    case EPI_KV: {
+      // row r of the batch goes to cache slot (request, head, pos) of its
+      // columns' layer and kind: 8 columns (16 bytes) at a time
+      const int kvd = E.n_kv * E.head_dim;
+      const int n_used = E.row_off[E.n_req];   // rows past it are computed, not stored
+      const bool v8 = (E.head_dim & 7) == 0;
+      for (int i = etid; i < nr * 16; i += kEpiThreads) {
+        const int r = i >> 4, c = (i & 15) * 8;
+        const int row = crow0 + r;
+        if (col0 + c >= E.N_feat || row >= n_used) continue;
+        const int req = row_request(E.row_off, E.n_req, row);
+        const int pos = E.pos0[req] + (row - E.row_off[req]);
+        if (pos < 0 || pos >= E.cap) continue;
+        for (int e = 0; e < 8; e += v8 ? 8 : 1) {
+          const int col = col0 + c + e;
+          if (col >= E.N_feat) break;
+          const int layer = col / (2 * kvd), kind = (col / kvd) & 1, cc = col % kvd;
+          T* dst = static_cast<T*>(kind == 0 ? E.cache_k[layer] : E.cache_v[layer]) +
+                   (((size_t)req * E.n_kv + cc / E.head_dim) * E.cap + pos) * E.head_dim +
+                   cc % E.head_dim;
+          if (v8 && col + 8 <= E.N_feat && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+            *reinterpret_cast<uint4*>(dst) = pack8_bf16(buf + r * kBufLd + c);
+          } else {
+            const int ne = v8 ? 8 : 1;
+            for (int q = 0; q < ne && col + q < E.N_feat; ++q)
+              dst[q] = from_f32<T>(buf[r * kBufLd + c + e + q]);
+          }
+        }
+      }
+      break;
+    }
     case EPI_SWIGLU: {
       T* out = static_cast<T*>(E.out);
       const int oc0 = col0 >> 1;
@@ -451,7 +482,7 @@ __device__ __forceinline__ void epi_copy_out(const EpiParams& E, const float* bu
 // shared-memory transpose).  The sum is slot 0 + slot 1 + ... in that order
 // (deterministic): slot 0 from TMEM when `tmem` (a tile this CTA owns alone),
 // else every slot from the partial-sum buffer.  STORE, STORE_F32, QKV, RESID,
-// SWIGLU and LOGITS without a fused top-K.
+// SWIGLU, KV and LOGITS without a fused top-K.
 template <typename T>
 __device__ __forceinline__ void epi_tile_batched(const EpiParams& E, bool tmem, uint32_t tacc,
                                                  int col0, int row0, int rs0, int rs1,
@@ -464,7 +495,9 @@ __device__ __forceinline__ void epi_tile_batched(const EpiParams& E, bool tmem, 
   const int half = E.head_dim >> 1;
   const float gain =
       (E.kind == EPI_RESID && cvalid) ? to_f32<T>(static_cast<const T*>(E.gain)[col]) : 0.f;
-  const bool rot = E.kind == EPI_QKV && col < E.rope_cols;
+  // RoPE columns: the rotated part of Q and K (QKV), the K part (KV)
+  const bool rot = (E.kind == EPI_QKV && col < E.rope_cols) ||
+                   (E.kind == EPI_KV && cvalid && ((col / (E.n_kv * E.head_dim)) & 1) == 0);
   const int ihalf = rot ? (col % E.head_dim) % half : 0;
   // the row scales and the zeroed sums of squares are written by all threads
   ptx::named_bar_sync(1, kEpiThreads);
@@ -558,6 +591,24 @@ __device__ __forceinline__ void epi_tile_batched(const EpiParams& E, bool tmem, 
         ptx::named_bar_sync(1, kEpiThreads);
         break;
       }
+      case EPI_KV: {
+        // K columns rotate with their partner column (another warp's)
+#pragma unroll
+        for (int r = 0; r < RB; ++r) buf[r * kBufLd + f] = acc[r];
+        ptx::named_bar_sync(1, kEpiThreads);
+        const int i = col % E.head_dim;
+        const int pf = (i < half) ? f + half : f - half;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          val[r] = acc[r];
+          if (rot) {
+            const float pv = buf[r * kBufLd + pf];
+            val[r] = (i < half) ? (acc[r] * in_a[r] - pv * in_b[r]) : (acc[r] * in_a[r] + pv * in_b[r]);
+          }
+        }
+        ptx::named_bar_sync(1, kEpiThreads);
+        break;
+      }
       default:   // EPI_STORE_F32
 #pragma unroll
         for (int r = 0; r < RB; ++r) val[r] = acc[r];
@@ -604,7 +655,10 @@ __device__ __forceinline__ bool epi_share_smem(const EpiParams& E, uint8_t* ring
   const int R = rs1 - rs0;
   const int half = E.head_dim >> 1;
   const bool has_x = E.kind == EPI_RESID;
-  const bool trot = E.kind == EPI_QKV && col0 < E.rope_cols;
+  // rotated tiles: Q and K of QKV; K of KV (a tile lies in one kind: the
+  // caller checks that n_kv * head_dim is a multiple of the tile width)
+  const bool trot = (E.kind == EPI_QKV && col0 < E.rope_cols) ||
+                    (E.kind == EPI_KV && ((col0 / (E.n_kv * E.head_dim)) & 1) == 0);
   const uint32_t seg = static_cast<uint32_t>(R) * kTileN * 4;
   const uint32_t in_bytes = has_x ? seg : trot ? static_cast<uint32_t>(R * half * 8) : 0u;
   float* sl = reinterpret_cast<float*>(ring);
@@ -769,6 +823,46 @@ __device__ __forceinline__ bool epi_share_smem(const EpiParams& E, uint8_t* ring
           if (r0 + 4 * q < R)
             st4(static_cast<T*>(E.out) + (size_t)(row0 + rs0 + r) * E.ldo + col, v[0], v[1],
                 v[2], v[3]);
+        }
+        break;
+      }
+      case EPI_KV: {
+        // as QKV without the row scale, each row to its request's cache slot
+        const int kvd = E.n_kv * E.head_dim;
+        const int layer = col / (2 * kvd), cc = col % kvd;
+        const int head = cc / E.head_dim, ii = cc % E.head_dim;
+        T* cache = static_cast<T*>(trot ? E.cache_k[layer] : E.cache_v[layer]);
+        const int n_used = E.row_off[E.n_req];   // rows past it are computed, not stored
+        const int pl = half >> 2;
+#pragma unroll
+        for (int q = 0; q < RQ; ++q) {
+          const int r = min(r0 + 4 * q, R - 1);
+          float v[4] = {a[q].x, a[q].y, a[q].z, a[q].w};
+          if (trot) {
+            const float* cs = sin_ + ((size_t)r * half + ih) * 2;
+            float pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, v[e], pl);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float c = cs[2 * e], sn = cs[2 * e + 1];
+              v[e] = lo ? (v[e] * c - pv[e] * sn) : (v[e] * c + pv[e] * sn);
+            }
+          }
+          const int row = row0 + rs0 + r;
+          if (r0 + 4 * q < R && row < n_used) {
+            const int req = row_request(E.row_off, E.n_req, row);
+            const int pos = E.pos0[req] + (row - E.row_off[req]);
+            if (pos >= 0 && pos < E.cap) {
+              T* dst = cache + (((size_t)req * E.n_kv + head) * E.cap + pos) * E.head_dim + ii;
+              if ((reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+                st4(dst, v[0], v[1], v[2], v[3]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = from_f32<T>(v[e]);
+              }
+            }
+          }
         }
         break;
       }
@@ -1057,7 +1151,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       // all its contributors.  Each posts its partial sums (c_first too) in
       // a first pass over its tiles, then finishes its share of the tile's rows
       // from all the slots in a second pass (below).
-      const bool bphase = kMulti && !fused_tk && E.kind != EPI_KV;
+      const bool bphase = kMulti && !fused_tk;
       while (u < u_end) {
         const int acc = tile_i & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_i >> 1) & 1u;
@@ -1291,7 +1385,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                    reinterpret_cast<uintptr_t>(E.gain);
           const bool vec_ok = (E.N_feat % kTileN) == 0 && (E.ldo & 3) == 0 &&
                               (ptr_or & 15) == 0 &&
-                              (E.kind != EPI_QKV || (E.head_dim & 7) == 0);
+                              (E.kind != EPI_QKV || (E.head_dim & 7) == 0) &&
+                              (E.kind != EPI_KV || ((E.head_dim & 7) == 0 &&
+                                                    (E.n_kv * E.head_dim) % kTileN == 0));
           if (vec_ok && share_in <= SL.bar_off) {
             if (!scales_once) ptx::named_bar_sync(1, kEpiThreads);   // s_scale written
             if (!epi_share_smem<T>(E, smem, sbar, sphase, slots, nslots, p.n_tile,

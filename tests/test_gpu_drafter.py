@@ -72,6 +72,11 @@ def _i32(a):
     (0, [5, 3], [10, 60]),            # fp32: two requests, ragged
     (1, [16], [2032]),                # 4B shape: one cycle's worth at the tail
     (1, [7, 16, 1], [0, 100, 2047]),  # ragged rows, last slot of the cache
+    # 256-row tiles (a batch's injection): 320 rows over 20 requests, and 700
+    # rows in three tiles (the last ragged), split tiles finished by all their
+    # contributors
+    (1, [16] * 20, [97 * i % 2000 for i in range(20)]),
+    (1, [100, 250, 350], [0, 500, 1600]),
 ])
 def test_inject_matches_oracle(wid, rows_per_req, pos0):
     wl = WORKLOADS[wid]
