@@ -1572,6 +1572,20 @@ TcPlan tc_plan(int M_rows, int N_feat, int K, int grid, int tk_kpad) {
   pl.total_units = (long long)pl.n_ftiles * pl.n_rtiles * pl.kblocks;
   pl.grid = static_cast<int>(pl.total_units < grid ? pl.total_units : grid);
   if (pl.grid < 1) pl.grid = 1;
+  // Several row tiles (compute-bound tiles of up to 256 rows): where a grid
+  // of at least five sixths of the SMs gives every CTA whole half tiles, use
+  // it -- split tiles then have two contributors at most, each ending on the
+  // half-tile boundary, or none, which shortens the finish after the MMAs
+  // more than the idle SMs lengthen them.
+  if (pl.n_rtiles > 1 && pl.kblocks >= 2 && pl.kblocks % 2 == 0) {
+    const long long half = pl.kblocks / 2;
+    for (int g = pl.grid; g >= (5 * pl.grid + 5) / 6; --g) {
+      if (pl.total_units % g == 0 && (pl.total_units / g) % half == 0) {
+        pl.grid = g;
+        break;
+      }
+    }
+  }
   const int n_tiles = pl.n_ftiles * pl.n_rtiles;
   int ms = 1;
   for (int t = 0; t < n_tiles; ++t) {
