@@ -18,10 +18,17 @@
 // MMA), the context split into chunks of 128-key tiles so the grid is about
 // one wave, and the tree's own keys as the last tiles of the last chunk.  Each
 // CTA posts an unnormalised partial (O, max, sum) of its rows; the last CTA of
-// a (query tile, KV head) to finish merges the others' partials into its own
-// and writes the bf16 rows (an arrival counter, no waiting).  Nodes are numbered in pop
-// order, so an ancestor has a smaller number than its descendant: the tree
-// tiles of query tile qt hold keys 0 .. 32 qt + 31 only.
+// a (query tile, KV head) to finish merges every chunk's partial, in chunk
+// order, and writes the bf16 rows (an arrival counter, no waiting).  Nodes are
+// numbered in pop order, so an ancestor has a smaller number than its
+// descendant: the tree tiles of query tile qt hold keys 0 .. 32 qt + 31 only.
+//
+// Block mode (the drafter's attention of "DFlash: Block Diffusion for Flash
+// Speculative Decoding", section 3.4.4, for batches): the L <= 32 block rows
+// take the place of a query tile's nodes (rows L .. 31 of each head are dead),
+// every block key is visible to every row (the anchor row only its own key
+// when the anchor is isolated), each request's context ends at its own length,
+// and the block keys ride in the chunk holding that end; later chunks exit.
 //
 // Per CTA, on the 5th-generation tensor cores (accumulators in TMEM):
 //   S_t  = Q K_t^T      A = Q (K-major), B = K tile (K-major), S in TMEM
