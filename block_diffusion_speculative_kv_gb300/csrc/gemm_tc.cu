@@ -14,7 +14,13 @@
 // is split over several CTAs is finished by the CTA holding its first K blocks
 // (they end that CTA's range, so it is among the last to get there): the
 // others post fp32 partial sums and a release-add on the tile's counter, and
-// it adds them, in a fixed order, to its own accumulator.
+// it adds them, in a fixed order, to its own accumulator.  With row tiles of
+// 32..256 rows (the kMulti instantiation) every contributor of a split tile
+// posts its partial sums and then finishes a share of the tile's rows from all
+// slots, in slot order; tiles run row-tile-major (tile t is row tile
+// t / n_ftiles), so the grid's halves read each weight tile at the same time
+// for different row tiles; and a phase takes a slightly smaller grid where
+// that gives every CTA whole half tiles (tc_plan).
 //
 // Chains.  One launch runs up to kMaxPhases dependent GEMMs ("phases", e.g.
 // W_o -> W_gate|up -> W_down -> next layer's W_qkv), each GEMM's activations
