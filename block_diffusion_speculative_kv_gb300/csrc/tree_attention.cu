@@ -679,8 +679,13 @@ dflash_status launch_block_attention_tc(const AttnParams& p, int* arrivals, int*
                      "block attention: needs G <= 4, L <= 32 and chunks of 128-key tiles");
   const long long kv_rows = (long long)p.n_req * p.n_kv * p.cap;
   const long long blk_rows = (long long)p.n_req * p.L;
-  if (kv_rows >= (1ll << 31) || blk_rows >= (1ll << 31) || p.qkv_ld % 8)
-    return set_error(DFLASH_ERR_UNSUPPORTED, "block attention: cache rows exceed 2^31");
+  if (kv_rows >= (1ll << 31) || blk_rows >= (1ll << 31))
+    return set_error(DFLASH_ERR_UNSUPPORTED, "block attention: cache or block rows exceed 2^31");
+  if (p.qkv_ld % 8 || (reinterpret_cast<uintptr_t>(p.qkv) & 15) ||
+      ((reinterpret_cast<uintptr_t>(p.cache_k) | reinterpret_cast<uintptr_t>(p.cache_v)) & 15))
+    return set_error(DFLASH_ERR_UNSUPPORTED,
+                     "block attention: the QKV row stride must be a multiple of 8 and the QKV "
+                     "and cache buffers 16-byte aligned");
   TreeTcParams tp{};
   tp.a = p;
   tp.a.n_qt = 1;
